@@ -1,0 +1,360 @@
+"""Benchmark of the grouped-conv weight gradient on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-extra]
+
+A step is one call of wg_conv_bwd_weight -- the whole path: every launch it makes
+(split-K stage 1, the stage-2 reduce or the atomic-mode memset) -- over one batch
+of synthetic, seeded inputs already resident in HBM.  The headline workload is
+the 2-D dense 56x56, C = K = 64, N = 32, 3x3 problem with bf16 inputs and bf16
+dW; the other workloads are reported under "workloads".  L2 is flushed (a 256 MiB
+write) before every timed step, outside the timed events.
+
+Prints one JSON line on rank 0.  Multi-GPU runs (torchrun) are independent
+replicas (weak scaling): the path has no exchange step on one node.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from implicit_gemm_gb300 import binding, build, synth  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20
+
+
+def spec(ndim, G, N, C, K, inn, filt, stride, dil, pl, pr, in_dtype, out_dtype):
+    return {"ndim": ndim, "G": G, "N": N, "C": C, "K": K, "in": inn, "filt": filt, "stride": stride, "dil": dil,
+            "pad_l": pl, "pad_r": pr, "in_dtype": in_dtype, "out_dtype": out_dtype}
+
+
+# name -> (spec, distribution, seed index, split_k, mode, group_merge)
+WORKLOADS = {
+    "2d_dense_n32_h56_c64_k64": (spec(2, 1, 32, 64, 64, [56, 56], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16",
+                                      "bf16"), ("uniform", -1.0, 1.0), 2, 0, "auto", 0),
+    "2d_tiny_n1_h8_c16_k32": (spec(2, 1, 1, 16, 32, [8, 8], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16", "fp32"),
+                              ("uniform", -1.0, 1.0), 1, 0, "auto", 0),
+    "2d_grouped_g32_c8_k8_n32_h28": (spec(2, 32, 32, 8, 8, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16",
+                                          "fp32"), ("normal", 0.0, 1.0), 3, 0, "auto", 0),
+    "2d_depthwise_g512_n64_h28": (spec(2, 512, 64, 1, 1, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16",
+                                       "fp32"), ("uniform", -1.0, 1.0), 4, 0, "auto", 8),
+    "3d_n4_d16_c128_k96_s2": (spec(3, 1, 4, 128, 96, [16, 16, 16], [3, 3, 3], [2, 2, 2], [1, 1, 1], [1, 1, 1],
+                                   [1, 1, 1], "fp16", "fp32"), ("normal", 0.0, 0.5), 5, 8, "atomic", 0),
+}
+HEADLINE = "2d_dense_n32_h56_c64_k64"
+
+
+def out_dims(sp):
+    return binding.wg_problem_normalize(sp)
+
+
+def sizes(sp):
+    o = out_dims(sp)
+    T = int(np.prod(sp["filt"]))
+    P = sp["N"] * int(np.prod(o))
+    nx = sp["N"] * int(np.prod(sp["in"])) * sp["G"] * sp["C"]
+    ndy = P * sp["G"] * sp["K"]
+    ndw = sp["G"] * sp["K"] * T * sp["C"]
+    flops = 2.0 * sp["G"] * sp["K"] * sp["C"] * T * P
+    wsz = 4 if sp["out_dtype"] == "fp32" else 2
+    return {"out": o, "nx": nx, "ndy": ndy, "ndw": ndw, "flops": flops,
+            "bytes": 2.0 * nx + 2.0 * ndy + float(wsz) * ndw, "wsz": wsz}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return {"hbm": float(d["hbm_gbs"]), "bf16": float(d["bf16_tflops"]),
+                "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "src": "measured"}
+    except Exception:
+        return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "src": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, ws, rank):
+    """Reference arm: the fp64 CPU oracle, as it stands, on this host's cores."""
+    import oracle  # the one other place the bench runs the oracle
+    if rank != 0:
+        return
+    sp = dict(WORKLOADS[args.workload][0])
+    # A bounded sample of the workload: 2 of the batch's images per step.
+    nsample = min(2, sp["N"])
+    sps = dict(sp, N=nsample)
+    dist, seed = WORKLOADS[args.workload][1], WORKLOADS[args.workload][2]
+    s = sizes(sps)
+    x = oracle.decode(synth.tensor_bits(1000 + seed, s["nx"], sp["in_dtype"], *dist), sp["in_dtype"])
+    dy = oracle.decode(synth.tensor_bits(2000 + seed, s["ndy"], sp["in_dtype"], *dist), sp["in_dtype"])
+    for _ in range(args.warmup):
+        oracle.wgrad(sps, x, dy)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.wgrad(sps, x, dy)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = s["flops"] / dt / 1e12
+    line = {"impl": "reference", "metric": "wgrad TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": args.workload, "sample_images": nsample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+                             "sample": f"{nsample} of {sp['N']} images of {args.workload} per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(name):
+    """The oracle timed on this host's cores on the full workload (about a second per run)."""
+    import oracle
+    sp, dist, seed = WORKLOADS[name][0], WORKLOADS[name][1], WORKLOADS[name][2]
+    s = sizes(sp)
+    x = oracle.decode(synth.tensor_bits(1000 + seed, s["nx"], sp["in_dtype"], *dist), sp["in_dtype"])
+    dy = oracle.decode(synth.tensor_bits(2000 + seed, s["ndy"], sp["in_dtype"], *dist), sp["in_dtype"])
+    runs, t0 = 0, time.perf_counter()
+    while runs < 1 or time.perf_counter() - t0 < 1.5:
+        oracle.wgrad(sp, x, dy)
+        runs += 1
+    dt = (time.perf_counter() - t0) / runs
+    return {"value": s["flops"] / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"full {name} workload, {runs} run(s), fp64 direct loop with |dY*X| sums"}
+
+
+class Workload:
+    def __init__(self, torch, name):
+        self.torch = torch
+        self.name = name
+        sp, dist, seed, self.split_k, self.mode, self.gm = WORKLOADS[name]
+        self.sp = sp
+        self.s = sizes(sp)
+        tdt = torch.bfloat16 if sp["in_dtype"] == "bf16" else torch.float16
+        xb = synth.tensor_bits(1000 + seed, self.s["nx"], sp["in_dtype"], *dist)
+        dyb = synth.tensor_bits(2000 + seed, self.s["ndy"], sp["in_dtype"], *dist)
+        self.x_host = torch.from_numpy(xb.view(np.int16)).view(tdt).pin_memory()
+        self.dy_host = torch.from_numpy(dyb.view(np.int16)).view(tdt).pin_memory()
+        self.x = self.x_host.cuda()
+        self.dy = self.dy_host.cuda()
+        odt = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}[sp["out_dtype"]]
+        self.dw = torch.empty(self.s["ndw"], dtype=odt, device="cuda")
+        self.dw_host = torch.empty(self.s["ndw"], dtype=odt).pin_memory()
+        self.ws_bytes = binding.wg_workspace_size(sp, self.split_k, self.mode, self.gm)
+        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device="cuda")
+        self.plan = binding.wg_plan_string(sp, self.split_k, self.mode, self.gm)
+        self.launches_per_step = 1 + (1 if "mode=deterministic" in self.plan else 0)
+
+    def step(self, stream):
+        binding.wg_conv_bwd_weight(self.sp, self.x, self.dy, self.dw, self.split_k, self.mode, self.gm, self.ws,
+                                   self.ws_bytes, stream)
+
+    def e2e_step(self, stream):
+        self.x.copy_(self.x_host, non_blocking=True)
+        self.dy.copy_(self.dy_host, non_blocking=True)
+        self.step(stream)
+        self.dw_host.copy_(self.dw, non_blocking=True)
+
+
+def time_steps(torch, wl, steps, warmup, flush, stream, e2e=False):
+    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each step."""
+    fn = wl.e2e_step if e2e else wl.step
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.zero_()
+            fn(stream)
+        stream.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fn(stream)
+            b.record(stream)
+        stream.synchronize()
+    binding.wg_check_status(stream)
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=list(WORKLOADS))
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads and the CPU baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device: the wgrad path has no CPU fallback")
+    torch.cuda.set_device(local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    build.build()
+    binding.load()
+    stream = torch.cuda.Stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    pk = peaks()
+
+    wl = Workload(torch, args.workload)
+    sampler = ClockSampler(local)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    t_wall = time.perf_counter()
+    times = time_steps(torch, wl, args.steps, args.warmup, flush, stream)
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    torch.cuda.synchronize()
+    step_ms = float(np.mean(times))
+    if pg:
+        t = torch.tensor([step_ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        step_ms = float(t.item())
+        pg.barrier()
+    s = wl.s
+    value = ws * s["flops"] / (step_ms * 1e-3) / 1e12
+
+    # End to end through the same C ABI call, host buffers: H2D of X and dY from
+    # pinned memory, the call, D2H of dW, all inside the timed events.
+    e2e_times = time_steps(torch, wl, max(20, args.steps // 10), args.warmup, flush, stream, e2e=True)
+    e2e_ms = float(np.mean(e2e_times))
+    if pg:
+        t = torch.tensor([e2e_ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # Roofline of the step on its dominant kernel: algorithmic FLOPs and bytes of
+    # one launch over the measured step time; the bound is the slower of the two.
+    t_flop = s["flops"] / (pk["bf16"] * 1e12)
+    t_byte = s["bytes"] / (pk["hbm"] * 1e9)
+    if t_byte >= t_flop:
+        roof = {"bound": "hbm", "achieved": s["bytes"] / (step_ms * 1e-3) / 1e9, "peak": pk["hbm"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": s["flops"] / (step_ms * 1e-3) / 1e12, "peak": pk["bf16"],
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["peak_source"] = pk["src"]
+    roof["kernel"] = "igemm_wgrad_kernel" if "igemm" in wl.plan else "depthwise_wgrad_kernel"
+    roof["timed"] = "whole step (all launches of the call) with CUDA events"
+
+    extra = {}
+    if rank == 0 and not args.no_extra:
+        for name in WORKLOADS:
+            if name == args.workload:
+                continue
+            w2 = Workload(torch, name)
+            tt = time_steps(torch, w2, 300, 10, flush, stream)
+            ms = float(np.mean(tt))
+            s2 = w2.s
+            tf, tb = s2["flops"] / (pk["bf16"] * 1e12), s2["bytes"] / (pk["hbm"] * 1e9)
+            extra[name] = {"ms_per_step": ms, "tflops": s2["flops"] / (ms * 1e-3) / 1e12,
+                           "gbs": s2["bytes"] / (ms * 1e-3) / 1e9, "roofline_us": max(tf, tb) * 1e6,
+                           "bound": "hbm" if tb >= tf else "tensor",
+                           "roofline_frac": max(tf, tb) / (ms * 1e-3), "plan": w2.plan}
+            del w2
+
+    if rank == 0:
+        line = {"metric": "wgrad TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16" if wl.sp["in_dtype"] == "bf16" else "fp16",
+                "data": "synthetic (seeded splitmix64)",
+                "config": {"workload": args.workload, "G": wl.sp["G"], "N": wl.sp["N"], "in": wl.sp["in"],
+                           "C": wl.sp["C"], "K": wl.sp["K"], "filt": wl.sp["filt"], "stride": wl.sp["stride"],
+                           "pad": wl.sp["pad_l"], "in_dtype": wl.sp["in_dtype"], "out_dtype": wl.sp["out_dtype"],
+                           "split_k": wl.split_k, "mode": wl.mode, "plan": wl.plan,
+                           "l2": "flushed by a 256 MiB write before every timed step (outside the events)",
+                           "parallelism": f"replicas x{ws}"},
+                "roofline": roof, "clocks": clocks, "gpu_launches": wl.launches_per_step * args.steps,
+                "e2e": {"value": ws * s["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                        "h2d_bytes_per_step": 2 * (s["nx"] + s["ndy"]), "d2h_bytes_per_step": s["wsz"] * s["ndw"],
+                        "ms_per_step": e2e_ms},
+                "wall_s_timed": t_wall, "workloads": extra}
+        if ws == 1 and not args.no_extra:
+            line["cpu_baseline"] = cpu_baseline(args.workload)
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,184 @@
+"""ctypes binding of libwgrad.so (include/wgrad.h).  Argument marshalling only.
+
+Every function here has the name of the C entry point it calls.  Tensors may be
+torch tensors (their data_ptr() is passed) or plain integer device addresses.
+The library must have been built (``python -m implicit_gemm_gb300.build``);
+loading raises if it is missing -- there is no other code path.
+
+A problem spec is a dict: ndim, G, N, C, K, and per-dim lists in, filt,
+stride, dil, pad_l, pad_r (ndim entries, outermost first), plus in_dtype
+('bf16' | 'fp16') and out_dtype ('fp32' | 'bf16' | 'fp16').
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+DTYPES = {"bf16": 0, "fp16": 1, "fp32": 2}
+MODES = {"auto": 0, "direct": 1, "atomic": 2, "deterministic": 3}
+STATUS = {0: "WG_OK", 1: "WG_ERR_INVALID_ARGUMENT", 2: "WG_ERR_NOT_SUPPORTED", 3: "WG_ERR_MISALIGNED",
+          4: "WG_ERR_WORKSPACE", 5: "WG_ERR_CUDA", 6: "WG_ERR_DEVICE_TIMEOUT"}
+
+
+class WgProblem(ctypes.Structure):
+    _fields_ = [("ndim", ctypes.c_int), ("G", ctypes.c_int), ("N", ctypes.c_int), ("C", ctypes.c_int),
+                ("K", ctypes.c_int), ("in_", ctypes.c_int * 3), ("filt", ctypes.c_int * 3),
+                ("out", ctypes.c_int * 3), ("stride", ctypes.c_int * 3), ("dil", ctypes.c_int * 3),
+                ("pad_l", ctypes.c_int * 3), ("pad_r", ctypes.c_int * 3), ("in_dtype", ctypes.c_int),
+                ("out_dtype", ctypes.c_int)]
+
+
+class WgOptions(ctypes.Structure):
+    _fields_ = [("split_k", ctypes.c_int), ("mode", ctypes.c_int), ("group_merge", ctypes.c_int)]
+
+
+class WgradError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+EXPORTS = ("wg_problem_normalize", "wg_workspace_size", "wg_conv_bwd_weight", "wg_check_status",
+           "wg_plan_string", "wg_status_string", "wg_last_error")
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libwgrad.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError(f"libwgrad.so not found at {_build.LIB}; build it with "
+                                   "`python -m implicit_gemm_gb300.build` (needs nvcc)")
+            lib = ctypes.CDLL(_build.LIB)
+            P, O = ctypes.POINTER(WgProblem), ctypes.POINTER(WgOptions)
+            lib.wg_problem_normalize.argtypes = [P]
+            lib.wg_workspace_size.argtypes = [P, O, ctypes.POINTER(ctypes.c_size_t)]
+            lib.wg_conv_bwd_weight.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, O,
+                                               ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+            lib.wg_check_status.argtypes = [ctypes.c_void_p]
+            lib.wg_plan_string.argtypes = [P, O, ctypes.c_char_p, ctypes.c_size_t]
+            lib.wg_status_string.argtypes = [ctypes.c_int]
+            lib.wg_status_string.restype = ctypes.c_char_p
+            lib.wg_last_error.restype = ctypes.c_char_p
+            for name in EXPORTS:
+                if name not in ("wg_status_string", "wg_last_error"):
+                    getattr(lib, name).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _check(st: int):
+    if st != 0:
+        raise WgradError(st, load().wg_last_error().decode())
+
+
+def make_problem(spec: dict) -> WgProblem:
+    p = WgProblem()
+    nd = spec["ndim"]
+    p.ndim, p.G, p.N, p.C, p.K = nd, spec["G"], spec["N"], spec["C"], spec["K"]
+    for key, field, default in (("in", "in_", 1), ("filt", "filt", 1), ("stride", "stride", 1),
+                                ("dil", "dil", 1), ("pad_l", "pad_l", 0), ("pad_r", "pad_r", 0),
+                                ("out", "out", 0)):
+        vals = list(spec.get(key, [default] * max(nd, 0)))
+        arr = getattr(p, field)
+        for i in range(3):
+            arr[i] = vals[i] if i < min(nd, len(vals)) else 0
+    p.in_dtype = DTYPES[spec.get("in_dtype", "bf16")]
+    p.out_dtype = DTYPES[spec.get("out_dtype", "fp32")]
+    return p
+
+
+def make_options(split_k: int = 0, mode: str = "auto", group_merge: int = 0) -> WgOptions:
+    return WgOptions(int(split_k), MODES[mode], int(group_merge))
+
+
+def _addr(t) -> int:
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    return int(t.data_ptr())
+
+
+def wg_problem_normalize(spec: dict) -> list:
+    """Derived output lengths (ndim entries)."""
+    p = make_problem(spec)
+    _check(load().wg_problem_normalize(ctypes.byref(p)))
+    return [p.out[i] for i in range(spec["ndim"])]
+
+
+def wg_workspace_size(spec: dict, split_k: int = 0, mode: str = "auto", group_merge: int = 0) -> int:
+    p, o, n = make_problem(spec), make_options(split_k, mode, group_merge), ctypes.c_size_t(0)
+    _check(load().wg_workspace_size(ctypes.byref(p), ctypes.byref(o), ctypes.byref(n)))
+    return int(n.value)
+
+
+def wg_plan_string(spec: dict, split_k: int = 0, mode: str = "auto", group_merge: int = 0) -> str:
+    p, o = make_problem(spec), make_options(split_k, mode, group_merge)
+    buf = ctypes.create_string_buffer(2048)
+    _check(load().wg_plan_string(ctypes.byref(p), ctypes.byref(o), buf, len(buf)))
+    return buf.value.decode()
+
+
+def wg_conv_bwd_weight(spec: dict, x, dy, dw, split_k: int = 0, mode: str = "auto", group_merge: int = 0,
+                       workspace=None, ws_bytes: int | None = None, stream=None) -> None:
+    """Launch the weight gradient on `stream` (torch stream, raw handle int, or None for
+    torch's current stream when torch is loaded, else the legacy default stream)."""
+    p, o = make_problem(spec), make_options(split_k, mode, group_merge)
+    if ws_bytes is None:
+        ws_bytes = 0 if workspace is None else (workspace.numel() * workspace.element_size()
+                                                if hasattr(workspace, "numel") else 0)
+    _check(load().wg_conv_bwd_weight(ctypes.byref(p), _addr(x), _addr(dy), _addr(dw), ctypes.byref(o),
+                                     _addr(workspace), int(ws_bytes), _stream_handle(stream)))
+
+
+def wg_check_status(stream=None) -> None:
+    _check(load().wg_check_status(_stream_handle(stream)))
+
+
+def wg_status_string(status: int) -> str:
+    return load().wg_status_string(int(status)).decode()
+
+
+def wg_last_error() -> str:
+    return load().wg_last_error().decode()
+
+
+def _stream_handle(stream):
+    if stream is None:
+        try:
+            import torch
+            if torch.cuda.is_available() and torch.cuda.is_initialized():
+                return int(torch.cuda.current_stream().cuda_stream)
+        except Exception:  # pragma: no cover - torch missing
+            pass
+        return None
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def conv_bwd_weight(spec: dict, x, dy, split_k: int = 0, mode: str = "auto", group_merge: int = 0, out=None,
+                    stream=None):
+    """Convenience wrapper over wg_conv_bwd_weight for torch CUDA tensors: allocates dW
+    (G, K, *filt, C) in spec['out_dtype'] and the workspace it needs with torch, then calls
+    the library."""
+    import torch
+    tdt = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}[spec.get("out_dtype", "fp32")]
+    if out is None:
+        out = torch.empty((spec["G"], spec["K"], *spec["filt"], spec["C"]), dtype=tdt, device=x.device)
+    nbytes = wg_workspace_size(spec, split_k, mode, group_merge)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=x.device) if nbytes else None
+    wg_conv_bwd_weight(spec, x, dy, out, split_k, mode, group_merge, ws, nbytes, stream)
+    return out

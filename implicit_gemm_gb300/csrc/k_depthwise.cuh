@@ -1,0 +1,243 @@
+// Depthwise (C = K = 1 per group) weight gradient on CUDA cores.
+//
+//     dW[g, tap] = sum over pixels p of dY[p, g] * X[p shifted by tap, g]
+//
+// A depthwise group makes both implicit-GEMM operands single channels, so the
+// per-group GEMM is 1 x YX x N*Ho*Wo: no dense contraction is left for the
+// tensor cores.  Following the group-merge idea of PR #12359 ("add group
+// merging (Gm) for depthwise grouped conv"), Gm adjacent groups are handled
+// together so that the channel run -- contiguous in NHWGC / NHWGK -- becomes
+// the vector axis: each thread owns Gm consecutive channels (a 2*Gm-byte
+// vector) and all YX taps of them.  Merging divides the parallelism by Gm and
+// the pixel split (the "split-K" of this kernel) multiplies it back.
+//
+// A CTA owns CB channels and a slice of (n, row-strip) tiles.  A producer warp
+// streams each tile's X rows (with halo, zero-filled outside the image by TMA)
+// and dY rows into a shared-memory ring; compute threads (channel vector,
+// output row, column segment) accumulate in registers, then reduce over the
+// CTA through shared memory and over splits via atomics or the workspace.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace wg {
+
+struct DwParams {
+    int G, Ho, Wo, Y, X, T;
+    int sh, sw, dh, dw, plh, plw;
+    int CB, R, nseg, seg_len, nused;
+    int xw, xh, n_hstrips, per_split, total_tiles;
+    int stages, x_bytes_al, stage_bytes, x_tx, dy_tx;
+    int mode, out_dtype;
+    void* out;
+    long long split_stride;
+};
+
+template <bool BF16, int GM>
+struct VecLoad;
+
+template <bool BF16>
+__device__ __forceinline__ void cvt2(uint32_t u, float& a, float& b)
+{
+    if (BF16) {
+        a = __uint_as_float(u << 16);
+        b = __uint_as_float(u & 0xFFFF0000u);
+    } else {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u));
+        a = f.x;
+        b = f.y;
+    }
+}
+
+template <bool BF16, int GM>
+__device__ __forceinline__ void load_vec(const uint16_t* p, float (&v)[GM])
+{
+    if constexpr (GM == 8) {
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
+        cvt2<BF16>(u.x, v[0], v[1]);
+        cvt2<BF16>(u.y, v[2], v[3]);
+        cvt2<BF16>(u.z, v[4], v[5]);
+        cvt2<BF16>(u.w, v[6], v[7]);
+    } else if constexpr (GM == 4) {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        cvt2<BF16>(u.x, v[0], v[1]);
+        cvt2<BF16>(u.y, v[2], v[3]);
+    } else if constexpr (GM == 2) {
+        cvt2<BF16>(*reinterpret_cast<const uint32_t*>(p), v[0], v[1]);
+    } else {
+        const uint32_t u = *p;
+        float dummy;
+        cvt2<BF16>(u, v[0], dummy);
+        (void)dummy;
+    }
+}
+
+template <bool BF16, int GM, bool SLIDE3>
+__global__ void __launch_bounds__(288, 1)
+    depthwise_wgrad_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
+                           const __grid_constant__ DwParams p)
+{
+    constexpr int MAXT = 9;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int nthreads = blockDim.x - 32;
+    const int red_bytes = nthreads * p.T * GM * 4;
+    uint8_t* tail = smem + max(p.stages * p.stage_bytes, red_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(tail);
+    uint64_t* empty = full + 8;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cb = blockIdx.x, split = blockIdx.y;
+    const int t0 = split * p.per_split;
+    const int ntl = max(0, min(p.per_split, p.total_tiles - t0));
+    const int n_cwarps = nthreads >> 5;
+
+    if (tid == 0) {
+        for (int i = 0; i < p.stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], (uint32_t)n_cwarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    float acc[MAXT][GM];
+#pragma unroll
+    for (int t = 0; t < MAXT; ++t)
+#pragma unroll
+        for (int j = 0; j < GM; ++j) acc[t][j] = 0.f;
+
+    const int NV = p.CB / GM;
+    if (warp == n_cwarps) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            tma_prefetch_desc(&tmx);
+            tma_prefetch_desc(&tmy);
+            for (int i = 0; i < ntl; ++i) {
+                const int st = i % p.stages;
+                const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
+                if (i >= p.stages && !mbar_wait(&empty[st], ph ^ 1u)) break;
+                const int tile = t0 + i;
+                const int n = tile / p.n_hstrips;
+                const int ho0 = (tile - n * p.n_hstrips) * p.R;
+                uint8_t* sb = smem + st * p.stage_bytes;
+                mbar_arrive_expect_tx(&full[st], (uint32_t)(p.x_tx + p.dy_tx));
+                tma_load_5d(sb, &tmx, &full[st], cb * p.CB, -p.plw, ho0 * p.sh - p.plh, 0, n);
+                tma_load_5d(sb + p.x_bytes_al, &tmy, &full[st], cb * p.CB, 0, ho0, 0, n);
+            }
+        }
+    } else {
+        // ------------------------------------------------ compute threads
+        const bool active = tid < p.nused;
+        const int v = tid % NV, rest = tid / NV;
+        const int seg = rest % p.nseg, r = rest / p.nseg;
+        const int wo_a = seg * p.seg_len, wo_b = min(p.Wo, wo_a + p.seg_len);
+        int tap_off[MAXT];
+#pragma unroll
+        for (int t = 0; t < MAXT; ++t) {
+            const int tt = t < p.T ? t : 0;
+            const int ty = tt / p.X, tx = tt - (tt / p.X) * p.X;
+            tap_off[t] = (ty * p.dh * p.xw + tx * p.dw) * p.CB;
+        }
+        for (int i = 0; i < ntl; ++i) {
+            const int st = i % p.stages;
+            const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
+            if (!mbar_wait(&full[st], ph)) break;
+            const int tile = t0 + i;
+            const int n = tile / p.n_hstrips;
+            const int ho0 = (tile - n * p.n_hstrips) * p.R;
+            if (active && ho0 + r < p.Ho && wo_a < wo_b) {
+                const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + st * p.stage_bytes);
+                const uint16_t* ys = reinterpret_cast<const uint16_t*>(smem + st * p.stage_bytes + p.x_bytes_al);
+                const int cv = v * GM;
+                if constexpr (SLIDE3) {
+                    // 3x3 filter, stride 1 and dilation 1 along W: keep a 3x3
+                    // window of X vectors in registers, one new column per pixel.
+                    const uint16_t* xr[3];
+#pragma unroll
+                    for (int y = 0; y < 3; ++y) xr[y] = xs + (r * p.sh + y * p.dh) * p.xw * p.CB + cv;
+                    float w[3][3][GM];
+#pragma unroll
+                    for (int y = 0; y < 3; ++y) {
+                        load_vec<BF16, GM>(xr[y] + (wo_a + 0) * p.CB, w[y][0]);
+                        load_vec<BF16, GM>(xr[y] + (wo_a + 1) * p.CB, w[y][1]);
+                    }
+                    const uint16_t* yr = ys + (r * p.Wo) * p.CB + cv;
+                    for (int wo = wo_a; wo < wo_b; ++wo) {
+#pragma unroll
+                        for (int y = 0; y < 3; ++y) load_vec<BF16, GM>(xr[y] + (wo + 2) * p.CB, w[y][2]);
+                        float dy[GM];
+                        load_vec<BF16, GM>(yr + wo * p.CB, dy);
+#pragma unroll
+                        for (int y = 0; y < 3; ++y)
+#pragma unroll
+                            for (int x = 0; x < 3; ++x)
+#pragma unroll
+                                for (int j = 0; j < GM; ++j) acc[y * 3 + x][j] = fmaf(dy[j], w[y][x][j], acc[y * 3 + x][j]);
+#pragma unroll
+                        for (int y = 0; y < 3; ++y)
+#pragma unroll
+                            for (int j = 0; j < GM; ++j) {
+                                w[y][0][j] = w[y][1][j];
+                                w[y][1][j] = w[y][2][j];
+                            }
+                    }
+                } else {
+                    for (int wo = wo_a; wo < wo_b; ++wo) {
+                        float dy[GM];
+                        load_vec<BF16, GM>(ys + (r * p.Wo + wo) * p.CB + cv, dy);
+                        const uint16_t* xb = xs + ((r * p.sh) * p.xw + wo * p.sw) * p.CB + cv;
+#pragma unroll
+                        for (int t = 0; t < MAXT; ++t) {
+                            if (t < p.T) {
+                                float xv[GM];
+                                load_vec<BF16, GM>(xb + tap_off[t], xv);
+#pragma unroll
+                                for (int j = 0; j < GM; ++j) acc[t][j] = fmaf(dy[j], xv[j], acc[t][j]);
+                            }
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+    }
+    __syncthreads();
+    // ---------------------------------------------------- reduce over the CTA
+    float* red = reinterpret_cast<float*>(smem);
+    if (tid < p.nused) {
+        const int slot = tid / NV, v = tid % NV;
+#pragma unroll
+        for (int t = 0; t < MAXT; ++t)
+            if (t < p.T)
+#pragma unroll
+                for (int j = 0; j < GM; ++j) red[(slot * p.T + t) * p.CB + v * GM + j] = acc[t][j];
+    }
+    __syncthreads();
+    const int nslots = p.R * p.nseg;
+    for (int idx = tid; idx < p.T * p.CB; idx += blockDim.x) {
+        const int t = idx / p.CB, c = idx - t * p.CB;
+        float s = 0.f;
+        for (int sl = 0; sl < nslots; ++sl) s += red[(sl * p.T + t) * p.CB + c];
+        const int g = cb * p.CB + c;
+        if (g >= p.G) continue;
+        const long long o = (long long)g * p.T + t;
+        if (p.mode == 2) {
+            if (ntl > 0) red_add_f32(static_cast<float*>(p.out) + o, s);
+        } else if (p.mode == 3) {
+            static_cast<float*>(p.out)[split * p.split_stride + o] = s;
+        } else if (p.out_dtype == 2) {
+            static_cast<float*>(p.out)[o] = s;
+        } else if (p.out_dtype == 0) {
+            static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(s);
+        } else {
+            static_cast<__half*>(p.out)[o] = __float2half_rn(s);
+        }
+    }
+}
+
+}  // namespace wg

@@ -1,0 +1,469 @@
+// Problem normalisation and launch planning (host only).
+//
+// Normalisation follows the host-argument record of "Composable Kernel:
+// grouped_convolution_backward_weight_kernel.hpp Source File"
+// (GroupedConvBwdWeightHostArgs: G_, N_, C_, K_, spatial lengths, strides,
+// dilations, left/right pads).  That page takes the output lengths as an input;
+// here they are derived with the standard rule and a caller-supplied value must
+// agree with it.
+//
+// The implicit GEMM of that page (GemmM = K, GemmN = C*YX, GemmK = N*Ho*Wo,
+// batched over G) is planned with the roles of M and N swapped for the tensor
+// cores: MMA rows are (tap, channel) pairs -- the long axis -- and MMA columns
+// are output channels k.
+#include "plan.h"
+
+#include <algorithm>
+#include <array>
+#include <vector>
+#include <cmath>
+#include <cstdio>
+#include <cstdarg>
+#include <cstring>
+
+namespace wg {
+
+namespace {
+
+long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+int round_up(int a, int b) { return (int)cdiv(a, b) * b; }
+int pow2_at_least(int v)
+{
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+int fail(std::string* err, int status, const char* fmt, ...) __attribute__((format(printf, 3, 4)));
+int fail(std::string* err, int status, const char* fmt, ...)
+{
+    if (err) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        *err = buf;
+    }
+    return status;
+}
+
+// Candidate pixel tiles (w, h, d, n) for the tensor-core path: KT = product, a
+// multiple of 16 (the MMA K of kind::f16) and at most 256; each extent at most
+// the (rounded-up) output extent.  With w8 the w extent is a multiple of 8, so
+// that every 8-pixel K group is one contiguous run of a halo patch row.
+void enumerate_tiles(const Problem& pb, bool w8, std::vector<std::array<int, 4>>* out)
+{
+    const int Wo = pb.out[2], Ho = pb.out[1], Do = pb.out[0], N = pb.N;
+    const int lim_w = std::min(256 / pb.stride[2], round_up(Wo, w8 ? 8 : 16));
+    const int lim_h = std::min(256 / pb.stride[1], pow2_at_least(Ho));
+    const int lim_d = std::min(256 / pb.stride[0], pow2_at_least(Do));
+    const int lim_n = std::min(256, pow2_at_least(N));
+    out->clear();
+    for (int bw = w8 ? 8 : 1; bw <= lim_w; bw += w8 ? 8 : 1)
+        for (int bh = 1; bh <= lim_h && bw * bh <= 256; ++bh)
+            for (int bd = 1; bd <= lim_d && bw * bh * bd <= 256; ++bd)
+                for (int bn = 1; bn <= lim_n && bw * bh * bd * bn <= 256; ++bn)
+                    if ((bw * bh * bd * bn) % 16 == 0) out->push_back({bw, bh, bd, bn});
+}
+
+// Stride phases of one spatial dim: tap t reads input offset t*dil = q*stride + ph.
+struct DimPhases {
+    int nph;
+    int phval[8];
+    int phidx[kMaxHaloFilter];
+    int q[kMaxHaloFilter];
+    int qmax;
+};
+
+bool dim_phases(int F, int s, int d, DimPhases* o)
+{
+    if (F > kMaxHaloFilter || s > 8) return false;
+    bool used[8] = {false, false, false, false, false, false, false, false};
+    o->qmax = 0;
+    for (int t = 0; t < F; ++t) {
+        used[(t * d) % s] = true;
+        o->qmax = std::max(o->qmax, (t * d) / s);
+    }
+    o->nph = 0;
+    int idx_of[8];
+    for (int ph = 0; ph < s; ++ph)
+        if (used[ph]) idx_of[ph] = o->nph, o->phval[o->nph++] = ph;
+    for (int t = 0; t < F; ++t) o->phidx[t] = idx_of[(t * d) % s], o->q[t] = (t * d) / s;
+    return true;
+}
+
+struct IgCand {
+    int halo, box[4], nt[4], KT, mt, stages, stage_bytes, patch[3], patch_bytes, n_patches, dy_off;
+    long long cost;
+};
+
+int plan_igemm(Plan* pl, const wg_options& o, int num_sms, std::string* err)
+{
+    const Problem& pb = pl->pb;
+    IgemmPlan& ig = pl->ig;
+    std::memset(&ig, 0, sizeof ig);
+    for (int j = 0; j < 3; ++j)
+        if (pb.stride[j] > 8)
+            return fail(err, WG_ERR_NOT_SUPPORTED, "stride above 8 (TMA element strides are at most 8)");
+    // Channel / k windows.  A group whose first channel is not 8-aligned can
+    // start up to 7 channels into the window (TMA coordinates must be 16-byte aligned).
+    const int cmis = (pb.C % 8) ? 7 : 0, kmis = (pb.K % 8) ? 7 : 0;
+    int Gm = 1;
+    if (pb.C + cmis <= 64 && pb.K + kmis <= 256)
+        while (Gm < pb.G && (Gm + 1) * pb.C + cmis <= 64 && (Gm + 1) * pb.K + kmis <= 256) ++Gm;
+    ig.Gm = Gm;
+    ig.n_gblocks = (int)cdiv(pb.G, Gm);
+    if (ig.n_gblocks > 65535) return fail(err, WG_ERR_NOT_SUPPORTED, "too many group blocks (%d)", ig.n_gblocks);
+    ig.n_cchunks = (int)cdiv(Gm * pb.C + cmis, 64);
+    const int kwin = Gm * pb.K + kmis;
+    ig.n_ntiles = (int)cdiv(kwin, 256);
+    ig.Nt = round_up((int)cdiv(kwin, ig.n_ntiles), 16);
+    ig.n_katoms = (int)cdiv(ig.Nt, 64);
+    if (pb.T * ig.n_cchunks > (1 << 24)) return fail(err, WG_ERR_NOT_SUPPORTED, "filter too large");
+    ig.n_atoms = (int)(pb.T * ig.n_cchunks);
+    ig.n_mtiles = (int)cdiv(ig.n_atoms, 2);
+
+    // Stride phases per dim, in (w, h, d) order.
+    DimPhases ph[3];
+    bool halo_ok = ig.n_atoms <= kMaxHaloAtoms;
+    for (int i = 0; i < 3; ++i) halo_ok = dim_phases(pb.filt[2 - i], pb.stride[2 - i], pb.dil[2 - i], &ph[i]) && halo_ok;
+    const int n_combos = halo_ok ? ph[0].nph * ph[1].nph * ph[2].nph : 0;
+    if (halo_ok && n_combos * ig.n_cchunks > kMaxPatches) halo_ok = false;
+
+    const int avail = kMaxSmemPerCta - 3072;
+    const int mt_max = std::min(ig.n_mtiles, kMaxTmemCols / ig.Nt);
+    IgCand best{};
+    best.cost = -1;
+    std::vector<std::array<int, 4>> tiles;
+    for (int halo = halo_ok ? 1 : 0; halo >= 0; --halo) {
+        enumerate_tiles(pb, halo != 0, &tiles);
+        for (const auto& t : tiles) {
+            IgCand c{};
+            c.halo = halo;
+            for (int i = 0; i < 4; ++i) c.box[i] = t[i];
+            c.nt[0] = (int)cdiv(pb.out[2], c.box[0]);
+            c.nt[1] = (int)cdiv(pb.out[1], c.box[1]);
+            c.nt[2] = (int)cdiv(pb.out[0], c.box[2]);
+            c.nt[3] = (int)cdiv(pb.N, c.box[3]);
+            c.KT = c.box[0] * c.box[1] * c.box[2] * c.box[3];
+            const int slot = c.KT * 128;
+            if (halo) {
+                bool fits = true;
+                for (int i = 0; i < 3; ++i) {
+                    c.patch[i] = c.box[i] + ph[i].qmax;
+                    if (c.patch[i] * pb.stride[2 - i] > 256) fits = false;
+                }
+                if (!fits) continue;
+                const long long rows = (long long)c.patch[0] * c.patch[1] * c.patch[2] * c.box[3];
+                if (rows * 128 > avail) continue;
+                c.patch_bytes = round_up((int)(rows * 128), 1024);
+                c.n_patches = n_combos * ig.n_cchunks;
+            } else {
+                for (int i = 0; i < 3; ++i) c.patch[i] = c.box[i];
+                c.patch_bytes = slot;
+            }
+            const long long ktiles = (long long)c.nt[0] * c.nt[1] * c.nt[2] * c.nt[3];
+            for (int mt = mt_max; mt >= 1; --mt) {
+                const int n_x = halo ? c.n_patches : 2 * mt;
+                const long long stage = (long long)n_x * c.patch_bytes + (long long)ig.n_katoms * slot;
+                if (stage > avail) continue;
+                const int stages = std::min(8, (int)(avail / stage));
+                if (stages < 2) continue;
+                // Per K-tile and CTA: tensor-core cycles (M128 x N x K16 ~ N/2
+                // cycles) against shared-memory fill at ~64 B/cycle, plus a fixed
+                // overhead; fewer than 3 stages exposes latency.
+                const long long mranges = cdiv(ig.n_mtiles, mt);
+                const long long mma_clk = (long long)mt * (c.KT / 16) * (ig.Nt / 2);
+                const long long load_clk = stage / 64;
+                long long tile_clk = std::max(mma_clk, load_clk) + 64;
+                if (stages < 3) tile_clk = tile_clk * 13 / 10;
+                const long long cost = mranges * ig.n_ntiles * ig.n_gblocks * ktiles * tile_clk;
+                if (best.cost < 0 || cost < best.cost) {
+                    c.mt = mt;
+                    c.stages = stages;
+                    c.stage_bytes = (int)stage;
+                    c.dy_off = n_x * c.patch_bytes;
+                    c.cost = cost;
+                    best = c;
+                }
+                if (stages >= 3) break;  // smaller mt only re-reads more
+            }
+        }
+    }
+    if (best.cost < 0) return fail(err, WG_ERR_NOT_SUPPORTED, "no tile configuration fits shared memory");
+    ig.halo = best.halo;
+    std::memcpy(ig.box, best.box, sizeof best.box);
+    std::memcpy(ig.ntile, best.nt, sizeof best.nt);
+    std::memcpy(ig.patch, best.patch, sizeof best.patch);
+    ig.KT = best.KT;
+    ig.slot_bytes = best.KT * 128;
+    ig.patch_bytes = best.patch_bytes;
+    ig.n_mranges = (int)cdiv(ig.n_mtiles, best.mt);
+    ig.mt_per_cta = (int)cdiv(ig.n_mtiles, ig.n_mranges);
+    ig.n_patches = ig.halo ? best.n_patches : 2 * ig.mt_per_cta;
+    ig.dy_off = ig.n_patches * ig.patch_bytes;
+    ig.stage_bytes = ig.dy_off + ig.n_katoms * ig.slot_bytes;
+    ig.stages = std::min(8, avail / ig.stage_bytes);
+    // Stage buffers, then 1 KB of slack that a padding atom's reads may reach,
+    // then 1 KB of barriers and tables; plus 1 KB to align the base.
+    ig.smem_bytes = ig.stages * ig.stage_bytes + 3072;
+    ig.tmem_cols = std::max(32, pow2_at_least(ig.mt_per_cta * ig.Nt));
+    ig.total_kt = (long long)ig.ntile[0] * ig.ntile[1] * ig.ntile[2] * ig.ntile[3];
+    ig.est_cycles = best.cost / std::max(1, num_sms);
+    if (ig.total_kt > (1ll << 31) - 1) return fail(err, WG_ERR_NOT_SUPPORTED, "GemmK too large");
+    if (ig.halo) {
+        for (int i = 0; i < 3; ++i) ig.n_phase[i] = ph[i].nph;
+        // Patches in (phase d, phase h, phase w, chunk) order; atoms sorted by
+        // their offset in the stage so that the two atoms of an M-tile are a
+        // non-negative LBO apart.
+        int p = 0;
+        for (int a = 0; a < ph[2].nph; ++a)
+            for (int b = 0; b < ph[1].nph; ++b)
+                for (int cph = 0; cph < ph[0].nph; ++cph)
+                    for (int cc = 0; cc < ig.n_cchunks; ++cc, ++p) {
+                        ig.patch_ph[p][0] = (unsigned char)ph[0].phval[cph];
+                        ig.patch_ph[p][1] = (unsigned char)ph[1].phval[b];
+                        ig.patch_ph[p][2] = (unsigned char)ph[2].phval[a];
+                        ig.patch_ph[p][3] = (unsigned char)cc;
+                    }
+        struct At { unsigned off; int tap, cc; };
+        At at[kMaxHaloAtoms];
+        int na = 0;
+        const int X = pb.filt[2], Y = pb.filt[1], Z = pb.filt[0];
+        for (int z = 0; z < Z; ++z)
+            for (int y = 0; y < Y; ++y)
+                for (int x = 0; x < X; ++x)
+                    for (int cc = 0; cc < ig.n_cchunks; ++cc) {
+                        const int combo = (ph[2].phidx[z] * ph[1].nph + ph[1].phidx[y]) * ph[0].nph + ph[0].phidx[x];
+                        const int patch = combo * ig.n_cchunks + cc;
+                        const long long qoff =
+                            ((long long)ph[2].q[z] * ig.patch[1] + ph[1].q[y]) * ig.patch[0] + ph[0].q[x];
+                        at[na].off = (unsigned)(patch * ig.patch_bytes + qoff * 128);
+                        at[na].tap = (z * Y + y) * X + x;
+                        at[na].cc = cc;
+                        ++na;
+                    }
+        std::stable_sort(at, at + na, [](const At& l, const At& r) { return l.off < r.off; });
+        for (int i = 0; i < na; ++i) {
+            ig.atom_off[i] = at[i].off;
+            ig.atom_tap[i] = (unsigned short)at[i].tap;
+            ig.atom_cc[i] = (unsigned char)at[i].cc;
+        }
+    }
+
+    const long long base = (long long)ig.n_mranges * ig.n_ntiles * ig.n_gblocks;
+    if (base > 65535LL * 65535LL) return fail(err, WG_ERR_NOT_SUPPORTED, "grid too large");
+    int S;
+    if (o.split_k > 0) {
+        S = o.split_k;
+    } else if (o.mode == WG_MODE_DIRECT) {
+        S = 1;
+    } else {
+        S = (int)std::max(1LL, (long long)std::llround((double)num_sms / (double)base));
+        S = (int)std::min<long long>(S, ig.total_kt);
+        S = std::min(S, 65535);
+        const long long per = cdiv(ig.total_kt, S);
+        S = (int)cdiv(ig.total_kt, per);
+    }
+    if (S > 65535) return fail(err, WG_ERR_NOT_SUPPORTED, "split_k %d above 65535", S);
+    pl->S = S;
+    pl->per_split = cdiv(ig.total_kt, S);
+    pl->grid[0] = (unsigned)(ig.n_mranges * ig.n_ntiles);
+    pl->grid[1] = (unsigned)ig.n_gblocks;
+    pl->grid[2] = (unsigned)S;
+    pl->block = 192;
+    return WG_OK;
+}
+
+bool dw_eligible(const Problem& pb)
+{
+    if (pb.C != 1 || pb.K != 1 || pb.ndim > 2 || pb.T > 9 || pb.G % 8) return false;
+    const int wspan = (pb.out[2] - 1) * pb.stride[2] + (pb.filt[2] - 1) * pb.dil[2] + 1;
+    return wspan <= 256 && pb.out[2] <= 256;
+}
+
+int plan_depthwise(Plan* pl, const wg_options& o, int num_sms, std::string* err)
+{
+    const Problem& pb = pl->pb;
+    DwPlan& dw = pl->dw;
+    std::memset(&dw, 0, sizeof dw);
+    dw.CB = std::min(64, pb.G);
+    dw.n_cblocks = (int)cdiv(pb.G, dw.CB);
+    dw.Gm = o.group_merge > 0 ? o.group_merge : 8;
+    const int NV = dw.CB / dw.Gm;
+    const int Wo = pb.out[2], Ho = pb.out[1];
+    dw.xw = (Wo - 1) * pb.stride[2] + (pb.filt[2] - 1) * pb.dil[2] + 1;
+    const int avail = kMaxSmemPerCta - 1024 - 512;
+    // Rows per tile: little padding in Ho, at least 3 stages, at most 256 compute threads.
+    int bestR = 0;
+    long long best = -1;
+    for (int R = std::min(8, Ho); R >= 1; --R) {
+        if (NV * R > 256) continue;
+        const int xh = (R - 1) * pb.stride[1] + (pb.filt[1] - 1) * pb.dil[1] + 1;
+        if (xh > 256) continue;
+        const int stage = dw.CB * 2 * (dw.xw * xh + Wo * R);
+        if (avail / stage < 3) continue;
+        const long long padded = cdiv(Ho, R) * R;
+        const long long cost = padded * 1000 + (8 - R);  // less padding first, then taller tiles
+        if (best < 0 || cost < best) best = cost, bestR = R;
+    }
+    if (!bestR) return fail(err, WG_ERR_NOT_SUPPORTED, "depthwise tile does not fit shared memory");
+    dw.R = bestR;
+    dw.xh = (dw.R - 1) * pb.stride[1] + (pb.filt[1] - 1) * pb.dil[1] + 1;
+    dw.nseg = std::max(1, std::min(Wo, 256 / (NV * dw.R)));
+    dw.seg_len = (int)cdiv(Wo, dw.nseg);
+    dw.nseg = (int)cdiv(Wo, dw.seg_len);
+    dw.threads = round_up(NV * dw.R * dw.nseg, 32);
+    dw.x_bytes = dw.CB * 2 * dw.xw * dw.xh;
+    dw.dy_bytes = dw.CB * 2 * Wo * dw.R;
+    dw.stage_bytes = round_up(dw.x_bytes, 128) + round_up(dw.dy_bytes, 128);
+    dw.stages = std::min(6, avail / dw.stage_bytes);
+    const int red_bytes = dw.threads * (int)pb.T * dw.Gm * 4;
+    dw.smem_bytes = std::max(dw.stages * dw.stage_bytes, red_bytes) + 1024 + 512;
+    if (dw.smem_bytes > kMaxSmemPerCta) return fail(err, WG_ERR_NOT_SUPPORTED, "depthwise reduction too large");
+    dw.sliding = (pb.stride[2] == 1 && pb.dil[2] == 1) ? 1 : 0;
+    dw.total_tiles = (long long)pb.N * cdiv(Ho, dw.R);
+    int S;
+    if (o.split_k > 0) {
+        S = o.split_k;
+    } else if (o.mode == WG_MODE_DIRECT) {
+        S = 1;
+    } else {
+        S = (int)std::max(1LL, (long long)std::llround((double)num_sms / (double)dw.n_cblocks));
+        S = (int)std::min<long long>(S, dw.total_tiles);
+        S = std::min(S, 65535);
+        const long long per = cdiv(dw.total_tiles, S);
+        S = (int)cdiv(dw.total_tiles, per);
+    }
+    if (S > 65535) return fail(err, WG_ERR_NOT_SUPPORTED, "split_k %d above 65535", S);
+    pl->S = S;
+    pl->per_split = cdiv(dw.total_tiles, S);
+    pl->grid[0] = (unsigned)dw.n_cblocks;
+    pl->grid[1] = (unsigned)S;
+    pl->grid[2] = 1;
+    pl->block = (unsigned)(dw.threads + 32);
+    return WG_OK;
+}
+
+}  // namespace
+
+int normalize(const wg_problem* p, Problem* o, std::string* err)
+{
+    if (!p) return fail(err, WG_ERR_INVALID_ARGUMENT, "problem is NULL");
+    std::memset(o, 0, sizeof *o);
+    if (p->ndim < 1 || p->ndim > 3) return fail(err, WG_ERR_INVALID_ARGUMENT, "ndim must be 1, 2 or 3 (got %d)", p->ndim);
+    if (p->G < 1 || p->N < 1 || p->C < 1 || p->K < 1)
+        return fail(err, WG_ERR_INVALID_ARGUMENT, "G, N, C, K must be positive");
+    if (p->in_dtype != WG_BF16 && p->in_dtype != WG_FP16)
+        return fail(err, WG_ERR_INVALID_ARGUMENT, "in_dtype must be WG_BF16 or WG_FP16");
+    if (p->out_dtype != WG_FP32 && p->out_dtype != WG_BF16 && p->out_dtype != WG_FP16)
+        return fail(err, WG_ERR_INVALID_ARGUMENT, "out_dtype must be WG_FP32, WG_BF16 or WG_FP16");
+    o->ndim = p->ndim;
+    o->G = p->G, o->N = p->N, o->C = p->C, o->K = p->K;
+    o->in_dtype = p->in_dtype, o->out_dtype = p->out_dtype;
+    const int off = 3 - p->ndim;
+    for (int i = 0; i < 3; ++i) {
+        o->in[i] = o->filt[i] = o->out[i] = o->stride[i] = o->dil[i] = 1;
+        o->pad_l[i] = o->pad_r[i] = 0;
+    }
+    for (int i = 0; i < p->ndim; ++i) {
+        const int j = off + i;
+        if (p->in[i] < 1 || p->filt[i] < 1 || p->stride[i] < 1 || p->dil[i] < 1 || p->pad_l[i] < 0 || p->pad_r[i] < 0)
+            return fail(err, WG_ERR_INVALID_ARGUMENT,
+                        "spatial dim %d: in, filt, stride, dil must be >= 1 and pads >= 0", i);
+        const long long num = (long long)p->in[i] + p->pad_l[i] + p->pad_r[i] - (long long)p->dil[i] * (p->filt[i] - 1) - 1;
+        if (num < 0)
+            return fail(err, WG_ERR_INVALID_ARGUMENT, "spatial dim %d: dilated filter larger than padded input", i);
+        const long long out = num / p->stride[i] + 1;
+        if (out > (1 << 30)) return fail(err, WG_ERR_INVALID_ARGUMENT, "spatial dim %d: output too large", i);
+        if (p->out[i] != 0 && p->out[i] != out)
+            return fail(err, WG_ERR_INVALID_ARGUMENT, "spatial dim %d: out=%d but the derived length is %lld", i,
+                        p->out[i], out);
+        o->in[j] = p->in[i], o->filt[j] = p->filt[i], o->out[j] = (int)out;
+        o->stride[j] = p->stride[i], o->dil[j] = p->dil[i], o->pad_l[j] = p->pad_l[i], o->pad_r[j] = p->pad_r[i];
+    }
+    o->T = (long long)o->filt[0] * o->filt[1] * o->filt[2];
+    o->P = (long long)o->N * o->out[0] * o->out[1] * o->out[2];
+    o->x_elems = (long long)o->N * o->in[0] * o->in[1] * o->in[2] * o->G * o->C;
+    o->dy_elems = o->P * o->G * o->K;
+    o->dw_elems = (long long)o->G * o->K * o->T * o->C;
+    const long long lim = (1ll << 31) - 1;
+    if (o->x_elems > lim || o->dy_elems > lim || o->dw_elems > lim)
+        return fail(err, WG_ERR_NOT_SUPPORTED, "a tensor has 2^31 or more elements");
+    return WG_OK;
+}
+
+int make_plan(const wg_problem* p, const wg_options* opt, int num_sms, Plan* pl, std::string* err)
+{
+    std::memset(pl, 0, sizeof *pl);
+    int st = normalize(p, &pl->pb, err);
+    if (st) return st;
+    const Problem& pb = pl->pb;
+    wg_options o{0, WG_MODE_AUTO, 0};
+    if (opt) o = *opt;
+    if (num_sms <= 0) num_sms = kDefaultSMs;
+    if (o.split_k < 0) return fail(err, WG_ERR_INVALID_ARGUMENT, "split_k must be >= 0");
+    if (o.mode < WG_MODE_AUTO || o.mode > WG_MODE_DETERMINISTIC) return fail(err, WG_ERR_INVALID_ARGUMENT, "bad mode");
+    if (o.group_merge != 0 && o.group_merge != 1 && o.group_merge != 2 && o.group_merge != 4 && o.group_merge != 8)
+        return fail(err, WG_ERR_INVALID_ARGUMENT, "group_merge must be 0, 1, 2, 4 or 8");
+    if (o.mode == WG_MODE_DIRECT && o.split_k > 1)
+        return fail(err, WG_ERR_INVALID_ARGUMENT, "mode DIRECT takes no split (split_k %d)", o.split_k);
+    if (o.mode == WG_MODE_ATOMIC && pb.out_dtype != WG_FP32)
+        return fail(err, WG_ERR_NOT_SUPPORTED, "atomic split-K accumulates in fp32: dW must be WG_FP32");
+    if (((long long)pb.G * pb.C * 2) % 16 || ((long long)pb.G * pb.K * 2) % 16)
+        return fail(err, WG_ERR_NOT_SUPPORTED, "G*C and G*K must be multiples of 8 (16-byte pixel rows for TMA)");
+    const bool depthwise = pb.C == 1 && pb.K == 1;
+    if (o.group_merge > 1 && !depthwise)
+        return fail(err, WG_ERR_NOT_SUPPORTED, "group_merge > 1 is for depthwise problems (C = K = 1) only");
+    if (depthwise && dw_eligible(pb)) {
+        pl->kind = KIND_DEPTHWISE;
+        st = plan_depthwise(pl, o, num_sms, err);
+    } else {
+        if (o.group_merge > 1)
+            return fail(err, WG_ERR_NOT_SUPPORTED,
+                        "group_merge > 1 needs the depthwise kernel (1-D/2-D, <= 9 taps, G %% 8 == 0)");
+        pl->kind = KIND_IGEMM;
+        st = plan_igemm(pl, o, num_sms, err);
+    }
+    if (st) return st;
+    if (o.mode == WG_MODE_ATOMIC)
+        pl->mode = MODE_ATOMIC;
+    else if (pl->S == 1)
+        pl->mode = MODE_DIRECT;
+    else
+        pl->mode = MODE_DETERMINISTIC;
+    pl->ws_bytes = pl->mode == MODE_DETERMINISTIC ? (size_t)pl->S * (size_t)pb.dw_elems * 4 : 0;
+    return WG_OK;
+}
+
+std::string plan_string(const Plan& pl)
+{
+    const Problem& pb = pl.pb;
+    char buf[1024];
+    const char* mode = pl.mode == MODE_DIRECT ? "direct" : pl.mode == MODE_ATOMIC ? "atomic" : "deterministic";
+    if (pl.kind == KIND_IGEMM) {
+        const IgemmPlan& ig = pl.ig;
+        snprintf(buf, sizeof buf,
+                 "kernel=igemm_tcgen05 %s mode=%s S=%d Gm=%d gblocks=%d cchunks=%d Nt=%d ntiles=%d katoms=%d "
+                 "box=(w%d,h%d,d%d,n%d) KT=%d ktiles=%lld per_split=%lld atoms=%d mtiles=%d mt_per_cta=%d "
+                 "mranges=%d tmem_cols=%d stages=%d stage_bytes=%d smem=%d grid=(%u,%u,%u) block=%u ws=%zu",
+                 ig.halo ? "halo" : "pertap", mode, pl.S, ig.Gm, ig.n_gblocks, ig.n_cchunks, ig.Nt, ig.n_ntiles, ig.n_katoms, ig.box[0], ig.box[1],
+                 ig.box[2], ig.box[3], ig.KT, ig.total_kt, pl.per_split, ig.n_atoms, ig.n_mtiles, ig.mt_per_cta,
+                 ig.n_mranges, ig.tmem_cols, ig.stages, ig.stage_bytes, ig.smem_bytes, pl.grid[0], pl.grid[1],
+                 pl.grid[2], pl.block, pl.ws_bytes);
+    } else {
+        const DwPlan& dw = pl.dw;
+        snprintf(buf, sizeof buf,
+                 "kernel=depthwise mode=%s S=%d Gm=%d CB=%d cblocks=%d R=%d nseg=%d seg_len=%d threads=%d "
+                 "xtile=(w%d,h%d) tiles=%lld per_split=%lld stages=%d stage_bytes=%d smem=%d sliding=%d "
+                 "grid=(%u,%u,%u) block=%u ws=%zu",
+                 mode, pl.S, dw.Gm, dw.CB, dw.n_cblocks, dw.R, dw.nseg, dw.seg_len, dw.threads, dw.xw, dw.xh,
+                 dw.total_tiles, pl.per_split, dw.stages, dw.stage_bytes, dw.smem_bytes, dw.sliding, pl.grid[0],
+                 pl.grid[1], pl.grid[2], pl.block, pl.ws_bytes);
+    }
+    (void)pb;
+    return buf;
+}
+
+}  // namespace wg

@@ -1,0 +1,111 @@
+// Host-side problem normalisation and launch planning for the wgrad kernels.
+// Pure C++ (no CUDA calls): the plan is a function of the problem, the options
+// and the SM count.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/wgrad.h"
+
+namespace wg {
+
+constexpr int kDefaultSMs = 152;        // GB300: 2 dies x 76 SMs
+constexpr int kMaxSmemPerCta = 232448;  // 227 KB opt-in dynamic shared memory
+constexpr int kMaxTmemCols = 512;
+constexpr int kMaxPatches = 32;
+constexpr int kMaxHaloAtoms = 256;
+constexpr int kMaxHaloFilter = 32;
+
+enum Kind { KIND_IGEMM = 0, KIND_DEPTHWISE = 1 };
+enum Mode { MODE_DIRECT = 1, MODE_ATOMIC = 2, MODE_DETERMINISTIC = 3 };
+
+// Normalised problem: every spatial array has 3 entries ordered (D, H, W);
+// lower ranks put 1 (pads 0) in the leading unused entries.
+struct Problem {
+    int ndim, G, N, C, K;
+    int in[3], filt[3], out[3], stride[3], dil[3], pad_l[3], pad_r[3];
+    int in_dtype, out_dtype;
+    long long T;  // filter taps Z*Y*X
+    long long P;  // GemmK = N*Do*Ho*Wo
+    long long x_elems, dy_elems, dw_elems;
+};
+
+// Tensor-core implicit GEMM (kernel igemm_wgrad).  The CTA tile is
+// D[(tap, c) rows x k cols]; rows come in "atoms" of 64 channels of one tap.
+struct IgemmPlan {
+    int Gm;           // groups folded into one CTA channel window
+    int n_gblocks;    // ceil(G / Gm)
+    int n_cchunks;    // 64-channel chunks per tap in the window
+    int Nt;           // MMA N (k columns per N-tile), multiple of 16, <= 256
+    int n_ntiles;     // N-tiles over the k window
+    int n_katoms;     // 64-wide dY chunks per N-tile
+    int box[4];       // pixel tile extent along (w, h, d, n)
+    int ntile[4];     // tiles along (w, h, d, n)
+    int KT;           // pixels per K-tile = product of box
+    long long total_kt;
+    int n_atoms;      // taps x chunks
+    int n_mtiles;     // ceil(n_atoms / 2): MMA M = 128 = two atoms
+    int mt_per_cta;   // M-tiles accumulated by one CTA (TMEM columns = mt_per_cta * Nt)
+    int n_mranges;    // ceil(n_mtiles / mt_per_cta)
+    int tmem_cols;    // power of two >= mt_per_cta * Nt
+    int stages;
+    int slot_bytes;   // KT * 128 bytes: one 64-channel dY chunk of one K-tile
+    int stage_bytes;
+    int smem_bytes;   // dynamic shared memory per CTA
+    // X staging.  halo = 1: per K-tile one patch per (stride phase, channel
+    // chunk) covering every tap, taps read as row-shifted views of it.
+    // halo = 0: one box per atom (tap, chunk), 2 * mt_per_cta boxes per K-tile.
+    int halo;
+    int patch[3];     // patch extent along (w, h, d) in strided input pixels
+    int patch_bytes;  // bytes per patch, 1024-aligned
+    int n_patches;    // patches (or boxes) per K-tile
+    int dy_off;       // byte offset of the dY chunks inside a stage
+    int n_phase[3];   // stride phases used along (w, h, d)
+    unsigned char patch_ph[kMaxPatches][4];  // phase value (w, h, d) and channel chunk of each patch
+    unsigned int atom_off[kMaxHaloAtoms];    // byte offset of atom (patch + tap row shift) in a stage
+    unsigned short atom_tap[kMaxHaloAtoms];
+    unsigned char atom_cc[kMaxHaloAtoms];
+    long long est_cycles;  // planner's cost estimate (for the plan string)
+};
+
+// CUDA-core depthwise kernel (cpg = kpg = 1).
+struct DwPlan {
+    int CB;           // channels per CTA
+    int n_cblocks;
+    int Gm;           // channels per thread vector (group-merge degree)
+    int R;            // output rows per tile
+    int nseg;         // column segments per row
+    int seg_len;      // output columns per segment
+    int threads;      // compute threads (a producer warp is added on top)
+    int xw, xh;       // X tile extent (w, h) in input pixels
+    long long total_tiles;  // N * ceil(Ho / R)
+    int stages;
+    int x_bytes, dy_bytes, stage_bytes, smem_bytes;
+    int sliding;      // 1: register sliding window along W (stride 1, dilation 1 in W)
+};
+
+struct Plan {
+    Problem pb;
+    int kind;
+    int mode;
+    int S;              // split degree of GemmK
+    long long per_split;  // K-tiles (igemm) or row tiles (depthwise) per split
+    size_t ws_bytes;
+    unsigned grid[3];
+    unsigned block;
+    IgemmPlan ig;
+    DwPlan dw;
+};
+
+// Validate and normalise.  Returns a wg_status; *err gets the reason.
+int normalize(const wg_problem* p, Problem* out, std::string* err);
+
+// Choose kernel, tiles, split degree and mode.  num_sms <= 0 means kDefaultSMs.
+int make_plan(const wg_problem* p, const wg_options* opt, int num_sms, Plan* out, std::string* err);
+
+std::string plan_string(const Plan& pl);
+
+}  // namespace wg

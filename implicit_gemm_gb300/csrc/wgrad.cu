@@ -1,0 +1,384 @@
+// C ABI of libwgrad.so (declared in include/wgrad.h): validation, planning,
+// TMA tensor-map encoding and kernel launches.  No device memory is allocated
+// here; every buffer is the caller's.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <map>
+#include <mutex>
+#include <string>
+
+#include "../../include/wgrad.h"
+#include "k_depthwise.cuh"
+#include "k_igemm.cuh"
+#include "plan.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+int set_err(int status, const std::string& msg)
+{
+    g_err = msg;
+    return status;
+}
+
+int cuda_fail(const char* what, cudaError_t e)
+{
+    return set_err(WG_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// SM count of the current device (kDefaultSMs when no device is visible, so
+// host-only queries give the same plan on a machine without a GPU).
+int num_sms()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return wg::kDefaultSMs;
+    }
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return wg::kDefaultSMs;
+    }
+    return n;
+}
+
+// Plans are a pure function of (problem, options, SM count); successful ones
+// are cached so that repeated calls skip the tile search.
+int plan_for(const wg_problem* p, const wg_options* opt, wg::Plan* pl)
+{
+    static std::mutex mu;
+    static std::map<std::string, wg::Plan> cache;
+    const int sms = num_sms();
+    std::string key;
+    if (p) {
+        wg_options o{0, WG_MODE_AUTO, 0};
+        if (opt) o = *opt;
+        key.assign(reinterpret_cast<const char*>(p), sizeof *p);
+        key.append(reinterpret_cast<const char*>(&o), sizeof o);
+        key.append(reinterpret_cast<const char*>(&sms), sizeof sms);
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            *pl = it->second;
+            return WG_OK;
+        }
+    }
+    std::string err;
+    const int st = wg::make_plan(p, opt, sms, pl, &err);
+    if (st) return set_err(st, err);
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache.size() > 1024) cache.clear();
+    cache.emplace(key, *pl);
+    return WG_OK;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+int encode(CUtensorMap* tm, int in_dtype, void* base, const cuuint64_t dims[5], const cuuint32_t box[5],
+           const cuuint32_t estr[5], CUtensorMapSwizzle swz, const char* what)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return set_err(WG_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t strides[4];
+    cuuint64_t s = dims[0] * 2;
+    for (int i = 0; i < 4; ++i) {
+        strides[i] = s;
+        s *= dims[i + 1];
+    }
+    const CUtensorMapDataType dt = in_dtype == WG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUresult r = fn(tm, dt, 5, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char buf[256];
+        snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled(%s) failed with CUresult %d (box %u,%u,%u,%u,%u)", what, (int)r,
+                 box[0], box[1], box[2], box[3], box[4]);
+        return set_err(WG_ERR_CUDA, buf);
+    }
+    return WG_OK;
+}
+
+template <typename K>
+int ensure_smem(K kernel, int bytes)
+{
+    // Idempotent and cheap; set per call so a kernel first used with a small
+    // configuration still accepts a larger one later.
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", e);
+    return WG_OK;
+}
+
+int launch_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, void* ws, cudaStream_t stream)
+{
+    const wg::Problem& pb = pl.pb;
+    const wg::IgemmPlan& ig = pl.ig;
+    CUtensorMap tmx, tmy;
+    const cuuint64_t GC = (cuuint64_t)pb.G * pb.C, GK = (cuuint64_t)pb.G * pb.K;
+    {
+        const cuuint64_t dims[5] = {GC, (cuuint64_t)pb.in[2], (cuuint64_t)pb.in[1], (cuuint64_t)pb.in[0],
+                                    (cuuint64_t)pb.N};
+        const cuuint32_t box[5] = {64, (cuuint32_t)(ig.patch[0] * pb.stride[2]), (cuuint32_t)(ig.patch[1] * pb.stride[1]),
+                                   (cuuint32_t)(ig.patch[2] * pb.stride[0]), (cuuint32_t)ig.box[3]};
+        const cuuint32_t estr[5] = {1, (cuuint32_t)pb.stride[2], (cuuint32_t)pb.stride[1], (cuuint32_t)pb.stride[0], 1};
+        const int st = encode(&tmx, pb.in_dtype, const_cast<void*>(x), dims, box, estr, CU_TENSOR_MAP_SWIZZLE_128B, "X");
+        if (st) return st;
+    }
+    {
+        const cuuint64_t dims[5] = {GK, (cuuint64_t)pb.out[2], (cuuint64_t)pb.out[1], (cuuint64_t)pb.out[0],
+                                    (cuuint64_t)pb.N};
+        const cuuint32_t box[5] = {64, (cuuint32_t)ig.box[0], (cuuint32_t)ig.box[1], (cuuint32_t)ig.box[2],
+                                   (cuuint32_t)ig.box[3]};
+        const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        const int st = encode(&tmy, pb.in_dtype, const_cast<void*>(dy), dims, box, estr, CU_TENSOR_MAP_SWIZZLE_128B, "dY");
+        if (st) return st;
+    }
+    wg::IgParams prm;
+    memset(&prm, 0, sizeof prm);
+    prm.G = pb.G, prm.C = pb.C, prm.K = pb.K, prm.T = (int)pb.T, prm.GC = (int)GC, prm.GK = (int)GK;
+    prm.X = pb.filt[2], prm.Y = pb.filt[1];
+    prm.ncc = ig.n_cchunks;
+    for (int i = 0; i < 3; ++i) {
+        prm.s[i] = pb.stride[2 - i];
+        prm.d[i] = pb.dil[2 - i];
+        prm.pl[i] = pb.pad_l[2 - i];
+        prm.patch[i] = ig.patch[i];
+    }
+    for (int i = 0; i < 4; ++i) prm.box[i] = ig.box[i], prm.ntile[i] = ig.ntile[i];
+    prm.KT = ig.KT, prm.ksteps = ig.KT / 16;
+    prm.per_split = (int)pl.per_split, prm.total_kt = (int)ig.total_kt;
+    prm.Gm = ig.Gm, prm.Nt = ig.Nt, prm.n_ntiles = ig.n_ntiles, prm.n_katoms = ig.n_katoms;
+    prm.n_atoms = ig.n_atoms, prm.n_mtiles = ig.n_mtiles, prm.mtpc = ig.mt_per_cta;
+    prm.halo = ig.halo;
+    prm.patch_bytes = ig.patch_bytes;
+    prm.patch_tx = ig.halo ? ig.patch[0] * ig.patch[1] * ig.patch[2] * ig.box[3] * 128 : ig.slot_bytes;
+    prm.n_patches = ig.n_patches, prm.dy_off = ig.dy_off, prm.slot_bytes = ig.slot_bytes;
+    prm.stage_bytes = ig.stage_bytes, prm.stages = ig.stages, prm.tmem_cols = ig.tmem_cols;
+    prm.idesc = wg::make_idesc_f16(pb.in_dtype == WG_BF16, true, true, 128, ig.Nt);
+    prm.mode = pl.mode, prm.out_dtype = pb.out_dtype;
+    prm.out = pl.mode == wg::MODE_DETERMINISTIC ? ws : dw;
+    prm.split_stride = pb.dw_elems;
+    if (ig.halo) {
+        memcpy(prm.patch_ph, ig.patch_ph, sizeof prm.patch_ph);
+        for (int i = 0; i < ig.n_atoms; ++i) {
+            prm.atom_off[i] = ig.atom_off[i];
+            prm.atom_tap[i] = ig.atom_tap[i];
+            prm.atom_cc[i] = ig.atom_cc[i];
+        }
+    }
+    int st = ensure_smem(wg::igemm_wgrad_kernel, ig.smem_bytes);
+    if (st) return st;
+    if (pl.mode == wg::MODE_ATOMIC) {
+        const cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)pb.dw_elems * 4, stream);
+        if (e != cudaSuccess) return cuda_fail("cudaMemsetAsync(dW)", e);
+    }
+    wg::igemm_wgrad_kernel<<<dim3(pl.grid[0], pl.grid[1], pl.grid[2]), pl.block, ig.smem_bytes, stream>>>(tmx, tmy, prm);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail("igemm_wgrad_kernel launch", e);
+    if (pl.mode == wg::MODE_DETERMINISTIC) {
+        const long long work = (pb.dw_elems & 3) ? pb.dw_elems : pb.dw_elems / 4;
+        const int blocks = (int)std::min<long long>((work + 255) / 256, 4LL * num_sms());
+        wg::reduce_splits_kernel<<<blocks, 256, 0, stream>>>(static_cast<const float*>(ws), dw, pb.dw_elems, pl.S,
+                                                             pb.out_dtype);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail("reduce_splits_kernel launch", e);
+    }
+    return WG_OK;
+}
+
+template <bool BF16, int GM, bool SLIDE>
+int launch_dw_t(const wg::Plan& pl, const CUtensorMap& tmx, const CUtensorMap& tmy, const wg::DwParams& prm,
+                cudaStream_t stream)
+{
+    auto k = wg::depthwise_wgrad_kernel<BF16, GM, SLIDE>;
+    const int st = ensure_smem(k, pl.dw.smem_bytes);
+    if (st) return st;
+    k<<<dim3(pl.grid[0], pl.grid[1], pl.grid[2]), pl.block, pl.dw.smem_bytes, stream>>>(tmx, tmy, prm);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail("depthwise_wgrad_kernel launch", e);
+    return WG_OK;
+}
+
+template <bool BF16, int GM>
+int launch_dw_g(const wg::Plan& pl, const CUtensorMap& a, const CUtensorMap& b, const wg::DwParams& prm, cudaStream_t s)
+{
+    const bool slide = pl.dw.sliding && pl.pb.filt[1] == 3 && pl.pb.filt[2] == 3;
+    return slide ? launch_dw_t<BF16, GM, true>(pl, a, b, prm, s) : launch_dw_t<BF16, GM, false>(pl, a, b, prm, s);
+}
+
+template <bool BF16>
+int launch_dw_b(const wg::Plan& pl, const CUtensorMap& a, const CUtensorMap& b, const wg::DwParams& prm, cudaStream_t s)
+{
+    switch (pl.dw.Gm) {
+        case 1: return launch_dw_g<BF16, 1>(pl, a, b, prm, s);
+        case 2: return launch_dw_g<BF16, 2>(pl, a, b, prm, s);
+        case 4: return launch_dw_g<BF16, 4>(pl, a, b, prm, s);
+        default: return launch_dw_g<BF16, 8>(pl, a, b, prm, s);
+    }
+}
+
+int launch_depthwise(const wg::Plan& pl, const void* x, const void* dy, void* dw, void* ws, cudaStream_t stream)
+{
+    const wg::Problem& pb = pl.pb;
+    const wg::DwPlan& d = pl.dw;
+    CUtensorMap tmx, tmy;
+    {
+        const cuuint64_t dims[5] = {(cuuint64_t)pb.G, (cuuint64_t)pb.in[2], (cuuint64_t)pb.in[1], 1, (cuuint64_t)pb.N};
+        const cuuint32_t box[5] = {(cuuint32_t)d.CB, (cuuint32_t)d.xw, (cuuint32_t)d.xh, 1, 1};
+        const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        const int st = encode(&tmx, pb.in_dtype, const_cast<void*>(x), dims, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE, "X");
+        if (st) return st;
+    }
+    {
+        const cuuint64_t dims[5] = {(cuuint64_t)pb.G, (cuuint64_t)pb.out[2], (cuuint64_t)pb.out[1], 1, (cuuint64_t)pb.N};
+        const cuuint32_t box[5] = {(cuuint32_t)d.CB, (cuuint32_t)pb.out[2], (cuuint32_t)d.R, 1, 1};
+        const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        const int st = encode(&tmy, pb.in_dtype, const_cast<void*>(dy), dims, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE, "dY");
+        if (st) return st;
+    }
+    wg::DwParams prm;
+    memset(&prm, 0, sizeof prm);
+    prm.G = pb.G, prm.Ho = pb.out[1], prm.Wo = pb.out[2], prm.Y = pb.filt[1], prm.X = pb.filt[2], prm.T = (int)pb.T;
+    prm.sh = pb.stride[1], prm.sw = pb.stride[2], prm.dh = pb.dil[1], prm.dw = pb.dil[2];
+    prm.plh = pb.pad_l[1], prm.plw = pb.pad_l[2];
+    prm.CB = d.CB, prm.R = d.R, prm.nseg = d.nseg, prm.seg_len = d.seg_len;
+    prm.nused = (d.CB / d.Gm) * d.R * d.nseg;
+    prm.xw = d.xw, prm.xh = d.xh;
+    prm.n_hstrips = (pb.out[1] + d.R - 1) / d.R;
+    prm.per_split = (int)pl.per_split, prm.total_tiles = (int)d.total_tiles;
+    prm.stages = d.stages, prm.stage_bytes = d.stage_bytes;
+    prm.x_bytes_al = (d.x_bytes + 127) / 128 * 128;
+    prm.x_tx = d.x_bytes, prm.dy_tx = d.dy_bytes;
+    prm.mode = pl.mode, prm.out_dtype = pb.out_dtype;
+    prm.out = pl.mode == wg::MODE_DETERMINISTIC ? ws : dw;
+    prm.split_stride = pb.dw_elems;
+    if (pl.mode == wg::MODE_ATOMIC) {
+        const cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)pb.dw_elems * 4, stream);
+        if (e != cudaSuccess) return cuda_fail("cudaMemsetAsync(dW)", e);
+    }
+    int st = pb.in_dtype == WG_BF16 ? launch_dw_b<true>(pl, tmx, tmy, prm, stream)
+                                    : launch_dw_b<false>(pl, tmx, tmy, prm, stream);
+    if (st) return st;
+    if (pl.mode == wg::MODE_DETERMINISTIC) {
+        const long long work = (pb.dw_elems & 3) ? pb.dw_elems : pb.dw_elems / 4;
+        const int blocks = (int)std::min<long long>((work + 255) / 256, 4LL * num_sms());
+        wg::reduce_splits_kernel<<<blocks, 256, 0, stream>>>(static_cast<const float*>(ws), dw, pb.dw_elems, pl.S,
+                                                             pb.out_dtype);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail("reduce_splits_kernel launch", e);
+    }
+    return WG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* wg_status_string(int s)
+{
+    switch (s) {
+        case WG_OK: return "WG_OK";
+        case WG_ERR_INVALID_ARGUMENT: return "WG_ERR_INVALID_ARGUMENT";
+        case WG_ERR_NOT_SUPPORTED: return "WG_ERR_NOT_SUPPORTED";
+        case WG_ERR_MISALIGNED: return "WG_ERR_MISALIGNED";
+        case WG_ERR_WORKSPACE: return "WG_ERR_WORKSPACE";
+        case WG_ERR_CUDA: return "WG_ERR_CUDA";
+        case WG_ERR_DEVICE_TIMEOUT: return "WG_ERR_DEVICE_TIMEOUT";
+        default: return "WG_ERR_UNKNOWN";
+    }
+}
+
+const char* wg_last_error(void) { return g_err.c_str(); }
+
+int wg_problem_normalize(wg_problem* p)
+{
+    wg::Problem pb;
+    std::string err;
+    const int st = wg::normalize(p, &pb, &err);
+    if (st) return set_err(st, err);
+    for (int i = 0; i < p->ndim; ++i) p->out[i] = pb.out[3 - p->ndim + i];
+    return WG_OK;
+}
+
+int wg_workspace_size(const wg_problem* p, const wg_options* opt, size_t* bytes)
+{
+    if (!bytes) return set_err(WG_ERR_INVALID_ARGUMENT, "bytes is NULL");
+    wg::Plan pl;
+    const int st = plan_for(p, opt, &pl);
+    if (st) return st;
+    *bytes = pl.ws_bytes;
+    return WG_OK;
+}
+
+int wg_plan_string(const wg_problem* p, const wg_options* opt, char* buf, size_t n)
+{
+    if (!buf || n == 0) return set_err(WG_ERR_INVALID_ARGUMENT, "buffer is NULL or empty");
+    wg::Plan pl;
+    const int st = plan_for(p, opt, &pl);
+    if (st) return st;
+    snprintf(buf, n, "%s", wg::plan_string(pl).c_str());
+    return WG_OK;
+}
+
+int wg_conv_bwd_weight(const wg_problem* p, const void* x, const void* dy, void* dw, const wg_options* opt,
+                       void* workspace, size_t ws_bytes, void* stream)
+{
+    wg::Plan pl;
+    int st = plan_for(p, opt, &pl);
+    if (st) return st;
+    if (!x || !dy || !dw) return set_err(WG_ERR_INVALID_ARGUMENT, "x, dy and dw must be non-NULL device pointers");
+    if (!aligned16(x) || !aligned16(dy) || !aligned16(dw))
+        return set_err(WG_ERR_MISALIGNED, "x, dy and dw must be 16-byte aligned");
+    if (pl.ws_bytes > 0) {
+        if (!workspace || ws_bytes < pl.ws_bytes) {
+            char buf[160];
+            snprintf(buf, sizeof buf, "workspace of %zu bytes needed (got %zu%s)", pl.ws_bytes, ws_bytes,
+                     workspace ? "" : ", NULL");
+            return set_err(WG_ERR_WORKSPACE, buf);
+        }
+        if (!aligned16(workspace)) return set_err(WG_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = pl.kind == wg::KIND_IGEMM ? launch_igemm(pl, x, dy, dw, workspace, s)
+                                   : launch_depthwise(pl, x, dy, dw, workspace, s);
+    return st;
+}
+
+int wg_check_status(void* stream)
+{
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+    unsigned int v = 0;
+    e = cudaMemcpyFromSymbol(&v, wg::g_status, sizeof v);
+    if (e != cudaSuccess) return cuda_fail("cudaMemcpyFromSymbol(status)", e);
+    if (v) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(wg::g_status, &zero, sizeof zero);
+        if (e != cudaSuccess) return cuda_fail("cudaMemcpyToSymbol(status)", e);
+        return set_err(WG_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out");
+    }
+    return WG_OK;
+}
+
+}  // extern "C"

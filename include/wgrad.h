@@ -1,0 +1,146 @@
+/*
+ * wgrad.h — C ABI of libwgrad.so: grouped-convolution backward-weight (wgrad)
+ * on one NVIDIA GB300 (sm_103a), lowered as an implicit GEMM.
+ *
+ * Operation (weight gradient of a grouped convolution):
+ *
+ *   dW[g,k,(z),(y),x,c] = sum over n,(od),(oh),ow of
+ *        dY[n,(od),(oh),ow,g,k] * X[n,(od*sd-pld+z*dd),(oh*sh-plh+y*dh),ow*sw-plw+x*dw,g,c]
+ *
+ * where terms whose input position falls outside the image are zero (implicit
+ * zero padding).  Layouts, one per spatial rank, are those of the
+ * GroupedConvBwdWeightKernelArgs constructors in "Composable Kernel:
+ * grouped_convolution_backward_weight_kernel.hpp Source File":
+ *   1-D  X = NWGC,   dW = GKXC,   dY = NWGK
+ *   2-D  X = NHWGC,  dW = GKYXC,  dY = NHWGK
+ *   3-D  X = NDHWGC, dW = GKZYXC, dY = NDHWGK
+ * all packed (no custom strides), C and K being the channels of one group.
+ * The implicit GEMM of that page has GemmM = K, GemmN = C*Z*Y*X,
+ * GemmK = N*Do*Ho*Wo and GemmBatch = G.
+ *
+ * Conventions for every entry point below:
+ *  - Pointers x, dy, dw and workspace are DEVICE pointers on the current CUDA
+ *    device, owned by the caller.  The library allocates no device memory.
+ *  - x, dy, dw and workspace must be 16-byte aligned (WG_ERR_MISALIGNED).
+ *  - dW is overwritten (beta = 0) in every mode.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  All device work is stream-ordered; return codes report host-side
+ *    validation and launch errors only.  Device-side errors (a bounded wait
+ *    that ran out) are reported by wg_check_status.
+ *  - On a non-zero return, wg_last_error() gives a one-line reason.
+ *  - Thread-safe: calls keep no state between them except the device status
+ *    word read by wg_check_status.
+ */
+#ifndef WGRAD_H
+#define WGRAD_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define WG_API __attribute__((visibility("default")))
+#else
+#define WG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { WG_BF16 = 0, WG_FP16 = 1, WG_FP32 = 2 } wg_dtype;
+
+/* How split-K partial sums are combined.
+ *  DIRECT:        no split (split_k must be 1 or 0); dW = cast(sum).
+ *  ATOMIC:        dW is zeroed on the stream first (the Preprocess memset of the
+ *                 CK page), then every split adds its fp32 partial with a
+ *                 global atomic.  fp32 dW only.  Not bitwise reproducible.
+ *  DETERMINISTIC: two-stage: every split writes an fp32 partial to the
+ *                 workspace, then a second kernel sums the splits in index
+ *                 order s = 0..S-1 and casts (round to nearest even) to dW.
+ *                 Bitwise reproducible for a given problem and split degree.
+ *  AUTO:          DIRECT when the chosen split degree is 1, else DETERMINISTIC. */
+typedef enum {
+    WG_MODE_AUTO = 0,
+    WG_MODE_DIRECT = 1,
+    WG_MODE_ATOMIC = 2,
+    WG_MODE_DETERMINISTIC = 3
+} wg_mode;
+
+typedef enum {
+    WG_OK = 0,
+    WG_ERR_INVALID_ARGUMENT = 1, /* non-positive size, derived output <= 0, out[] mismatch, NULL pointer */
+    WG_ERR_NOT_SUPPORTED = 2,    /* valid problem outside what the kernels handle (IsSupportedArgument = false) */
+    WG_ERR_MISALIGNED = 3,       /* a base pointer is not 16-byte aligned */
+    WG_ERR_WORKSPACE = 4,        /* workspace missing or smaller than wg_workspace_size */
+    WG_ERR_CUDA = 5,             /* a CUDA runtime/driver call failed */
+    WG_ERR_DEVICE_TIMEOUT = 6    /* a kernel's bounded wait ran out (reported by wg_check_status) */
+} wg_status;
+
+/* Problem record (the host arguments of the CK page: G_, N_, C_, K_, spatial
+ * lengths, strides, dilations, left/right pads).
+ * Spatial arrays use their first `ndim` entries, outermost dimension first
+ * (D, H, W for 3-D; H, W for 2-D; W for 1-D); the other entries are ignored. */
+typedef struct {
+    int ndim;              /* 1, 2 or 3 */
+    int G, N, C, K;        /* groups, batch, channels per group (input C, output K) */
+    int in[3];             /* input spatial lengths */
+    int filt[3];           /* filter spatial lengths */
+    int out[3];            /* output lengths: 0 = derive; non-zero must equal the derived value */
+    int stride[3], dil[3]; /* >= 1 */
+    int pad_l[3], pad_r[3];/* >= 0 */
+    wg_dtype in_dtype;     /* X and dY: WG_BF16 or WG_FP16 (both the same) */
+    wg_dtype out_dtype;    /* dW: WG_FP32, WG_BF16 or WG_FP16 */
+} wg_problem;
+
+/* Per-call options (the CK page's k_batch, plus the two ways of combining splits).
+ *  split_k:     0 = choose automatically, 1 = no split, S > 1 = S splits of GemmK.
+ *  mode:        see wg_mode.
+ *  group_merge: depthwise problems only (C = K = 1): channels handled per thread
+ *               vector (1, 2, 4 or 8); 0 = choose automatically.  Must be 0 or 1
+ *               for other problems. */
+typedef struct {
+    int split_k;
+    wg_mode mode;
+    int group_merge;
+} wg_options;
+
+/* Validate `p` and fill p->out[] with the derived output lengths
+ * (out = floor((in + pad_l + pad_r - dil*(filt-1) - 1) / stride) + 1 per dim).
+ * Returns WG_OK or WG_ERR_INVALID_ARGUMENT.  Host only. */
+WG_API int wg_problem_normalize(wg_problem* p);
+
+/* Bytes of device workspace that wg_conv_bwd_weight needs for (p, opt)
+ * (0 unless the chosen mode is DETERMINISTIC with more than one split, where it
+ * is S * G*K*Z*Y*X*C * 4, the unmerged size).  opt may be NULL (all defaults).
+ * Returns WG_OK, WG_ERR_INVALID_ARGUMENT or WG_ERR_NOT_SUPPORTED.  Host only. */
+WG_API int wg_workspace_size(const wg_problem* p, const wg_options* opt, size_t* bytes);
+
+/* Compute dW for problem p on `stream`.
+ *  x:  input activations, in_dtype, layout N(D)(H)WGC
+ *  dy: output gradient,   in_dtype, layout N(Do)(Ho)WoGK
+ *  dw: weight gradient,  out_dtype, layout GK(Z)(Y)XC — overwritten
+ *  workspace / ws_bytes: at least wg_workspace_size bytes (may be NULL when that is 0)
+ * Returns WG_OK or an error status; nothing is launched on an error. */
+WG_API int wg_conv_bwd_weight(const wg_problem* p, const void* x, const void* dy, void* dw, const wg_options* opt,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, then read and clear the device status word that the
+ * kernels set when a bounded wait runs out.  Returns WG_OK,
+ * WG_ERR_DEVICE_TIMEOUT or WG_ERR_CUDA. */
+WG_API int wg_check_status(void* stream);
+
+/* Human-readable plan for (p, opt): kernel, tiles, split degree, mode, grid,
+ * shared memory, workspace.  Writes at most n bytes including the NUL.
+ * Returns WG_OK or a validation status.  Host only. */
+WG_API int wg_plan_string(const wg_problem* p, const wg_options* opt, char* buf, size_t n);
+
+/* Static name of a status code. */
+WG_API const char* wg_status_string(int status);
+
+/* One-line reason for the last non-zero return on the calling thread. */
+WG_API const char* wg_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WGRAD_H */

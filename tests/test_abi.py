@@ -1,0 +1,118 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for sm_103a,
+loads, exports every symbol include/wgrad.h declares, and validates arguments
+before touching the device.  Only calls that fail validation are made here, so
+nothing is ever launched."""
+import os
+import re
+
+import pytest
+
+import oracle
+
+from implicit_gemm_gb300 import binding, build
+from tests.common import WORKLOADS, spec
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def header_symbols():
+    with open(os.path.join(ROOT, "include", "wgrad.h")) as f:
+        txt = f.read()
+    return sorted(set(re.findall(r"WG_API\s+[\w\s\*]+?\b(wg_\w+)\s*\(", txt)))
+
+
+def test_exports_every_declared_symbol(lib):
+    syms = header_symbols()
+    assert set(syms) == set(binding.EXPORTS), syms
+    for s in syms:
+        assert hasattr(lib, s), s
+
+
+def test_status_strings(lib):
+    for code, name in binding.STATUS.items():
+        assert binding.wg_status_string(code) == name
+
+
+def test_normalize_derives_output():
+    assert binding.wg_problem_normalize(spec(2, 1, 1, 1, 1, [8, 8], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])) == [8, 8]
+    assert binding.wg_problem_normalize(spec(3, 1, 4, 8, 8, [16, 16, 16], [3, 3, 3], [2, 2, 2], [1, 1, 1], [1, 1, 1],
+                                             [1, 1, 1])) == [8, 8, 8]
+    for sp in (spec(1, 1, 1, 8, 8, [11], [3], [2], [2], [2], [0]), spec(2, 1, 1, 8, 8, [7, 13], [2, 5], [3, 2], [2, 1],
+                                                                     [0, 2], [3, 1])):
+        assert binding.wg_problem_normalize(sp) == oracle.out_dims(sp)
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(ndim=4), 1), (dict(G=0), 1), (dict(N=-1), 1), (dict(C=0), 1),
+    (dict(filt=[11, 3]), 1), (dict(stride=[0, 1]), 1), (dict(dil=[1, 0]), 1), (dict(pad_l=[-1, 0]), 1),
+    (dict(out=[7, 8]), 1), (dict(in_dtype="fp32"), 1),
+])
+def test_invalid_arguments(bad, status):
+    s = spec(2, 1, 1, 16, 16, [8, 8], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])
+    s.update(bad)
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_workspace_size(s)
+    assert e.value.status == status
+
+
+def test_not_supported_paths():
+    s = spec(2, 1, 1, 4, 4, [8, 8], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])  # G*C = 4: rows not 16 bytes
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_workspace_size(s)
+    assert e.value.status == 2
+    s = spec(2, 1, 1, 16, 16, [8, 8], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], out_dtype="bf16")
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_workspace_size(s, split_k=2, mode="atomic")  # fp32 atomics only
+    assert e.value.status == 2
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_workspace_size(s, group_merge=2)  # merge degree is a depthwise option
+    assert e.value.status == 2
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_workspace_size(s, split_k=2, mode="direct")
+    assert e.value.status == 1
+
+
+def test_workspace_sizes():
+    sp = WORKLOADS["2d_dense_n32_h56_c64_k64"][0]
+    E = 1 * 64 * 9 * 64
+    assert binding.wg_workspace_size(sp, split_k=1) == 0
+    assert binding.wg_workspace_size(sp, split_k=4, mode="deterministic") == 4 * E * 4
+    sp5 = WORKLOADS["3d_n4_d16_c128_k96_s2"][0]
+    assert binding.wg_workspace_size(sp5, split_k=8, mode="atomic") == 0
+    assert binding.wg_workspace_size(sp5, split_k=8, mode="deterministic") == 8 * 96 * 27 * 128 * 4
+
+
+def test_launch_argument_checks_before_device(lib):
+    sp = spec(2, 1, 1, 16, 16, [8, 8], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_conv_bwd_weight(sp, 0, 4096, 8192)
+    assert e.value.status == 1
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_conv_bwd_weight(sp, 4096 + 8, 8192, 12288)
+    assert e.value.status == 3
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_conv_bwd_weight(sp, 4096, 8192, 12288, split_k=3, mode="deterministic")
+    assert e.value.status == 4
+    assert "workspace" in binding.wg_last_error()
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_plans_for_workloads(name):
+    sp = WORKLOADS[name][0]
+    ps = binding.wg_plan_string(sp)
+    kind = "depthwise" if sp["C"] == 1 and sp["K"] == 1 else "igemm_tcgen05"
+    assert f"kernel={kind}" in ps
+    m = re.search(r"smem=(\d+)", ps)
+    assert int(m.group(1)) <= 232448
+
+
+def test_depthwise_merge_degrees():
+    sp = WORKLOADS["2d_depthwise_g512_n64_h28"][0]
+    for gm in (1, 2, 4, 8):
+        assert f"Gm={gm} " in binding.wg_plan_string(sp, group_merge=gm)

@@ -1,0 +1,172 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, element by element.
+
+* every full-size workload in the launch configurations the bench times (and the
+  other listed modes), every element compared;
+* small problems spanning several tiles and ragged tails over 1-D/2-D/3-D,
+  strides, dilations, asymmetric pads, group sizes (cpg 4, 8, 12, 24, 64, 128),
+  16-bit outputs, both input dtypes and every split mode;
+* integer-valued inputs (exact in bf16/fp16, partial sums below 2^24): the GPU
+  result must equal the oracle bit for bit in every mode;
+* deterministic split-K repeats bitwise; dW pre-filled with NaN must come back
+  fully written.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from implicit_gemm_gb300 import binding, build
+from tests.common import WORKLOADS, assert_close, make_inputs, spec, workload_inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    build.build()
+    binding.load()
+
+
+def to_dev(bits, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
+    return t.view(torch.bfloat16 if dtype == "bf16" else torch.float16)
+
+
+_TDT = {"fp32": "float32", "bf16": "bfloat16", "fp16": "float16"}
+
+
+def run_gpu(sp, x, dy, split_k=0, mode="auto", gm=0, xd=None, dyd=None):
+    xd = to_dev(x, sp["in_dtype"]) if xd is None else xd
+    dyd = to_dev(dy, sp["in_dtype"]) if dyd is None else dyd
+    out = torch.full((sp["G"], sp["K"], *sp["filt"], sp["C"]), float("nan"),
+                     dtype=getattr(torch, _TDT[sp["out_dtype"]]), device="cuda")
+    binding.conv_bwd_weight(sp, xd, dyd, split_k, mode, gm, out=out)
+    binding.wg_check_status()
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+def ref(sp, x, dy):
+    dt = sp["in_dtype"]
+    return oracle.wgrad(sp, oracle.decode(x, dt), oracle.decode(dy, dt))
+
+
+_WCACHE = {}
+
+
+def workload(name):
+    if name not in _WCACHE:
+        sp, (x, dy) = workload_inputs(name)
+        _WCACHE.clear()
+        _WCACHE[name] = (sp, x, dy, ref(sp, x, dy))
+    return _WCACHE[name]
+
+
+WORKLOAD_MODES = [
+    ("2d_tiny_n1_h8_c16_k32", 0, "auto", 0),
+    ("2d_dense_n32_h56_c64_k64", 1, "direct", 0),
+    ("2d_dense_n32_h56_c64_k64", 4, "deterministic", 0),
+    ("2d_dense_n32_h56_c64_k64", 0, "auto", 0),
+    ("2d_grouped_g32_c8_k8_n32_h28", 0, "auto", 0),
+    ("2d_grouped_g32_c8_k8_n32_h28", 0, "atomic", 0),
+    ("2d_depthwise_g512_n64_h28", 0, "auto", 1),
+    ("2d_depthwise_g512_n64_h28", 0, "auto", 2),
+    ("2d_depthwise_g512_n64_h28", 0, "auto", 4),
+    ("2d_depthwise_g512_n64_h28", 0, "auto", 8),
+    ("2d_depthwise_g512_n64_h28", 0, "atomic", 8),
+    ("2d_depthwise_g512_n64_h28", 1, "direct", 8),
+    ("3d_n4_d16_c128_k96_s2", 8, "atomic", 0),
+    ("3d_n4_d16_c128_k96_s2", 8, "deterministic", 0),
+    ("3d_n4_d16_c128_k96_s2", 0, "auto", 0),
+]
+
+
+@pytest.mark.parametrize("name,split_k,mode,gm", WORKLOAD_MODES,
+                         ids=[f"{w[0]}-S{w[1]}-{w[2]}-gm{w[3]}" for w in WORKLOAD_MODES])
+def test_workload_full(name, split_k, mode, gm):
+    sp, x, dy, (dw, A) = workload(name)
+    got = run_gpu(sp, x, dy, split_k, mode, gm)
+    assert_close(got, dw, A, sp["out_dtype"], f"{name} S={split_k} {mode} gm={gm}")
+
+
+SMALL = [
+    # (spec, modes)
+    spec(2, 1, 2, 16, 16, [9, 11], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
+    spec(2, 1, 3, 64, 64, [13, 10], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], out_dtype="bf16"),
+    spec(2, 1, 2, 128, 32, [7, 9], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
+    spec(2, 1, 2, 24, 40, [10, 7], [3, 2], [2, 1], [1, 2], [0, 1], [2, 0]),
+    spec(2, 4, 2, 4, 4, [6, 9], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
+    spec(2, 2, 2, 12, 12, [7, 7], [3, 3], [1, 1], [2, 2], [2, 2], [2, 2]),
+    spec(2, 6, 1, 8, 16, [8, 12], [1, 1]),
+    spec(2, 3, 2, 24, 8, [11, 6], [5, 3], [2, 2], [1, 1], [2, 1], [2, 1], in_dtype="fp16", out_dtype="fp16"),
+    spec(2, 2, 2, 64, 72, [6, 6], [2, 2], [3, 3], [1, 1], [0, 1], [1, 0]),
+    spec(1, 2, 3, 16, 8, [37], [5], [1], [2], [3], [1]),
+    spec(1, 1, 2, 48, 24, [29], [3], [2], [1], [1], [0], in_dtype="fp16"),
+    spec(3, 1, 2, 32, 16, [5, 6, 7], [3, 3, 3], [1, 1, 1], [1, 1, 1], [1, 1, 1], [1, 1, 1]),
+    spec(3, 2, 1, 8, 8, [7, 6, 9], [2, 3, 3], [2, 1, 2], [1, 2, 1], [0, 1, 1], [1, 1, 0]),
+    spec(3, 1, 3, 128, 96, [9, 9, 9], [3, 3, 3], [2, 2, 2], [1, 1, 1], [1, 1, 1], [1, 1, 1], in_dtype="fp16"),
+    # depthwise: fast 3x3 window, generic taps, stride, ragged channel block, 1-D
+    spec(2, 64, 2, 1, 1, [9, 13], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
+    spec(2, 72, 3, 1, 1, [10, 7], [3, 2], [2, 1], [1, 2], [1, 0], [0, 1]),
+    spec(2, 16, 2, 1, 1, [8, 9], [1, 3], [1, 2], [1, 1], [0, 1], [0, 1], in_dtype="fp16", out_dtype="bf16"),
+    spec(1, 24, 3, 1, 1, [40], [3], [1], [1], [1], [1]),
+    spec(3, 8, 2, 1, 1, [5, 5, 5], [3, 3, 3], [1, 1, 1], [1, 1, 1], [1, 1, 1], [1, 1, 1]),
+]
+MODES = [(0, "auto"), (1, "direct"), (3, "deterministic"), (5, "atomic"), (64, "deterministic")]
+
+
+def _ids(sp):
+    return (f"{sp['ndim']}d_G{sp['G']}_C{sp['C']}_K{sp['K']}_in{'x'.join(map(str, sp['in']))}_f"
+            f"{'x'.join(map(str, sp['filt']))}_s{''.join(map(str, sp['stride']))}_{sp['in_dtype']}_{sp['out_dtype']}")
+
+
+@pytest.mark.parametrize("sp", SMALL, ids=_ids)
+def test_small_problems_all_modes(sp):
+    x, dy = make_inputs(sp, ("uniform", -1.0, 1.0), 7, 8)
+    dw, A = ref(sp, x, dy)
+    for split_k, mode in MODES:
+        if mode == "atomic" and sp["out_dtype"] != "fp32":
+            continue
+        got = run_gpu(sp, x, dy, split_k, mode)
+        assert_close(got, dw, A, sp["out_dtype"], f"{_ids(sp)} S={split_k} {mode}")
+
+
+@pytest.mark.parametrize("sp", [SMALL[0], SMALL[3], SMALL[4], SMALL[10], SMALL[12], SMALL[14], SMALL[15]], ids=_ids)
+def test_integer_inputs_bitwise(sp):
+    x, dy = make_inputs(sp, ("int", -2, 2), 17, 18)
+    dw, _ = ref(sp, x, dy)
+    assert np.all(np.abs(dw) < 2 ** 24)
+    for split_k, mode in MODES:
+        got = run_gpu(sp, x, dy, split_k, mode)
+        np.testing.assert_array_equal(got, dw, err_msg=f"{_ids(sp)} S={split_k} {mode}")
+
+
+@pytest.mark.parametrize("gm", [1, 2, 4, 8])
+def test_depthwise_merge_degrees_bitwise_equal(gm):
+    sp = spec(2, 64, 3, 1, 1, [11, 9], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])
+    x, dy = make_inputs(sp, ("int", -2, 2), 27, 28)
+    dw, _ = ref(sp, x, dy)
+    got = run_gpu(sp, x, dy, 3, "deterministic", gm)
+    np.testing.assert_array_equal(got, dw)
+
+
+@pytest.mark.parametrize("name", ["2d_dense_n32_h56_c64_k64", "2d_depthwise_g512_n64_h28", "3d_n4_d16_c128_k96_s2"])
+def test_deterministic_mode_repeats_bitwise(name):
+    sp, x, dy, _ = workload(name)
+    xd, dyd = to_dev(x, sp["in_dtype"]), to_dev(dy, sp["in_dtype"])
+    a = run_gpu(sp, x, dy, 0, "deterministic", xd=xd, dyd=dyd)
+    b = run_gpu(sp, x, dy, 0, "deterministic", xd=xd, dyd=dyd)
+    assert np.array_equal(a.view(np.int64), b.view(np.int64))
+
+
+def test_more_splits_than_tiles():
+    sp = spec(2, 1, 1, 16, 32, [8, 8], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])
+    x, dy = make_inputs(sp, ("int", -2, 2), 37, 38)
+    dw, _ = ref(sp, x, dy)
+    for mode in ("deterministic", "atomic"):
+        got = run_gpu(sp, x, dy, 7, mode)
+        np.testing.assert_array_equal(got, dw)
+
+
+def test_status_clear_after_runs():
+    binding.wg_check_status()

@@ -5,7 +5,10 @@
 
 A step is one call of wg_conv_bwd_weight -- the whole path: every launch it makes
 (split-K stage 1, the stage-2 reduce or the atomic-mode memset) -- over one batch
-of synthetic, seeded inputs already resident in HBM.  The headline workload is
+of synthetic, seeded inputs already resident in HBM.  For the device-side value
+the call's launches are captured once into a CUDA graph and replayed per step,
+so host-side argument handling is not inside the timed events; the e2e value
+times the plain C-ABI call with host buffers instead.  The headline workload is
 the 2-D dense 56x56, C = K = 64, N = 32, 3x3 problem with bf16 inputs and bf16
 dW; the other workloads are reported under "workloads".  L2 is flushed (a 256 MiB
 write) before every timed step, outside the timed events.
@@ -148,8 +151,8 @@ def run_reference(args, ws, rank):
     if rank != 0:
         return
     sp = dict(WORKLOADS[args.workload][0])
-    # A bounded sample of the workload: 2 of the batch's images per step.
-    nsample = min(2, sp["N"])
+    # A bounded sample of the workload: one of the batch's images per step.
+    nsample = 1
     sps = dict(sp, N=nsample)
     dist, seed = WORKLOADS[args.workload][1], WORKLOADS[args.workload][2]
     s = sizes(sps)
@@ -209,15 +212,29 @@ class Workload:
         self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device="cuda")
         self.plan = binding.wg_plan_string(sp, self.split_k, self.mode, self.gm)
         self.launches_per_step = 1 + (1 if "mode=deterministic" in self.plan else 0)
+        self.call = binding.PreparedCall(sp, self.x, self.dy, self.dw, self.split_k, self.mode, self.gm, self.ws,
+                                         self.ws_bytes)
+        self.graph = None
+
+    def capture(self, stream):
+        """Capture one step (every launch of the call) into a CUDA graph."""
+        torch = self.torch
+        with torch.cuda.stream(stream):
+            self.call(stream.cuda_stream)  # first call: plan, tensor maps, kernel attributes
+        stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=stream):
+            self.call(stream.cuda_stream)
+        stream.synchronize()
 
     def step(self, stream):
-        binding.wg_conv_bwd_weight(self.sp, self.x, self.dy, self.dw, self.split_k, self.mode, self.gm, self.ws,
-                                   self.ws_bytes, stream)
+        self.graph.replay()
 
     def e2e_step(self, stream):
+        # The public call itself (no graph), with host<->device copies.
         self.x.copy_(self.x_host, non_blocking=True)
         self.dy.copy_(self.dy_host, non_blocking=True)
-        self.step(stream)
+        self.call(stream.cuda_stream)
         self.dw_host.copy_(self.dw, non_blocking=True)
 
 
@@ -272,6 +289,7 @@ def main():
     pk = peaks()
 
     wl = Workload(torch, args.workload)
+    wl.capture(stream)
     sampler = ClockSampler(local)
     if pg:
         pg.barrier()
@@ -314,7 +332,7 @@ def main():
     roof["traffic"] = None
     roof["peak_source"] = pk["src"]
     roof["kernel"] = "igemm_wgrad_kernel" if "igemm" in wl.plan else "depthwise_wgrad_kernel"
-    roof["timed"] = "whole step (all launches of the call) with CUDA events"
+    roof["timed"] = "whole step (graph replay of every launch of the call) with CUDA events"
 
     extra = {}
     if rank == 0 and not args.no_extra:
@@ -322,6 +340,7 @@ def main():
             if name == args.workload:
                 continue
             w2 = Workload(torch, name)
+            w2.capture(stream)
             tt = time_steps(torch, w2, 300, 10, flush, stream)
             ms = float(np.mean(tt))
             s2 = w2.s

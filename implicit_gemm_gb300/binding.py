@@ -143,6 +143,27 @@ def wg_conv_bwd_weight(spec: dict, x, dy, dw, split_k: int = 0, mode: str = "aut
                                      _addr(workspace), int(ws_bytes), _stream_handle(stream)))
 
 
+class PreparedCall:
+    """wg_conv_bwd_weight with its arguments marshalled once: calling it makes one
+    ctypes call.  Keeps references to the tensors it was built from."""
+
+    def __init__(self, spec: dict, x, dy, dw, split_k: int = 0, mode: str = "auto", group_merge: int = 0,
+                 workspace=None, ws_bytes: int | None = None):
+        self._keep = (x, dy, dw, workspace)
+        self.p, self.o = make_problem(spec), make_options(split_k, mode, group_merge)
+        if ws_bytes is None:
+            ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        self.fn = load().wg_conv_bwd_weight
+        self.args = (ctypes.byref(self.p), ctypes.c_void_p(_addr(x)), ctypes.c_void_p(_addr(dy)),
+                     ctypes.c_void_p(_addr(dw)), ctypes.byref(self.o), ctypes.c_void_p(_addr(workspace)),
+                     ctypes.c_size_t(int(ws_bytes)))
+
+    def __call__(self, stream_handle: int | None = None) -> None:
+        st = self.fn(*self.args, stream_handle)
+        if st:
+            _check(st)
+
+
 def wg_check_status(stream=None) -> None:
     _check(load().wg_check_status(_stream_handle(stream)))
 

@@ -132,7 +132,7 @@ int plan_igemm(Plan* pl, const wg_options& o, int num_sms, std::string* err)
     if (halo_ok && n_combos * ig.n_cchunks > kMaxPatches) halo_ok = false;
 
     const int avail = kMaxSmemPerCta - 3072;
-    const int mt_max = std::min(ig.n_mtiles, kMaxTmemCols / ig.Nt);
+    const int mt_max = std::min({ig.n_mtiles, kMaxTmemCols / ig.Nt, kMaxMtPerCta});
     IgCand best{};
     best.cost = -1;
     std::vector<std::array<int, 4>> tiles;

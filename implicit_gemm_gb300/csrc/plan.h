@@ -16,6 +16,7 @@ constexpr int kDefaultSMs = 152;        // GB300: 2 dies x 76 SMs
 constexpr int kMaxSmemPerCta = 232448;  // 227 KB opt-in dynamic shared memory
 constexpr int kMaxTmemCols = 512;
 constexpr int kMaxPatches = 32;
+constexpr int kMaxMtPerCta = 16;  // M-tiles one CTA accumulates (the kernel's register table size)
 constexpr int kMaxHaloAtoms = 256;
 constexpr int kMaxHaloFilter = 32;
 

@@ -67,7 +67,7 @@ int num_sms()
 
 // Plans are a pure function of (problem, options, SM count); successful ones
 // are cached so that repeated calls skip the tile search.
-int plan_for(const wg_problem* p, const wg_options* opt, wg::Plan* pl)
+int plan_for(const wg_problem* p, const wg_options* opt, wg::Plan* pl, std::string* key_out = nullptr)
 {
     static std::mutex mu;
     static std::map<std::string, wg::Plan> cache;
@@ -83,6 +83,7 @@ int plan_for(const wg_problem* p, const wg_options* opt, wg::Plan* pl)
         auto it = cache.find(key);
         if (it != cache.end()) {
             *pl = it->second;
+            if (key_out) *key_out = key;
             return WG_OK;
         }
     }
@@ -92,6 +93,7 @@ int plan_for(const wg_problem* p, const wg_options* opt, wg::Plan* pl)
     std::lock_guard<std::mutex> lk(mu);
     if (cache.size() > 1024) cache.clear();
     cache.emplace(key, *pl);
+    if (key_out) *key_out = key;
     return WG_OK;
 }
 
@@ -120,21 +122,57 @@ int encode(CUtensorMap* tm, int in_dtype, void* base, const cuuint64_t dims[5], 
     return WG_OK;
 }
 
+// Raise a kernel's dynamic shared-memory limit when a launch needs more than
+// any earlier one (per device).
 template <typename K>
 int ensure_smem(K kernel, int bytes)
 {
-    // Idempotent and cheap; set per call so a kernel first used with a small
-    // configuration still accepts a larger one later.
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> done;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = done.find(key);
+    if (it != done.end() && it->second >= bytes) return WG_OK;
     const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", e);
+    done[key] = bytes;
     return WG_OK;
 }
 
-int launch_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, void* ws, cudaStream_t stream)
+// Encoded tensor maps and kernel parameters of one (plan, buffers) pair, kept
+// so that a repeated call only launches.
+struct Prepared {
+    CUtensorMap tmx, tmy;
+    wg::IgParams ig;
+    wg::DwParams dw;
+};
+
+std::mutex g_prep_mu;
+std::map<std::string, Prepared>& prep_cache()
+{
+    static std::map<std::string, Prepared> m;
+    return m;
+}
+
+std::string prep_key(const std::string& plan_key, const void* x, const void* dy, const void* dw, const void* ws)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const void* ptrs[4] = {x, dy, dw, ws};
+    std::string k = plan_key;
+    k.append(reinterpret_cast<const char*>(ptrs), sizeof ptrs);
+    k.append(reinterpret_cast<const char*>(&dev), sizeof dev);
+    return k;
+}
+
+int prepare_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, void* ws, Prepared* out)
 {
     const wg::Problem& pb = pl.pb;
     const wg::IgemmPlan& ig = pl.ig;
-    CUtensorMap tmx, tmy;
+    CUtensorMap& tmx = out->tmx;
+    CUtensorMap& tmy = out->tmy;
     const cuuint64_t GC = (cuuint64_t)pb.G * pb.C, GK = (cuuint64_t)pb.G * pb.K;
     {
         const cuuint64_t dims[5] = {GC, (cuuint64_t)pb.in[2], (cuuint64_t)pb.in[1], (cuuint64_t)pb.in[0],
@@ -154,7 +192,7 @@ int launch_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, vo
         const int st = encode(&tmy, pb.in_dtype, const_cast<void*>(dy), dims, box, estr, CU_TENSOR_MAP_SWIZZLE_128B, "dY");
         if (st) return st;
     }
-    wg::IgParams prm;
+    wg::IgParams& prm = out->ig;
     memset(&prm, 0, sizeof prm);
     prm.G = pb.G, prm.C = pb.C, prm.K = pb.K, prm.T = (int)pb.T, prm.GC = (int)GC, prm.GK = (int)GK;
     prm.X = pb.filt[2], prm.Y = pb.filt[1];
@@ -187,22 +225,37 @@ int launch_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, vo
             prm.atom_cc[i] = ig.atom_cc[i];
         }
     }
+    return WG_OK;
+}
+
+int launch_reduce(const wg::Problem& pb, int S, void* ws, void* dw, cudaStream_t stream)
+{
+    const long long n = (pb.dw_elems & 3) ? pb.dw_elems : pb.dw_elems / 4;
+    const long long blocks = (n + wg::kRedVecs - 1) / wg::kRedVecs;
+    wg::reduce_splits_kernel<<<(unsigned)blocks, dim3(wg::kRedVecs, wg::kRedLanes), 0, stream>>>(
+        static_cast<const float*>(ws), dw, pb.dw_elems, S, pb.out_dtype);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail("reduce_splits_kernel launch", e);
+    return WG_OK;
+}
+
+int launch_igemm(const wg::Plan& pl, const Prepared& pr, void* dw, void* ws, cudaStream_t stream)
+{
+    const wg::Problem& pb = pl.pb;
+    const wg::IgemmPlan& ig = pl.ig;
     int st = ensure_smem(wg::igemm_wgrad_kernel, ig.smem_bytes);
     if (st) return st;
     if (pl.mode == wg::MODE_ATOMIC) {
         const cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)pb.dw_elems * 4, stream);
         if (e != cudaSuccess) return cuda_fail("cudaMemsetAsync(dW)", e);
     }
-    wg::igemm_wgrad_kernel<<<dim3(pl.grid[0], pl.grid[1], pl.grid[2]), pl.block, ig.smem_bytes, stream>>>(tmx, tmy, prm);
+    wg::igemm_wgrad_kernel<<<dim3(pl.grid[0], pl.grid[1], pl.grid[2]), pl.block, ig.smem_bytes, stream>>>(pr.tmx, pr.tmy,
+                                                                                                          pr.ig);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail("igemm_wgrad_kernel launch", e);
     if (pl.mode == wg::MODE_DETERMINISTIC) {
-        const long long work = (pb.dw_elems & 3) ? pb.dw_elems : pb.dw_elems / 4;
-        const int blocks = (int)std::min<long long>((work + 255) / 256, 4LL * num_sms());
-        wg::reduce_splits_kernel<<<blocks, 256, 0, stream>>>(static_cast<const float*>(ws), dw, pb.dw_elems, pl.S,
-                                                             pb.out_dtype);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return cuda_fail("reduce_splits_kernel launch", e);
+        st = launch_reduce(pb, pl.S, ws, dw, stream);
+        if (st) return st;
     }
     return WG_OK;
 }
@@ -238,11 +291,12 @@ int launch_dw_b(const wg::Plan& pl, const CUtensorMap& a, const CUtensorMap& b, 
     }
 }
 
-int launch_depthwise(const wg::Plan& pl, const void* x, const void* dy, void* dw, void* ws, cudaStream_t stream)
+int prepare_depthwise(const wg::Plan& pl, const void* x, const void* dy, void* dw, void* ws, Prepared* out)
 {
     const wg::Problem& pb = pl.pb;
     const wg::DwPlan& d = pl.dw;
-    CUtensorMap tmx, tmy;
+    CUtensorMap& tmx = out->tmx;
+    CUtensorMap& tmy = out->tmy;
     {
         const cuuint64_t dims[5] = {(cuuint64_t)pb.G, (cuuint64_t)pb.in[2], (cuuint64_t)pb.in[1], 1, (cuuint64_t)pb.N};
         const cuuint32_t box[5] = {(cuuint32_t)d.CB, (cuuint32_t)d.xw, (cuuint32_t)d.xh, 1, 1};
@@ -257,7 +311,7 @@ int launch_depthwise(const wg::Plan& pl, const void* x, const void* dy, void* dw
         const int st = encode(&tmy, pb.in_dtype, const_cast<void*>(dy), dims, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE, "dY");
         if (st) return st;
     }
-    wg::DwParams prm;
+    wg::DwParams& prm = out->dw;
     memset(&prm, 0, sizeof prm);
     prm.G = pb.G, prm.Ho = pb.out[1], prm.Wo = pb.out[2], prm.Y = pb.filt[1], prm.X = pb.filt[2], prm.T = (int)pb.T;
     prm.sh = pb.stride[1], prm.sw = pb.stride[2], prm.dh = pb.dil[1], prm.dw = pb.dil[2];
@@ -273,20 +327,22 @@ int launch_depthwise(const wg::Plan& pl, const void* x, const void* dy, void* dw
     prm.mode = pl.mode, prm.out_dtype = pb.out_dtype;
     prm.out = pl.mode == wg::MODE_DETERMINISTIC ? ws : dw;
     prm.split_stride = pb.dw_elems;
+    return WG_OK;
+}
+
+int launch_depthwise(const wg::Plan& pl, const Prepared& pr, void* dw, void* ws, cudaStream_t stream)
+{
+    const wg::Problem& pb = pl.pb;
     if (pl.mode == wg::MODE_ATOMIC) {
         const cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)pb.dw_elems * 4, stream);
         if (e != cudaSuccess) return cuda_fail("cudaMemsetAsync(dW)", e);
     }
-    int st = pb.in_dtype == WG_BF16 ? launch_dw_b<true>(pl, tmx, tmy, prm, stream)
-                                    : launch_dw_b<false>(pl, tmx, tmy, prm, stream);
+    int st = pb.in_dtype == WG_BF16 ? launch_dw_b<true>(pl, pr.tmx, pr.tmy, pr.dw, stream)
+                                    : launch_dw_b<false>(pl, pr.tmx, pr.tmy, pr.dw, stream);
     if (st) return st;
     if (pl.mode == wg::MODE_DETERMINISTIC) {
-        const long long work = (pb.dw_elems & 3) ? pb.dw_elems : pb.dw_elems / 4;
-        const int blocks = (int)std::min<long long>((work + 255) / 256, 4LL * num_sms());
-        wg::reduce_splits_kernel<<<blocks, 256, 0, stream>>>(static_cast<const float*>(ws), dw, pb.dw_elems, pl.S,
-                                                             pb.out_dtype);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return cuda_fail("reduce_splits_kernel launch", e);
+        st = launch_reduce(pb, pl.S, ws, dw, stream);
+        if (st) return st;
     }
     return WG_OK;
 }
@@ -345,7 +401,8 @@ int wg_conv_bwd_weight(const wg_problem* p, const void* x, const void* dy, void*
                        void* workspace, size_t ws_bytes, void* stream)
 {
     wg::Plan pl;
-    int st = plan_for(p, opt, &pl);
+    std::string pkey;
+    int st = plan_for(p, opt, &pl, &pkey);
     if (st) return st;
     if (!x || !dy || !dw) return set_err(WG_ERR_INVALID_ARGUMENT, "x, dy and dw must be non-NULL device pointers");
     if (!aligned16(x) || !aligned16(dy) || !aligned16(dw))
@@ -360,8 +417,24 @@ int wg_conv_bwd_weight(const wg_problem* p, const void* x, const void* dy, void*
         if (!aligned16(workspace)) return set_err(WG_ERR_MISALIGNED, "workspace must be 16-byte aligned");
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    st = pl.kind == wg::KIND_IGEMM ? launch_igemm(pl, x, dy, dw, workspace, s)
-                                   : launch_depthwise(pl, x, dy, dw, workspace, s);
+    const void* ws_used = pl.ws_bytes > 0 ? workspace : nullptr;
+    const std::string key = prep_key(pkey, x, dy, dw, ws_used);
+    Prepared pr;
+    bool hit = false;
+    {
+        std::lock_guard<std::mutex> lk(g_prep_mu);
+        auto it = prep_cache().find(key);
+        if (it != prep_cache().end()) pr = it->second, hit = true;
+    }
+    if (!hit) {
+        st = pl.kind == wg::KIND_IGEMM ? prepare_igemm(pl, x, dy, dw, workspace, &pr)
+                                       : prepare_depthwise(pl, x, dy, dw, workspace, &pr);
+        if (st) return st;
+        std::lock_guard<std::mutex> lk(g_prep_mu);
+        if (prep_cache().size() > 256) prep_cache().clear();
+        prep_cache().emplace(key, pr);
+    }
+    st = pl.kind == wg::KIND_IGEMM ? launch_igemm(pl, pr, dw, workspace, s) : launch_depthwise(pl, pr, dw, workspace, s);
     return st;
 }
 

@@ -42,7 +42,7 @@ class WgradError(RuntimeError):
 
 
 EXPORTS = ("wg_problem_normalize", "wg_workspace_size", "wg_conv_bwd_weight", "wg_check_status",
-           "wg_plan_string", "wg_status_string", "wg_last_error")
+           "wg_plan_string", "wg_status_string", "wg_last_error", "wg_conv_bwd_weight_noalloc")
 
 _lib = None
 _lock = threading.Lock()
@@ -66,6 +66,8 @@ def load():
             lib.wg_workspace_size.argtypes = [P, O, ctypes.POINTER(ctypes.c_size_t)]
             lib.wg_conv_bwd_weight.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, O,
                                                ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+            lib.wg_conv_bwd_weight_noalloc.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, O,
+                                                       ctypes.c_void_p]
             lib.wg_check_status.argtypes = [ctypes.c_void_p]
             lib.wg_plan_string.argtypes = [P, O, ctypes.c_char_p, ctypes.c_size_t]
             lib.wg_status_string.argtypes = [ctypes.c_int]
@@ -162,6 +164,15 @@ class PreparedCall:
         st = self.fn(*self.args, stream_handle)
         if st:
             _check(st)
+
+
+def wg_conv_bwd_weight_noalloc(spec: dict, x, dy, dw, split_k: int = 0, mode: str = "auto", group_merge: int = 0,
+                               stream=None) -> None:
+    """wg_conv_bwd_weight for callers that cannot allocate: the split-K workspace comes
+    from the library's own 16 MiB device array (see include/wgrad.h)."""
+    p, o = make_problem(spec), make_options(split_k, mode, group_merge)
+    _check(load().wg_conv_bwd_weight_noalloc(ctypes.byref(p), _addr(x), _addr(dy), _addr(dw), ctypes.byref(o),
+                                             _stream_handle(stream)))
 
 
 def wg_check_status(stream=None) -> None:

@@ -455,3 +455,81 @@ int wg_check_status(void* stream)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Entry point for callers that cannot allocate device memory.
+//
+// wg_conv_bwd_weight takes its split-K workspace from the caller.  Some callers
+// cannot provide one: a plug-in whose host application owns every device
+// allocation through its own allocator, code running under a fixed device
+// memory budget, or a latency-critical path where cudaMalloc's implicit
+// synchronisation is not acceptable.  For them the workspace comes from the
+// file-scope array below, which every GPU that loads this library holds until
+// the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+int noalloc_scratch(void** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+    if (dev < 0 || dev >= kMaxDevices) return set_err(WG_ERR_NOT_SUPPORTED, "device ordinal above 63");
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress(scratch)", e);
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return WG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int wg_conv_bwd_weight_noalloc(const wg_problem* p, const void* x, const void* dy, void* dw, const wg_options* opt,
+                               void* stream)
+{
+    void* scratch = nullptr;
+    int st = noalloc_scratch(&scratch);
+    if (st) return st;
+    wg_options o{0, WG_MODE_AUTO, 0};
+    if (opt) o = *opt;
+    size_t need = 0;
+    st = wg_workspace_size(p, &o, &need);
+    if (st) return st;
+    if (need > kNoAllocScratchBytes) {
+        wg::Problem pb;
+        std::string err;
+        if (wg::normalize(p, &pb, &err)) return set_err(WG_ERR_INVALID_ARGUMENT, err);
+        const size_t per_split = (size_t)pb.dw_elems * 4;
+        const size_t fit = kNoAllocScratchBytes / per_split;
+        if (o.split_k != 0 || fit < 2) {
+            char buf[256];
+            snprintf(buf, sizeof buf,
+                     "the no-allocation entry point has %zu bytes of scratch; this problem and split degree need %zu",
+                     kNoAllocScratchBytes, need);
+            return set_err(WG_ERR_WORKSPACE, buf);
+        }
+        // Automatic split degree: the largest that fits the scratch array.
+        o.split_k = (int)std::min<size_t>(fit, 65535);
+        st = wg_workspace_size(p, &o, &need);
+        if (st) return st;
+        if (need > kNoAllocScratchBytes) return set_err(WG_ERR_WORKSPACE, "split-K workspace does not fit the scratch array");
+    }
+    return wg_conv_bwd_weight(p, x, dy, dw, &o, need ? scratch : nullptr, need ? kNoAllocScratchBytes : 0, stream);
+}
+
+}  // extern "C"

@@ -139,6 +139,31 @@ WG_API const char* wg_status_string(int status);
 /* One-line reason for the last non-zero return on the calling thread. */
 WG_API const char* wg_last_error(void);
 
+/* wg_conv_bwd_weight for callers that cannot allocate device memory (no
+ * counterpart in the CK page: it is a property of this library's API).
+ *
+ * Who needs it: wg_conv_bwd_weight asks the caller for the split-K workspace.
+ * A caller that cannot call cudaMalloc -- a plug-in whose host application owns
+ * all device memory through its own allocator, code held to a fixed device
+ * memory budget, a latency-critical path that cannot take cudaMalloc's implicit
+ * synchronisation -- cannot supply one.  This entry point takes the workspace
+ * from a 16 MiB array compiled into the library instead (every GPU that loads
+ * the library holds it until the process exits) and allocates nothing.
+ *
+ * Arguments and results are those of wg_conv_bwd_weight without the workspace.
+ * With split_k = 0 the split degree is capped so that the partial sums fit the
+ * array; an explicit split_k (or a dW too large for two splits) that needs more
+ * than 16 MiB returns WG_ERR_WORKSPACE with the sizes in wg_last_error().
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  All calls share the one array and it keeps the last call's
+ * contents; the kernels write every element they later read, so nothing needs
+ * clearing, but calls whose work overlaps on the GPU (other streams, other
+ * threads) race on it and must be serialised by the caller. */
+WG_API int wg_conv_bwd_weight_noalloc(const wg_problem* p, const void* x, const void* dy, void* dw,
+                                      const wg_options* opt, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -5,13 +5,15 @@
 
 A step is one call of wg_conv_bwd_weight -- the whole path: every launch it makes
 (split-K stage 1, the stage-2 reduce or the atomic-mode memset) -- over one batch
-of synthetic, seeded inputs already resident in HBM.  For the device-side value
-the call's launches are captured once into a CUDA graph and replayed per step,
-so host-side argument handling is not inside the timed events; the e2e value
-times the plain C-ABI call with host buffers instead.  The headline workload is
+of synthetic, seeded inputs already resident in HBM.  The device-side value
+times each call between CUDA events on its stream; the L2 flush in front of
+every step keeps the GPU busy long enough for the host to enqueue the call, so
+host-side time is not inside the events (--graph replays a captured CUDA graph
+of the call instead).  The e2e value times the same call with host buffers.  The headline workload is
 the 2-D dense 56x56, C = K = 64, N = 32, 3x3 problem with bf16 inputs and bf16
 dW; the other workloads are reported under "workloads".  L2 is flushed (a 256 MiB
-write) before every timed step, outside the timed events.
+write, then a 256 MiB read of another buffer so the write's dirty lines are
+written back before the timed events) before every timed step.
 
 Prints one JSON line on rank 0.  Multi-GPU runs (torchrun) are independent
 replicas (weak scaling): the path has no exchange step on one node.
@@ -228,7 +230,10 @@ class Workload:
         stream.synchronize()
 
     def step(self, stream):
-        self.graph.replay()
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self.call(stream.cuda_stream)
 
     def e2e_step(self, stream):
         # The public call itself (no graph), with host<->device copies.
@@ -238,17 +243,33 @@ class Workload:
         self.dw_host.copy_(self.dw, non_blocking=True)
 
 
+class L2Flush:
+    """Evicts the inputs from L2 between timed steps: writes a 256 MiB buffer (twice
+    the L2), then reads another 256 MiB buffer so that the write-back of the dirty
+    lines the write leaves behind happens here and not inside the next timed step."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device="cuda")
+        self.sink = torch.empty((), dtype=torch.int64, device="cuda")
+
+    def __call__(self):
+        self.w.zero_()
+        self.torch.sum(self.r, dim=0, out=self.sink)
+
+
 def time_steps(torch, wl, steps, warmup, flush, stream, e2e=False):
     """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each step."""
     fn = wl.e2e_step if e2e else wl.step
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            flush.zero_()
+            flush()
             fn(stream)
         stream.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for a, b in evs:
-            flush.zero_()
+            flush()
             a.record(stream)
             fn(stream)
             b.record(stream)
@@ -265,6 +286,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=HEADLINE, choices=list(WORKLOADS))
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads and the CPU baseline")
+    ap.add_argument("--graph", action="store_true", help="replay a CUDA graph of the call instead of calling it")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -285,11 +307,12 @@ def main():
     build.build()
     binding.load()
     stream = torch.cuda.Stream()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(torch)
     pk = peaks()
 
     wl = Workload(torch, args.workload)
-    wl.capture(stream)
+    if args.graph:
+        wl.capture(stream)
     sampler = ClockSampler(local)
     if pg:
         pg.barrier()
@@ -332,7 +355,8 @@ def main():
     roof["traffic"] = None
     roof["peak_source"] = pk["src"]
     roof["kernel"] = "igemm_wgrad_kernel" if "igemm" in wl.plan else "depthwise_wgrad_kernel"
-    roof["timed"] = "whole step (graph replay of every launch of the call) with CUDA events"
+    roof["timed"] = ("whole step (every launch of the call, " + ("graph replay" if args.graph else "direct call") +
+                     ") with CUDA events")
 
     extra = {}
     if rank == 0 and not args.no_extra:
@@ -340,7 +364,8 @@ def main():
             if name == args.workload:
                 continue
             w2 = Workload(torch, name)
-            w2.capture(stream)
+            if args.graph:
+                w2.capture(stream)
             tt = time_steps(torch, w2, 300, 10, flush, stream)
             ms = float(np.mean(tt))
             s2 = w2.s
@@ -360,7 +385,7 @@ def main():
                            "C": wl.sp["C"], "K": wl.sp["K"], "filt": wl.sp["filt"], "stride": wl.sp["stride"],
                            "pad": wl.sp["pad_l"], "in_dtype": wl.sp["in_dtype"], "out_dtype": wl.sp["out_dtype"],
                            "split_k": wl.split_k, "mode": wl.mode, "plan": wl.plan,
-                           "l2": "flushed by a 256 MiB write before every timed step (outside the events)",
+                           "l2": "flushed before every timed step (outside the events): write 256 MiB, then read another 256 MiB",
                            "parallelism": f"replicas x{ws}"},
                 "roofline": roof, "clocks": clocks, "gpu_launches": wl.launches_per_step * args.steps,
                 "e2e": {"value": ws * s["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",

@@ -75,8 +75,37 @@ __device__ __forceinline__ void load_vec(const uint16_t* p, float (&v)[GM])
     }
 }
 
+// One window column: the X vectors of the three filter rows at one input column.
+template <bool BF16, int GM>
+__device__ __forceinline__ void load_col3(const uint16_t* r0, const uint16_t* r1, const uint16_t* r2, int off,
+                                          float (&w)[3][GM])
+{
+    load_vec<BF16, GM>(r0 + off, w[0]);
+    load_vec<BF16, GM>(r1 + off, w[1]);
+    load_vec<BF16, GM>(r2 + off, w[2]);
+}
+
+// acc[y*3 + x] += dY(pixel) * X(row y, column x of the window (c0, c1, c2)).
+template <bool BF16, int GM>
+__device__ __forceinline__ void fma_col3(const uint16_t* dyp, const float (&c0)[3][GM], const float (&c1)[3][GM],
+                                         const float (&c2)[3][GM], float (&acc)[9][GM])
+{
+    float dy[GM];
+    load_vec<BF16, GM>(dyp, dy);
+#pragma unroll
+    for (int y = 0; y < 3; ++y)
+#pragma unroll
+        for (int j = 0; j < GM; ++j) {
+            acc[y * 3 + 0][j] = fmaf(dy[j], c0[y][j], acc[y * 3 + 0][j]);
+            acc[y * 3 + 1][j] = fmaf(dy[j], c1[y][j], acc[y * 3 + 1][j]);
+            acc[y * 3 + 2][j] = fmaf(dy[j], c2[y][j], acc[y * 3 + 2][j]);
+        }
+}
+
+// Vectors of 8 channels hold 72 accumulators plus a 72-register window: one CTA
+// per SM.  Narrower vectors fit two CTAs per SM.
 template <bool BF16, int GM, bool SLIDE3>
-__global__ void __launch_bounds__(288, 1)
+__global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
     depthwise_wgrad_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
                            const __grid_constant__ DwParams p)
 {
@@ -111,6 +140,7 @@ __global__ void __launch_bounds__(288, 1)
         for (int j = 0; j < GM; ++j) acc[t][j] = 0.f;
 
     const int NV = p.CB / GM;
+    const int CB = p.CB, Wo = p.Wo, xw = p.xw, sh = p.sh, dh = p.dh;
     if (warp == n_cwarps) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
@@ -135,13 +165,6 @@ __global__ void __launch_bounds__(288, 1)
         const int v = tid % NV, rest = tid / NV;
         const int seg = rest % p.nseg, r = rest / p.nseg;
         const int wo_a = seg * p.seg_len, wo_b = min(p.Wo, wo_a + p.seg_len);
-        int tap_off[MAXT];
-#pragma unroll
-        for (int t = 0; t < MAXT; ++t) {
-            const int tt = t < p.T ? t : 0;
-            const int ty = tt / p.X, tx = tt - (tt / p.X) * p.X;
-            tap_off[t] = (ty * p.dh * p.xw + tx * p.dw) * p.CB;
-        }
         for (int i = 0; i < ntl; ++i) {
             const int st = i % p.stages;
             const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
@@ -154,38 +177,43 @@ __global__ void __launch_bounds__(288, 1)
                 const uint16_t* ys = reinterpret_cast<const uint16_t*>(smem + st * p.stage_bytes + p.x_bytes_al);
                 const int cv = v * GM;
                 if constexpr (SLIDE3) {
-                    // 3x3 filter, stride 1 and dilation 1 along W: keep a 3x3
-                    // window of X vectors in registers, one new column per pixel.
-                    const uint16_t* xr[3];
-#pragma unroll
-                    for (int y = 0; y < 3; ++y) xr[y] = xs + (r * p.sh + y * p.dh) * p.xw * p.CB + cv;
-                    float w[3][3][GM];
-#pragma unroll
-                    for (int y = 0; y < 3; ++y) {
-                        load_vec<BF16, GM>(xr[y] + (wo_a + 0) * p.CB, w[y][0]);
-                        load_vec<BF16, GM>(xr[y] + (wo_a + 1) * p.CB, w[y][1]);
+                    // 3x3 filter, stride 1 and dilation 1 along W: a 3x3 window of
+                    // X vectors slides along the row, one new column per pixel.
+                    // Unrolled by 3 so the three window columns change roles
+                    // instead of being copied.
+                    const int CBv = CB;
+                    const uint16_t* xr0 = xs + (r * sh) * xw * CBv + cv;
+                    const uint16_t* xr1 = xr0 + dh * xw * CBv;
+                    const uint16_t* xr2 = xr1 + dh * xw * CBv;
+                    const uint16_t* yr = ys + (r * Wo) * CBv + cv;
+                    float wa[3][GM], wb[3][GM], wc[3][GM];
+                    load_col3<BF16, GM>(xr0, xr1, xr2, wo_a * CBv, wa);
+                    load_col3<BF16, GM>(xr0, xr1, xr2, (wo_a + 1) * CBv, wb);
+                    int wo = wo_a;
+                    for (; wo + 3 <= wo_b; wo += 3) {
+                        load_col3<BF16, GM>(xr0, xr1, xr2, (wo + 2) * CBv, wc);
+                        fma_col3<BF16, GM>(yr + wo * CBv, wa, wb, wc, acc);
+                        load_col3<BF16, GM>(xr0, xr1, xr2, (wo + 3) * CBv, wa);
+                        fma_col3<BF16, GM>(yr + (wo + 1) * CBv, wb, wc, wa, acc);
+                        load_col3<BF16, GM>(xr0, xr1, xr2, (wo + 4) * CBv, wb);
+                        fma_col3<BF16, GM>(yr + (wo + 2) * CBv, wc, wa, wb, acc);
                     }
-                    const uint16_t* yr = ys + (r * p.Wo) * p.CB + cv;
-                    for (int wo = wo_a; wo < wo_b; ++wo) {
-#pragma unroll
-                        for (int y = 0; y < 3; ++y) load_vec<BF16, GM>(xr[y] + (wo + 2) * p.CB, w[y][2]);
-                        float dy[GM];
-                        load_vec<BF16, GM>(yr + wo * p.CB, dy);
-#pragma unroll
-                        for (int y = 0; y < 3; ++y)
-#pragma unroll
-                            for (int x = 0; x < 3; ++x)
-#pragma unroll
-                                for (int j = 0; j < GM; ++j) acc[y * 3 + x][j] = fmaf(dy[j], w[y][x][j], acc[y * 3 + x][j]);
-#pragma unroll
-                        for (int y = 0; y < 3; ++y)
-#pragma unroll
-                            for (int j = 0; j < GM; ++j) {
-                                w[y][0][j] = w[y][1][j];
-                                w[y][1][j] = w[y][2][j];
-                            }
+                    if (wo < wo_b) {
+                        load_col3<BF16, GM>(xr0, xr1, xr2, (wo + 2) * CBv, wc);
+                        fma_col3<BF16, GM>(yr + wo * CBv, wa, wb, wc, acc);
+                        if (wo + 1 < wo_b) {
+                            load_col3<BF16, GM>(xr0, xr1, xr2, (wo + 3) * CBv, wa);
+                            fma_col3<BF16, GM>(yr + (wo + 1) * CBv, wb, wc, wa, acc);
+                        }
                     }
                 } else {
+                    int tap_off[MAXT];
+#pragma unroll
+                    for (int t = 0; t < MAXT; ++t) {
+                        const int tt = t < p.T ? t : 0;
+                        const int ty = tt / p.X, tx = tt - (tt / p.X) * p.X;
+                        tap_off[t] = (ty * p.dh * p.xw + tx * p.dw) * p.CB;
+                    }
                     for (int wo = wo_a; wo < wo_b; ++wo) {
                         float dy[GM];
                         load_vec<BF16, GM>(ys + (r * p.Wo + wo) * p.CB + cv, dy);

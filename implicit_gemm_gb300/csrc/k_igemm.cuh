@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(192, 1)
     } else {
         // ------------------------------------------------ epilogue (warps 2..5)
         if (nk > 0) {
-            mbar_wait(accb, 0);
+            mbar_wait_sleep(accb, 0);
             tc_fence_after();
         }
         const int q = warp & 3;

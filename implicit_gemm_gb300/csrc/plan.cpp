@@ -294,7 +294,10 @@ int plan_depthwise(Plan* pl, const wg_options& o, int num_sms, std::string* err)
     const int NV = dw.CB / dw.Gm;
     const int Wo = pb.out[2], Ho = pb.out[1];
     dw.xw = (Wo - 1) * pb.stride[2] + (pb.filt[2] - 1) * pb.dil[2] + 1;
-    const int avail = kMaxSmemPerCta - 1024 - 512;
+    // Two CTAs per SM when the channel vector is at most 4 wide (register use
+    // allows it): half the shared memory each.
+    const int ctas_per_sm = dw.Gm <= 4 ? 2 : 1;
+    const int avail = (ctas_per_sm == 2 ? kMaxSmemPerCta / 2 - 2048 : kMaxSmemPerCta) - 1024 - 512;
     // Rows per tile: little padding in Ho, at least 3 stages, at most 256 compute threads.
     int bestR = 0;
     long long best = -1;
@@ -318,7 +321,7 @@ int plan_depthwise(Plan* pl, const wg_options& o, int num_sms, std::string* err)
     dw.x_bytes = dw.CB * 2 * dw.xw * dw.xh;
     dw.dy_bytes = dw.CB * 2 * Wo * dw.R;
     dw.stage_bytes = round_up(dw.x_bytes, 128) + round_up(dw.dy_bytes, 128);
-    dw.stages = std::min(6, avail / dw.stage_bytes);
+    dw.stages = std::min(ctas_per_sm == 2 ? 4 : 6, avail / dw.stage_bytes);
     const int red_bytes = dw.threads * (int)pb.T * dw.Gm * 4;
     dw.smem_bytes = std::max(dw.stages * dw.stage_bytes, red_bytes) + 1024 + 512;
     if (dw.smem_bytes > kMaxSmemPerCta) return fail(err, WG_ERR_NOT_SUPPORTED, "depthwise reduction too large");
@@ -330,7 +333,7 @@ int plan_depthwise(Plan* pl, const wg_options& o, int num_sms, std::string* err)
     } else if (o.mode == WG_MODE_DIRECT) {
         S = 1;
     } else {
-        S = (int)std::max(1LL, (long long)std::llround((double)num_sms / (double)dw.n_cblocks));
+        S = (int)std::max(1LL, (long long)std::llround((double)num_sms * ctas_per_sm / (double)dw.n_cblocks));
         S = (int)std::min<long long>(S, dw.total_tiles);
         S = std::min(S, 65535);
         const long long per = cdiv(dw.total_tiles, S);

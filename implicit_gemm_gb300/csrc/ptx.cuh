@@ -65,17 +65,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 
 // Wait for the phase with the given parity to complete.  Returns false (and
 // sets the device status word) if it has not completed within kWaitLimitNs.
+// The timer is read once per 64 polls: each try_wait may itself suspend the
+// thread for a while, and timer reads between polls would steal issue slots
+// from the warps doing the work.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             atomicOr(&g_status, kStatusTimeout);
             return false;
         }
     }
-    return true;
+}
+
+// For long waits off the critical path (e.g. an epilogue waiting for the whole
+// mainloop): sleep between polls so the waiting warps leave the issue slots to
+// the producer and MMA warps.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        __nanosleep(200);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_status, kStatusTimeout);
+            return false;
+        }
+    }
 }
 
 // ---------------------------------------------------------------- TMA

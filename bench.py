@@ -11,9 +11,12 @@ every step keeps the GPU busy long enough for the host to enqueue the call, so
 host-side time is not inside the events (--graph replays a captured CUDA graph
 of the call instead).  The e2e value times the same call with host buffers.  The headline workload is
 the 2-D dense 56x56, C = K = 64, N = 32, 3x3 problem with bf16 inputs and bf16
-dW; the other workloads are reported under "workloads".  L2 is flushed (a 256 MiB
-write, then a 256 MiB read of another buffer so the write's dirty lines are
-written back before the timed events) before every timed step.
+dW; the other workloads are reported under "workloads".  No step finds its
+inputs in L2: each step reads the next of several copies of X and dY whose
+total exceeds twice the L2; inputs too small for that (the 8x8 problem) are
+evicted instead by an L2 flush before every step (a 256 MiB write, then a
+256 MiB read of another buffer so the write's dirty lines are written back
+before the timed events).
 
 Prints one JSON line on rank 0.  Multi-GPU runs (torchrun) are independent
 replicas (weak scaling): the path has no exchange step on one node.
@@ -193,8 +196,23 @@ def cpu_baseline(name):
             "sample": f"full {name} workload, {runs} run(s), fp64 direct loop with |dY*X| sums"}
 
 
+L2_BYTES = 129 * 1000 * 1000
+# DRAM bytes (read + write) of one launch of the workload's main kernel from an
+# ncu capture of the kernel as it now stands (summaries under profiles/); a
+# workload without such a capture reports null.
+TRAFFIC = {}
+MAX_COPIES = 512
+
+
 class Workload:
-    def __init__(self, torch, name):
+    """One workload's inputs, outputs and prepared calls.
+
+    So that no step finds its inputs in L2, each step reads the next of `copies`
+    identical copies of X and dY whose total size exceeds twice the L2 (a copy
+    was last read more than 129 MB of other input ago).  Inputs too small for
+    that within MAX_COPIES fall back to flushing L2 before every step."""
+
+    def __init__(self, torch, name, rotate=True):
         self.torch = torch
         self.name = name
         sp, dist, seed, self.split_k, self.mode, self.gm = WORKLOADS[name]
@@ -217,6 +235,24 @@ class Workload:
         self.call = binding.PreparedCall(sp, self.x, self.dy, self.dw, self.split_k, self.mode, self.gm, self.ws,
                                          self.ws_bytes)
         self.graph = None
+        in_bytes = 2 * (self.s["nx"] + self.s["ndy"])
+        need = -(-2 * L2_BYTES // in_bytes)
+        self.copies = max(2, need) if rotate and need <= MAX_COPIES else 1
+        self.calls = [self.call]
+        self.inputs = [(self.x, self.dy)]
+        for _ in range(self.copies - 1):
+            xc, dyc = self.x.clone(), self.dy.clone()
+            self.inputs.append((xc, dyc))
+            self.calls.append(binding.PreparedCall(sp, xc, dyc, self.dw, self.split_k, self.mode, self.gm, self.ws,
+                                                   self.ws_bytes))
+        self.next = 0
+        self.rotating = self.copies > 1
+
+    def l2_note(self):
+        if self.rotating:
+            mb = self.copies * 2 * (self.s["nx"] + self.s["ndy"]) / 1e6
+            return f"inputs rotate through {self.copies} copies ({mb:.0f} MB > 2x L2); no flush"
+        return "flushed before every timed step (outside the events): write 256 MiB, then read another 256 MiB"
 
     def capture(self, stream):
         """Capture one step (every launch of the call) into a CUDA graph."""
@@ -233,7 +269,8 @@ class Workload:
         if self.graph is not None:
             self.graph.replay()
         else:
-            self.call(stream.cuda_stream)
+            self.calls[self.next](stream.cuda_stream)
+            self.next = (self.next + 1) % self.copies
 
     def e2e_step(self, stream):
         # The public call itself (no graph), with host<->device copies.
@@ -259,20 +296,35 @@ class L2Flush:
         self.torch.sum(self.r, dim=0, out=self.sink)
 
 
-def time_steps(torch, wl, steps, warmup, flush, stream, e2e=False):
-    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each step."""
+def time_steps(torch, wl, steps, warmup, flush, stream, e2e=False, mark=False):
+    """Per-step CUDA-event times (ms) on `stream`; inputs not in L2 at each step
+    (rotating copies, else an L2 flush before the step).  With `mark`, the times
+    run from the step's start to the end of the call's main kernel (an event the
+    library records between its main and its reduction kernel)."""
     fn = wl.e2e_step if e2e else wl.step
+    do_flush = not e2e and (not wl.rotating or wl.graph is not None)
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            flush()
+            if do_flush:
+                flush()
             fn(stream)
         stream.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        if mark:
+            for _, b in evs:
+                b.record(stream)  # creates the event before the library records it
+            stream.synchronize()
         for a, b in evs:
-            flush()
+            if do_flush:
+                flush()
             a.record(stream)
-            fn(stream)
-            b.record(stream)
+            if mark:
+                binding.wg_set_mark_event(b)
+                fn(stream)
+            else:
+                fn(stream)
+                b.record(stream)
+        binding.wg_set_mark_event(None)
         stream.synchronize()
     binding.wg_check_status(stream)
     return [a.elapsed_time(b) for a, b in evs]
@@ -342,21 +394,30 @@ def main():
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         e2e_ms = float(t.item())
 
-    # Roofline of the step on its dominant kernel: algorithmic FLOPs and bytes of
-    # one launch over the measured step time; the bound is the slower of the two.
+    # Roofline of the dominant kernel (the call's main kernel: every FLOP of the
+    # step and every algorithmic byte read or written goes through it): its
+    # algorithmic FLOPs or bytes per launch over its average duration, measured
+    # in a second pass over the same steps with an event the library records
+    # right after it.  The bound is the slower of the two at the measured peaks.
+    kern_ms = step_ms
+    if not args.graph:
+        kern_ms = float(np.mean(time_steps(torch, wl, args.steps, args.warmup, flush, stream, mark=True)))
     t_flop = s["flops"] / (pk["bf16"] * 1e12)
     t_byte = s["bytes"] / (pk["hbm"] * 1e9)
     if t_byte >= t_flop:
-        roof = {"bound": "hbm", "achieved": s["bytes"] / (step_ms * 1e-3) / 1e9, "peak": pk["hbm"], "unit": "GB/s"}
+        roof = {"bound": "hbm", "achieved": s["bytes"] / (kern_ms * 1e-3) / 1e9, "peak": pk["hbm"], "unit": "GB/s"}
+        roof["step_frac"] = s["bytes"] / (step_ms * 1e-3) / 1e9 / pk["hbm"]
     else:
-        roof = {"bound": "tensor", "achieved": s["flops"] / (step_ms * 1e-3) / 1e12, "peak": pk["bf16"],
+        roof = {"bound": "tensor", "achieved": s["flops"] / (kern_ms * 1e-3) / 1e12, "peak": pk["bf16"],
                 "unit": "TFLOP/s"}
+        roof["step_frac"] = s["flops"] / (step_ms * 1e-3) / 1e12 / pk["bf16"]
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = TRAFFIC.get(args.workload)
     roof["peak_source"] = pk["src"]
     roof["kernel"] = "igemm_wgrad_kernel" if "igemm" in wl.plan else "depthwise_wgrad_kernel"
-    roof["timed"] = ("whole step (every launch of the call, " + ("graph replay" if args.graph else "direct call") +
-                     ") with CUDA events")
+    roof["kernel_ms"] = kern_ms
+    roof["timed"] = ("main kernel: CUDA events from the step start to a mark the library records after the kernel"
+                     if not args.graph else "whole step (graph replay) with CUDA events")
 
     extra = {}
     if rank == 0 and not args.no_extra:
@@ -368,12 +429,15 @@ def main():
                 w2.capture(stream)
             tt = time_steps(torch, w2, 300, 10, flush, stream)
             ms = float(np.mean(tt))
+            kms = ms if args.graph else float(np.mean(time_steps(torch, w2, 300, 10, flush, stream, mark=True)))
             s2 = w2.s
             tf, tb = s2["flops"] / (pk["bf16"] * 1e12), s2["bytes"] / (pk["hbm"] * 1e9)
             extra[name] = {"ms_per_step": ms, "tflops": s2["flops"] / (ms * 1e-3) / 1e12,
                            "gbs": s2["bytes"] / (ms * 1e-3) / 1e9, "roofline_us": max(tf, tb) * 1e6,
                            "bound": "hbm" if tb >= tf else "tensor",
-                           "roofline_frac": max(tf, tb) / (ms * 1e-3), "plan": w2.plan}
+                           "roofline_frac": max(tf, tb) / (ms * 1e-3), "kernel_ms": kms,
+                           "kernel_roofline_frac": max(tf, tb) / (kms * 1e-3), "traffic": TRAFFIC.get(name),
+                           "l2": w2.l2_note(), "plan": w2.plan}
             del w2
 
     if rank == 0:
@@ -385,7 +449,7 @@ def main():
                            "C": wl.sp["C"], "K": wl.sp["K"], "filt": wl.sp["filt"], "stride": wl.sp["stride"],
                            "pad": wl.sp["pad_l"], "in_dtype": wl.sp["in_dtype"], "out_dtype": wl.sp["out_dtype"],
                            "split_k": wl.split_k, "mode": wl.mode, "plan": wl.plan,
-                           "l2": "flushed before every timed step (outside the events): write 256 MiB, then read another 256 MiB",
+                           "l2": wl.l2_note() if not args.graph else "flushed before every timed step (graph mode)",
                            "parallelism": f"replicas x{ws}"},
                 "roofline": roof, "clocks": clocks, "gpu_launches": wl.launches_per_step * args.steps,
                 "e2e": {"value": ws * s["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",

@@ -32,7 +32,8 @@ class WgProblem(ctypes.Structure):
 
 
 class WgOptions(ctypes.Structure):
-    _fields_ = [("split_k", ctypes.c_int), ("mode", ctypes.c_int), ("group_merge", ctypes.c_int)]
+    _fields_ = [("split_k", ctypes.c_int), ("mode", ctypes.c_int), ("group_merge", ctypes.c_int),
+                ("cluster", ctypes.c_int)]
 
 
 class WgradError(RuntimeError):
@@ -42,7 +43,8 @@ class WgradError(RuntimeError):
 
 
 EXPORTS = ("wg_problem_normalize", "wg_workspace_size", "wg_conv_bwd_weight", "wg_check_status",
-           "wg_plan_string", "wg_status_string", "wg_last_error", "wg_conv_bwd_weight_noalloc")
+           "wg_plan_string", "wg_status_string", "wg_last_error", "wg_conv_bwd_weight_noalloc",
+           "wg_set_mark_event")
 
 _lib = None
 _lock = threading.Lock()
@@ -69,6 +71,7 @@ def load():
             lib.wg_conv_bwd_weight_noalloc.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, O,
                                                        ctypes.c_void_p]
             lib.wg_check_status.argtypes = [ctypes.c_void_p]
+            lib.wg_set_mark_event.argtypes = [ctypes.c_void_p]
             lib.wg_plan_string.argtypes = [P, O, ctypes.c_char_p, ctypes.c_size_t]
             lib.wg_status_string.argtypes = [ctypes.c_int]
             lib.wg_status_string.restype = ctypes.c_char_p
@@ -101,8 +104,8 @@ def make_problem(spec: dict) -> WgProblem:
     return p
 
 
-def make_options(split_k: int = 0, mode: str = "auto", group_merge: int = 0) -> WgOptions:
-    return WgOptions(int(split_k), MODES[mode], int(group_merge))
+def make_options(split_k: int = 0, mode: str = "auto", group_merge: int = 0, cluster: int = 0) -> WgOptions:
+    return WgOptions(int(split_k), MODES[mode], int(group_merge), int(cluster))
 
 
 def _addr(t) -> int:
@@ -120,24 +123,26 @@ def wg_problem_normalize(spec: dict) -> list:
     return [p.out[i] for i in range(spec["ndim"])]
 
 
-def wg_workspace_size(spec: dict, split_k: int = 0, mode: str = "auto", group_merge: int = 0) -> int:
-    p, o, n = make_problem(spec), make_options(split_k, mode, group_merge), ctypes.c_size_t(0)
+def wg_workspace_size(spec: dict, split_k: int = 0, mode: str = "auto", group_merge: int = 0, *,
+                      cluster: int = 0) -> int:
+    p, o, n = make_problem(spec), make_options(split_k, mode, group_merge, cluster), ctypes.c_size_t(0)
     _check(load().wg_workspace_size(ctypes.byref(p), ctypes.byref(o), ctypes.byref(n)))
     return int(n.value)
 
 
-def wg_plan_string(spec: dict, split_k: int = 0, mode: str = "auto", group_merge: int = 0) -> str:
-    p, o = make_problem(spec), make_options(split_k, mode, group_merge)
+def wg_plan_string(spec: dict, split_k: int = 0, mode: str = "auto", group_merge: int = 0, *,
+                   cluster: int = 0) -> str:
+    p, o = make_problem(spec), make_options(split_k, mode, group_merge, cluster)
     buf = ctypes.create_string_buffer(2048)
     _check(load().wg_plan_string(ctypes.byref(p), ctypes.byref(o), buf, len(buf)))
     return buf.value.decode()
 
 
 def wg_conv_bwd_weight(spec: dict, x, dy, dw, split_k: int = 0, mode: str = "auto", group_merge: int = 0,
-                       workspace=None, ws_bytes: int | None = None, stream=None) -> None:
+                       workspace=None, ws_bytes: int | None = None, stream=None, *, cluster: int = 0) -> None:
     """Launch the weight gradient on `stream` (torch stream, raw handle int, or None for
     torch's current stream when torch is loaded, else the legacy default stream)."""
-    p, o = make_problem(spec), make_options(split_k, mode, group_merge)
+    p, o = make_problem(spec), make_options(split_k, mode, group_merge, cluster)
     if ws_bytes is None:
         ws_bytes = 0 if workspace is None else (workspace.numel() * workspace.element_size()
                                                 if hasattr(workspace, "numel") else 0)
@@ -150,9 +155,9 @@ class PreparedCall:
     ctypes call.  Keeps references to the tensors it was built from."""
 
     def __init__(self, spec: dict, x, dy, dw, split_k: int = 0, mode: str = "auto", group_merge: int = 0,
-                 workspace=None, ws_bytes: int | None = None):
+                 workspace=None, ws_bytes: int | None = None, *, cluster: int = 0):
         self._keep = (x, dy, dw, workspace)
-        self.p, self.o = make_problem(spec), make_options(split_k, mode, group_merge)
+        self.p, self.o = make_problem(spec), make_options(split_k, mode, group_merge, cluster)
         if ws_bytes is None:
             ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
         self.fn = load().wg_conv_bwd_weight
@@ -167,12 +172,20 @@ class PreparedCall:
 
 
 def wg_conv_bwd_weight_noalloc(spec: dict, x, dy, dw, split_k: int = 0, mode: str = "auto", group_merge: int = 0,
-                               stream=None) -> None:
+                               stream=None, *, cluster: int = 0) -> None:
     """wg_conv_bwd_weight for callers that cannot allocate: the split-K workspace comes
     from the library's own 16 MiB device array (see include/wgrad.h)."""
-    p, o = make_problem(spec), make_options(split_k, mode, group_merge)
+    p, o = make_problem(spec), make_options(split_k, mode, group_merge, cluster)
     _check(load().wg_conv_bwd_weight_noalloc(ctypes.byref(p), _addr(x), _addr(dy), _addr(dw), ctypes.byref(o),
                                              _stream_handle(stream)))
+
+
+def wg_set_mark_event(event) -> None:
+    """Record `event` (a torch.cuda.Event, a raw cudaEvent_t, or None to stop) after
+    the main kernel of every following call from this thread (see include/wgrad.h).
+    A torch event must have been recorded once, so that it exists."""
+    h = None if event is None else (event if isinstance(event, int) else int(event.cuda_event))
+    _check(load().wg_set_mark_event(h))
 
 
 def wg_check_status(stream=None) -> None:
@@ -202,7 +215,7 @@ def _stream_handle(stream):
 
 
 def conv_bwd_weight(spec: dict, x, dy, split_k: int = 0, mode: str = "auto", group_merge: int = 0, out=None,
-                    stream=None):
+                    stream=None, *, cluster: int = 0):
     """Convenience wrapper over wg_conv_bwd_weight for torch CUDA tensors: allocates dW
     (G, K, *filt, C) in spec['out_dtype'] and the workspace it needs with torch, then calls
     the library."""
@@ -210,7 +223,7 @@ def conv_bwd_weight(spec: dict, x, dy, split_k: int = 0, mode: str = "auto", gro
     tdt = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}[spec.get("out_dtype", "fp32")]
     if out is None:
         out = torch.empty((spec["G"], spec["K"], *spec["filt"], spec["C"]), dtype=tdt, device=x.device)
-    nbytes = wg_workspace_size(spec, split_k, mode, group_merge)
+    nbytes = wg_workspace_size(spec, split_k, mode, group_merge, cluster=cluster)
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=x.device) if nbytes else None
-    wg_conv_bwd_weight(spec, x, dy, out, split_k, mode, group_merge, ws, nbytes, stream)
+    wg_conv_bwd_weight(spec, x, dy, out, split_k, mode, group_merge, ws, nbytes, stream, cluster=cluster)
     return out

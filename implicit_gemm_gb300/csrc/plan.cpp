@@ -95,11 +95,34 @@ bool dim_phases(int F, int s, int d, DimPhases* o)
 
 struct IgCand {
     int halo, box[4], nt[4], KT, mt, stages, stage_bytes, patch[3], patch_bytes, n_patches, dy_off;
-    long long cost;
+    long long cost, tile_clk;
 };
 
-int plan_igemm(Plan* pl, const wg_options& o, int num_sms, std::string* err)
+// Cost terms of the split-K epilogue, in SM cycles (GB300 at ~2 GHz): L2
+// takes ~2900 bytes per cycle device-wide; a second (reduction) kernel adds a
+// few microseconds of launch and ramp; the cluster reduction writes the CTA's
+// partial sums to shared memory and reads them back through distributed
+// shared memory at ~12 B/cycle (measured), plus two cluster barriers.
+constexpr long long kL2BytesPerClk = 2900;
+constexpr long long kReduceLaunchClk = 3000;
+
+long long epilogue_clk(long long dw_bytes, int n_out, int Q, long long red_bytes, bool atomic)
 {
+    long long c = 0;
+    if (Q > 1) c += red_bytes / 128 + red_bytes / 12 + 1500;
+    if (atomic) {
+        c += (long long)n_out * dw_bytes / (kL2BytesPerClk / 3);
+    } else if (n_out > 1) {
+        c += 2 * (long long)n_out * dw_bytes / kL2BytesPerClk + kReduceLaunchClk;
+    }
+    return c;
+}
+
+int cap_index(int q) { return q == 1 ? 0 : q == 2 ? 1 : q == 4 ? 2 : 3; }
+
+int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::string* err)
+{
+    const int num_sms = caps.num_sms;
     const Problem& pb = pl->pb;
     IgemmPlan& ig = pl->ig;
     std::memset(&ig, 0, sizeof ig);
@@ -185,6 +208,7 @@ int plan_igemm(Plan* pl, const wg_options& o, int num_sms, std::string* err)
                     c.stage_bytes = (int)stage;
                     c.dy_off = n_x * c.patch_bytes;
                     c.cost = cost;
+                    c.tile_clk = tile_clk;
                     best = c;
                 }
                 if (stages >= 3) break;  // smaller mt only re-reads more
@@ -211,6 +235,7 @@ int plan_igemm(Plan* pl, const wg_options& o, int num_sms, std::string* err)
     ig.tmem_cols = std::max(32, pow2_at_least(ig.mt_per_cta * ig.Nt));
     ig.total_kt = (long long)ig.ntile[0] * ig.ntile[1] * ig.ntile[2] * ig.ntile[3];
     ig.est_cycles = best.cost / std::max(1, num_sms);
+    ig.tile_clk = best.tile_clk;
     if (ig.total_kt > (1ll << 31) - 1) return fail(err, WG_ERR_NOT_SUPPORTED, "GemmK too large");
     if (ig.halo) {
         for (int i = 0; i < 3; ++i) ig.n_phase[i] = ph[i].nph;
@@ -254,19 +279,45 @@ int plan_igemm(Plan* pl, const wg_options& o, int num_sms, std::string* err)
 
     const long long base = (long long)ig.n_mranges * ig.n_ntiles * ig.n_gblocks;
     if (base > 65535LL * 65535LL) return fail(err, WG_ERR_NOT_SUPPORTED, "grid too large");
-    int S;
+    // Cluster reduction: the CTA's partial sums (mt_per_cta * Nt columns of 128
+    // fp32 rows) are staged in its pipeline buffers.
+    const long long red_bytes = (long long)ig.mt_per_cta * ig.Nt * 128 * 4;
+    const bool cl_ok = red_bytes <= (long long)ig.stages * ig.stage_bytes;
+    if (o.cluster > 1 && !cl_ok)
+        return fail(err, WG_ERR_NOT_SUPPORTED,
+                    "cluster reduction: the CTA's partial sums (%lld bytes) do not fit its shared memory", red_bytes);
+    const long long dw_bytes = pb.dw_elems * 4;
+    const bool atomic = o.mode == WG_MODE_ATOMIC;
+    int S, Q;
     if (o.split_k > 0) {
         S = o.split_k;
+        Q = o.cluster > 0 ? o.cluster : 1;
+        if (S % Q) return fail(err, WG_ERR_INVALID_ARGUMENT, "cluster %d does not divide split_k %d", Q, S);
     } else if (o.mode == WG_MODE_DIRECT) {
-        S = 1;
+        S = Q = o.cluster > 1 ? o.cluster : 1;
     } else {
-        S = (int)std::max(1LL, (long long)std::llround((double)num_sms / (double)base));
-        S = (int)std::min<long long>(S, ig.total_kt);
-        S = std::min(S, 65535);
-        const long long per = cdiv(ig.total_kt, S);
-        S = (int)cdiv(ig.total_kt, per);
+        // Fill the device in one wave for each cluster size, then keep the
+        // cheapest by the planner's cycle estimate.  Automatic plans use no
+        // clusters: distributed shared memory moves ~10-14 bytes per cycle per
+        // SM on GB300 (measured), so the cluster reduction was slower than
+        // writing the partial sums to L2 on every workload measured.
+        S = Q = 0;
+        long long best_clk = -1;
+        for (int q = 1; q <= 8; q *= 2) {
+            if (o.cluster > 0 ? q != o.cluster : q != 1) continue;
+            if (q > 1 && !cl_ok) continue;
+            const long long fit = caps.cluster_ctas[cap_index(q)] / (base * q);
+            long long s = q * std::max(1LL, fit);
+            s = std::min<long long>(s, round_up((int)std::min<long long>(ig.total_kt, 1 << 20), q));
+            const long long per = cdiv(ig.total_kt, s);
+            s = std::min<long long>(65535 / q * q, round_up((int)cdiv(ig.total_kt, per), q));
+            const long long clk = cdiv(ig.total_kt, s) * ig.tile_clk +
+                                  epilogue_clk(dw_bytes, (int)(s / q), q, red_bytes, atomic);
+            if (best_clk < 0 || clk < best_clk) best_clk = clk, S = (int)s, Q = q;
+        }
     }
     if (S > 65535) return fail(err, WG_ERR_NOT_SUPPORTED, "split_k %d above 65535", S);
+    ig.cluster = Q;
     pl->S = S;
     pl->per_split = cdiv(ig.total_kt, S);
     pl->grid[0] = (unsigned)(ig.n_mranges * ig.n_ntiles);
@@ -285,6 +336,8 @@ bool dw_eligible(const Problem& pb)
 
 int plan_depthwise(Plan* pl, const wg_options& o, int num_sms, std::string* err)
 {
+    if (o.cluster > 1)
+        return fail(err, WG_ERR_NOT_SUPPORTED, "cluster > 1 is for the tensor-core kernel (the depthwise kernel has none)");
     const Problem& pb = pl->pb;
     DwPlan& dw = pl->dw;
     std::memset(&dw, 0, sizeof dw);
@@ -397,21 +450,41 @@ int normalize(const wg_problem* p, Problem* o, std::string* err)
     return WG_OK;
 }
 
-int make_plan(const wg_problem* p, const wg_options* opt, int num_sms, Plan* pl, std::string* err)
+DeviceCaps default_caps(int num_sms)
+{
+    if (num_sms <= 0) num_sms = kDefaultSMs;
+    DeviceCaps c;
+    c.num_sms = num_sms;
+    c.cluster_ctas[0] = num_sms;
+    c.cluster_ctas[1] = num_sms;
+    c.cluster_ctas[2] = num_sms * 144 / 152;
+    c.cluster_ctas[3] = num_sms * 120 / 152;
+    return c;
+}
+
+int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps_in, Plan* pl, std::string* err)
 {
     std::memset(pl, 0, sizeof *pl);
     int st = normalize(p, &pl->pb, err);
     if (st) return st;
     const Problem& pb = pl->pb;
-    wg_options o{0, WG_MODE_AUTO, 0};
+    wg_options o{0, WG_MODE_AUTO, 0, 0};
     if (opt) o = *opt;
-    if (num_sms <= 0) num_sms = kDefaultSMs;
+    DeviceCaps caps = caps_in;
+    if (caps.num_sms <= 0) caps = default_caps(0);
+    for (int i = 0; i < 4; ++i)
+        if (caps.cluster_ctas[i] <= 0) caps.cluster_ctas[i] = default_caps(caps.num_sms).cluster_ctas[i];
+    const int num_sms = caps.num_sms;
     if (o.split_k < 0) return fail(err, WG_ERR_INVALID_ARGUMENT, "split_k must be >= 0");
     if (o.mode < WG_MODE_AUTO || o.mode > WG_MODE_DETERMINISTIC) return fail(err, WG_ERR_INVALID_ARGUMENT, "bad mode");
     if (o.group_merge != 0 && o.group_merge != 1 && o.group_merge != 2 && o.group_merge != 4 && o.group_merge != 8)
         return fail(err, WG_ERR_INVALID_ARGUMENT, "group_merge must be 0, 1, 2, 4 or 8");
-    if (o.mode == WG_MODE_DIRECT && o.split_k > 1)
-        return fail(err, WG_ERR_INVALID_ARGUMENT, "mode DIRECT takes no split (split_k %d)", o.split_k);
+    if (o.cluster != 0 && o.cluster != 1 && o.cluster != 2 && o.cluster != 4 && o.cluster != 8)
+        return fail(err, WG_ERR_INVALID_ARGUMENT, "cluster must be 0, 1, 2, 4 or 8");
+    if (o.mode == WG_MODE_DIRECT && o.split_k > 1 && o.split_k != o.cluster)
+        return fail(err, WG_ERR_INVALID_ARGUMENT,
+                    "mode DIRECT takes no split, or exactly one cluster of splits (split_k %d, cluster %d)", o.split_k,
+                    o.cluster);
     if (o.mode == WG_MODE_ATOMIC && pb.out_dtype != WG_FP32)
         return fail(err, WG_ERR_NOT_SUPPORTED, "atomic split-K accumulates in fp32: dW must be WG_FP32");
     if (((long long)pb.G * pb.C * 2) % 16 || ((long long)pb.G * pb.K * 2) % 16)
@@ -427,16 +500,18 @@ int make_plan(const wg_problem* p, const wg_options* opt, int num_sms, Plan* pl,
             return fail(err, WG_ERR_NOT_SUPPORTED,
                         "group_merge > 1 needs the depthwise kernel (1-D/2-D, <= 9 taps, G %% 8 == 0)");
         pl->kind = KIND_IGEMM;
-        st = plan_igemm(pl, o, num_sms, err);
+        st = plan_igemm(pl, o, caps, err);
     }
     if (st) return st;
+    // Partial sums that reach memory per dW element: one per cluster of splits.
+    const int n_out = pl->kind == KIND_IGEMM ? pl->S / pl->ig.cluster : pl->S;
     if (o.mode == WG_MODE_ATOMIC)
         pl->mode = MODE_ATOMIC;
-    else if (pl->S == 1)
+    else if (n_out == 1)
         pl->mode = MODE_DIRECT;
     else
         pl->mode = MODE_DETERMINISTIC;
-    pl->ws_bytes = pl->mode == MODE_DETERMINISTIC ? (size_t)pl->S * (size_t)pb.dw_elems * 4 : 0;
+    pl->ws_bytes = pl->mode == MODE_DETERMINISTIC ? (size_t)n_out * (size_t)pb.dw_elems * 4 : 0;
     return WG_OK;
 }
 
@@ -448,10 +523,11 @@ std::string plan_string(const Plan& pl)
     if (pl.kind == KIND_IGEMM) {
         const IgemmPlan& ig = pl.ig;
         snprintf(buf, sizeof buf,
-                 "kernel=igemm_tcgen05 %s mode=%s S=%d Gm=%d gblocks=%d cchunks=%d Nt=%d ntiles=%d katoms=%d "
+                 "kernel=igemm_tcgen05 %s mode=%s S=%d cluster=%d Gm=%d gblocks=%d cchunks=%d Nt=%d ntiles=%d "
+                 "katoms=%d "
                  "box=(w%d,h%d,d%d,n%d) KT=%d ktiles=%lld per_split=%lld atoms=%d mtiles=%d mt_per_cta=%d "
                  "mranges=%d tmem_cols=%d stages=%d stage_bytes=%d smem=%d grid=(%u,%u,%u) block=%u ws=%zu",
-                 ig.halo ? "halo" : "pertap", mode, pl.S, ig.Gm, ig.n_gblocks, ig.n_cchunks, ig.Nt, ig.n_ntiles, ig.n_katoms, ig.box[0], ig.box[1],
+                 ig.halo ? "halo" : "pertap", mode, pl.S, ig.cluster, ig.Gm, ig.n_gblocks, ig.n_cchunks, ig.Nt, ig.n_ntiles, ig.n_katoms, ig.box[0], ig.box[1],
                  ig.box[2], ig.box[3], ig.KT, ig.total_kt, pl.per_split, ig.n_atoms, ig.n_mtiles, ig.mt_per_cta,
                  ig.n_mranges, ig.tmem_cols, ig.stages, ig.stage_bytes, ig.smem_bytes, pl.grid[0], pl.grid[1],
                  pl.grid[2], pl.block, pl.ws_bytes);

@@ -1,6 +1,6 @@
 // Host-side problem normalisation and launch planning for the wgrad kernels.
 // Pure C++ (no CUDA calls): the plan is a function of the problem, the options
-// and the SM count.
+// and the device facts in DeviceCaps.
 #pragma once
 
 #include <stddef.h>
@@ -70,6 +70,8 @@ struct IgemmPlan {
     unsigned short atom_tap[kMaxHaloAtoms];
     unsigned char atom_cc[kMaxHaloAtoms];
     long long est_cycles;  // planner's cost estimate (for the plan string)
+    long long tile_clk;    // planner's estimate of one K-tile on one CTA, in SM cycles
+    int cluster;           // CTAs per thread-block cluster along the split (1: none)
 };
 
 // CUDA-core depthwise kernel (cpg = kpg = 1).
@@ -104,8 +106,19 @@ struct Plan {
 // Validate and normalise.  Returns a wg_status; *err gets the reason.
 int normalize(const wg_problem* p, Problem* out, std::string* err);
 
-// Choose kernel, tiles, split degree and mode.  num_sms <= 0 means kDefaultSMs.
-int make_plan(const wg_problem* p, const wg_options* opt, int num_sms, Plan* out, std::string* err);
+// Device facts the planner uses: SM count and, for clusters of 1, 2, 4 and 8
+// CTAs of the tensor-core kernel at its largest shared-memory size, how many
+// CTAs fit on the device at once (clusters must sit within one GPC).
+struct DeviceCaps {
+    int num_sms;
+    int cluster_ctas[4];
+};
+
+// GB300 values (measured), used when no device can be queried.
+DeviceCaps default_caps(int num_sms);
+
+// Choose kernel, tiles, split degree, cluster size and mode.
+int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps, Plan* out, std::string* err);
 
 std::string plan_string(const Plan& pl);
 

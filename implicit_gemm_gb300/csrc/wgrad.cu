@@ -18,6 +18,8 @@
 namespace {
 
 thread_local std::string g_err;
+// Event recorded after each call's main kernel (wg_set_mark_event); null = off.
+thread_local cudaEvent_t g_mark = nullptr;
 
 int set_err(int status, const std::string& msg)
 {
@@ -49,6 +51,25 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
+// Raise a kernel's dynamic shared-memory limit when a launch needs more than
+// any earlier one (per device).
+template <typename K>
+int ensure_smem(K kernel, int bytes)
+{
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> done;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = done.find(key);
+    if (it != done.end() && it->second >= bytes) return WG_OK;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", e);
+    done[key] = bytes;
+    return WG_OK;
+}
+
 // SM count of the current device (kDefaultSMs when no device is visible, so
 // host-only queries give the same plan on a machine without a GPU).
 int num_sms()
@@ -65,20 +86,65 @@ int num_sms()
     return n;
 }
 
-// Plans are a pure function of (problem, options, SM count); successful ones
-// are cached so that repeated calls skip the tile search.
+// Device facts for the planner: SM count, and how many CTAs of the
+// tensor-core kernel (at its largest shared-memory size) fit at once in
+// clusters of 1, 2, 4 and 8, from the occupancy calculator.  Queried once per
+// device; GB300 defaults when there is no device.
+wg::DeviceCaps device_caps()
+{
+    static std::mutex mu;
+    static std::map<int, wg::DeviceCaps> cache;
+    const int sms = num_sms();
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return wg::default_caps(sms);
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    wg::DeviceCaps c = wg::default_caps(sms);
+    const int smem = wg::kMaxSmemPerCta;
+    if (ensure_smem(wg::igemm_wgrad_kernel, smem) == WG_OK) {
+        for (int i = 0, q = 1; i < 4; ++i, q *= 2) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 1;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = (unsigned)q;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            cfg.gridDim = dim3(1, 1, (unsigned)q);
+            cfg.blockDim = dim3(192);
+            cfg.dynamicSmemBytes = (size_t)smem;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, wg::igemm_wgrad_kernel, &cfg) == cudaSuccess && n > 0)
+                c.cluster_ctas[i] = n * q;
+            else
+                cudaGetLastError();
+        }
+    } else {
+        cudaGetLastError();
+    }
+    cache.emplace(dev, c);
+    return c;
+}
+
+// Plans are a pure function of (problem, options, device facts); successful
+// ones are cached so that repeated calls skip the tile search.
 int plan_for(const wg_problem* p, const wg_options* opt, wg::Plan* pl, std::string* key_out = nullptr)
 {
     static std::mutex mu;
     static std::map<std::string, wg::Plan> cache;
-    const int sms = num_sms();
+    const wg::DeviceCaps caps = device_caps();
     std::string key;
     if (p) {
-        wg_options o{0, WG_MODE_AUTO, 0};
+        wg_options o{0, WG_MODE_AUTO, 0, 0};
         if (opt) o = *opt;
         key.assign(reinterpret_cast<const char*>(p), sizeof *p);
         key.append(reinterpret_cast<const char*>(&o), sizeof o);
-        key.append(reinterpret_cast<const char*>(&sms), sizeof sms);
+        key.append(reinterpret_cast<const char*>(&caps), sizeof caps);
         std::lock_guard<std::mutex> lk(mu);
         auto it = cache.find(key);
         if (it != cache.end()) {
@@ -88,7 +154,7 @@ int plan_for(const wg_problem* p, const wg_options* opt, wg::Plan* pl, std::stri
         }
     }
     std::string err;
-    const int st = wg::make_plan(p, opt, sms, pl, &err);
+    const int st = wg::make_plan(p, opt, caps, pl, &err);
     if (st) return set_err(st, err);
     std::lock_guard<std::mutex> lk(mu);
     if (cache.size() > 1024) cache.clear();
@@ -119,25 +185,6 @@ int encode(CUtensorMap* tm, int in_dtype, void* base, const cuuint64_t dims[5], 
                  box[0], box[1], box[2], box[3], box[4]);
         return set_err(WG_ERR_CUDA, buf);
     }
-    return WG_OK;
-}
-
-// Raise a kernel's dynamic shared-memory limit when a launch needs more than
-// any earlier one (per device).
-template <typename K>
-int ensure_smem(K kernel, int bytes)
-{
-    static std::mutex mu;
-    static std::map<std::pair<const void*, int>, int> done;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
-    std::lock_guard<std::mutex> lk(mu);
-    auto it = done.find(key);
-    if (it != done.end() && it->second >= bytes) return WG_OK;
-    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", e);
-    done[key] = bytes;
     return WG_OK;
 }
 
@@ -215,8 +262,26 @@ int prepare_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, v
     prm.stage_bytes = ig.stage_bytes, prm.stages = ig.stages, prm.tmem_cols = ig.tmem_cols;
     prm.idesc = wg::make_idesc_f16(pb.in_dtype == WG_BF16, true, true, 128, ig.Nt);
     prm.mode = pl.mode, prm.out_dtype = pb.out_dtype;
+    prm.clq = ig.cluster;
     prm.out = pl.mode == wg::MODE_DETERMINISTIC ? ws : dw;
     prm.split_stride = pb.dw_elems;
+    // K-step descriptor parts: pixel row r of the tile (w fastest) sits at patch
+    // row ((in*PD + id)*PH + ih)*PW + iw of a halo patch, at row r of a per-tap box.
+    for (int ks = 0; ks < 16 && ks < ig.KT / 16; ++ks) {
+        unsigned r[2];
+        for (int h = 0; h < 2; ++h) {
+            int q = 16 * ks + 8 * h;
+            const int iw = q % ig.box[0];
+            q /= ig.box[0];
+            const int ih = q % ig.box[1];
+            q /= ig.box[1];
+            const int id = q % ig.box[2];
+            const int in = q / ig.box[2];
+            r[h] = ig.halo ? (unsigned)(((in * ig.patch[2] + id) * ig.patch[1] + ih) * ig.patch[0] + iw)
+                           : (unsigned)(16 * ks + 8 * h);
+        }
+        prm.kd_table[ks] = ((unsigned long long)((r[1] - r[0]) * 8u) << 32) + (unsigned long long)(r[0] * 8u);
+    }
     if (ig.halo) {
         memcpy(prm.patch_ph, ig.patch_ph, sizeof prm.patch_ph);
         for (int i = 0; i < ig.n_atoms; ++i) {
@@ -228,14 +293,36 @@ int prepare_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, v
     return WG_OK;
 }
 
+// Stage 2 of deterministic split-K, launched as a programmatic dependent of the
+// split-K kernel just before it on the stream.
 int launch_reduce(const wg::Problem& pb, int S, void* ws, void* dw, cudaStream_t stream)
 {
-    const long long n = (pb.dw_elems & 3) ? pb.dw_elems : pb.dw_elems / 4;
-    const long long blocks = (n + wg::kRedVecs - 1) / wg::kRedVecs;
-    wg::reduce_splits_kernel<<<(unsigned)blocks, dim3(wg::kRedVecs, wg::kRedLanes), 0, stream>>>(
-        static_cast<const float*>(ws), dw, pb.dw_elems, S, pb.out_dtype);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail("reduce_splits_kernel launch", e);
+    const long long E = pb.dw_elems;
+    constexpr int kRedSmem = 200 * 1024;
+    int chunk = (int)std::min<long long>(4096, (kRedSmem / (4LL * S)) & ~3LL);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.stream = stream;
+    cfg.blockDim = dim3(wg::kRedThreads);
+    cudaError_t e;
+    const float* wsf = static_cast<const float*>(ws);
+    if ((E & 3) == 0 && chunk >= 4) {
+        chunk = (int)std::min<long long>(chunk, E);
+        const int smem = chunk * 4 * S + 128;
+        const int st = ensure_smem(wg::reduce_splits_bulk_kernel, smem);
+        if (st) return st;
+        cfg.gridDim = dim3((unsigned)((E + chunk - 1) / chunk));
+        cfg.dynamicSmemBytes = (size_t)smem;
+        e = cudaLaunchKernelEx(&cfg, wg::reduce_splits_bulk_kernel, wsf, dw, E, S, pb.out_dtype, chunk);
+    } else {
+        cfg.gridDim = dim3((unsigned)((E + wg::kRedThreads - 1) / wg::kRedThreads));
+        e = cudaLaunchKernelEx(&cfg, wg::reduce_splits_kernel, wsf, dw, E, S, pb.out_dtype);
+    }
+    if (e != cudaSuccess) return cuda_fail("reduce_splits launch", e);
     return WG_OK;
 }
 
@@ -249,12 +336,31 @@ int launch_igemm(const wg::Plan& pl, const Prepared& pr, void* dw, void* ws, cud
         const cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)pb.dw_elems * 4, stream);
         if (e != cudaSuccess) return cuda_fail("cudaMemsetAsync(dW)", e);
     }
-    wg::igemm_wgrad_kernel<<<dim3(pl.grid[0], pl.grid[1], pl.grid[2]), pl.block, ig.smem_bytes, stream>>>(pr.tmx, pr.tmy,
-                                                                                                          pr.ig);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if (ig.cluster > 1) {
+        // Consecutive splits form a cluster (grid z is a multiple of the cluster size).
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = (unsigned)ig.cluster;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(pl.grid[0], pl.grid[1], pl.grid[2]);
+        cfg.blockDim = dim3(pl.block);
+        cfg.dynamicSmemBytes = (size_t)ig.smem_bytes;
+        cfg.stream = stream;
+        e = cudaLaunchKernelEx(&cfg, wg::igemm_wgrad_kernel, pr.tmx, pr.tmy, pr.ig);
+    } else {
+        wg::igemm_wgrad_kernel<<<dim3(pl.grid[0], pl.grid[1], pl.grid[2]), pl.block, ig.smem_bytes, stream>>>(
+            pr.tmx, pr.tmy, pr.ig);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return cuda_fail("igemm_wgrad_kernel launch", e);
+    if (g_mark && (e = cudaEventRecord(g_mark, stream)) != cudaSuccess) return cuda_fail("cudaEventRecord(mark)", e);
     if (pl.mode == wg::MODE_DETERMINISTIC) {
-        st = launch_reduce(pb, pl.S, ws, dw, stream);
+        st = launch_reduce(pb, pl.S / ig.cluster, ws, dw, stream);
         if (st) return st;
     }
     return WG_OK;
@@ -340,6 +446,10 @@ int launch_depthwise(const wg::Plan& pl, const Prepared& pr, void* dw, void* ws,
     int st = pb.in_dtype == WG_BF16 ? launch_dw_b<true>(pl, pr.tmx, pr.tmy, pr.dw, stream)
                                     : launch_dw_b<false>(pl, pr.tmx, pr.tmy, pr.dw, stream);
     if (st) return st;
+    if (g_mark) {
+        const cudaError_t e = cudaEventRecord(g_mark, stream);
+        if (e != cudaSuccess) return cuda_fail("cudaEventRecord(mark)", e);
+    }
     if (pl.mode == wg::MODE_DETERMINISTIC) {
         st = launch_reduce(pb, pl.S, ws, dw, stream);
         if (st) return st;
@@ -366,6 +476,12 @@ const char* wg_status_string(int s)
 }
 
 const char* wg_last_error(void) { return g_err.c_str(); }
+
+int wg_set_mark_event(void* event)
+{
+    g_mark = static_cast<cudaEvent_t>(event);
+    return WG_OK;
+}
 
 int wg_problem_normalize(wg_problem* p)
 {
@@ -431,7 +547,7 @@ int wg_conv_bwd_weight(const wg_problem* p, const void* x, const void* dy, void*
                                        : prepare_depthwise(pl, x, dy, dw, workspace, &pr);
         if (st) return st;
         std::lock_guard<std::mutex> lk(g_prep_mu);
-        if (prep_cache().size() > 256) prep_cache().clear();
+        if (prep_cache().size() > 4096) prep_cache().clear();
         prep_cache().emplace(key, pr);
     }
     st = pl.kind == wg::KIND_IGEMM ? launch_igemm(pl, pr, dw, workspace, s) : launch_depthwise(pl, pr, dw, workspace, s);
@@ -505,7 +621,7 @@ int wg_conv_bwd_weight_noalloc(const wg_problem* p, const void* x, const void* d
     void* scratch = nullptr;
     int st = noalloc_scratch(&scratch);
     if (st) return st;
-    wg_options o{0, WG_MODE_AUTO, 0};
+    wg_options o{0, WG_MODE_AUTO, 0, 0};
     if (opt) o = *opt;
     size_t need = 0;
     st = wg_workspace_size(p, &o, &need);

@@ -96,11 +96,22 @@ typedef struct {
  *  mode:        see wg_mode.
  *  group_merge: depthwise problems only (C = K = 1): channels handled per thread
  *               vector (1, 2, 4 or 8); 0 = choose automatically.  Must be 0 or 1
- *               for other problems. */
+ *               for other problems.
+ *  cluster:     tensor-core path only: consecutive splits run as thread-block
+ *               clusters of this many CTAs (2, 4 or 8), which add their partial
+ *               sums in distributed shared memory (in cluster-rank order) before
+ *               anything leaves the SMs, so only S / cluster partial sums per dW
+ *               element reach memory.  0 or 1 = no clusters (the default:
+ *               distributed shared memory is slow enough on GB300 that this was
+ *               slower than the two-stage path on every workload measured).
+ *               Must divide split_k; must be 0 or 1 for the depthwise kernel.
+ *               With S == cluster the sums are final: mode DIRECT then accepts
+ *               the split, and no workspace is needed. */
 typedef struct {
     int split_k;
     wg_mode mode;
     int group_merge;
+    int cluster;
 } wg_options;
 
 /* Validate `p` and fill p->out[] with the derived output lengths
@@ -163,6 +174,17 @@ WG_API const char* wg_last_error(void);
  * threads) race on it and must be serialised by the caller. */
 WG_API int wg_conv_bwd_weight_noalloc(const wg_problem* p, const void* x, const void* dy, void* dw,
                                       const wg_options* opt, void* stream);
+
+/* Measurement hook (no counterpart in the CK page: it exists so that the
+ * kernels of one call can be timed separately with CUDA events).  While
+ * `event` (a cudaEvent_t owned by the caller, valid while set) is non-NULL,
+ * every wg_conv_bwd_weight / wg_conv_bwd_weight_noalloc call made by this host
+ * thread records it on the call's stream right after the call's main kernel
+ * (the tensor-core or depthwise kernel), before the split-K reduction kernel
+ * if the plan has one.  Between those two kernels the record takes away the
+ * reduction's early launch (programmatic dependent launch), so a step timed
+ * with it set is slightly slower.  NULL turns it off.  Returns WG_OK.  Host only. */
+WG_API int wg_set_mark_event(void* event);
 
 #ifdef __cplusplus
 }

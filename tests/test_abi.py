@@ -82,10 +82,40 @@ def test_workspace_sizes():
     sp = WORKLOADS["2d_dense_n32_h56_c64_k64"][0]
     E = 1 * 64 * 9 * 64
     assert binding.wg_workspace_size(sp, split_k=1) == 0
-    assert binding.wg_workspace_size(sp, split_k=4, mode="deterministic") == 4 * E * 4
+    assert binding.wg_workspace_size(sp, split_k=4, mode="deterministic", cluster=1) == 4 * E * 4
+    # Clusters add their splits on chip: one partial sum per cluster reaches memory.
+    assert binding.wg_workspace_size(sp, split_k=8, mode="deterministic", cluster=2) == 4 * E * 4
+    assert binding.wg_workspace_size(sp, split_k=8, mode="deterministic", cluster=4) == 2 * E * 4
+    # One cluster holds every split: its sums are final, no workspace.
+    assert binding.wg_workspace_size(sp, split_k=4, mode="deterministic", cluster=4) == 0
+    assert "mode=direct" in binding.wg_plan_string(sp, split_k=8, mode="direct", cluster=8)
     sp5 = WORKLOADS["3d_n4_d16_c128_k96_s2"][0]
     assert binding.wg_workspace_size(sp5, split_k=8, mode="atomic") == 0
-    assert binding.wg_workspace_size(sp5, split_k=8, mode="deterministic") == 8 * 96 * 27 * 128 * 4
+    assert binding.wg_workspace_size(sp5, split_k=8, mode="deterministic", cluster=1) == 8 * 96 * 27 * 128 * 4
+
+
+def test_cluster_option_checks():
+    sp = WORKLOADS["2d_dense_n32_h56_c64_k64"][0]
+    for bad in (3, 16, -1):
+        with pytest.raises(binding.WgradError) as e:
+            binding.wg_plan_string(sp, cluster=bad)
+        assert e.value.status == 1
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_plan_string(sp, split_k=6, cluster=4)
+    assert e.value.status == 1 and "divide" in binding.wg_last_error()
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_plan_string(sp, split_k=4, mode="direct", cluster=2)
+    assert e.value.status == 1
+    dw = WORKLOADS["2d_depthwise_g512_n64_h28"][0]
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_plan_string(dw, cluster=2)
+    assert e.value.status == 2
+    # Automatic choice: grid z a multiple of the cluster size.
+    for name in WORKLOADS:
+        ps = binding.wg_plan_string(WORKLOADS[name][0])
+        if "igemm" in ps:
+            S, q = int(re.search(r" S=(\d+)", ps).group(1)), int(re.search(r"cluster=(\d+)", ps).group(1))
+            assert S % q == 0, ps
 
 
 def test_launch_argument_checks_before_device(lib):
@@ -116,3 +146,9 @@ def test_depthwise_merge_degrees():
     sp = WORKLOADS["2d_depthwise_g512_n64_h28"][0]
     for gm in (1, 2, 4, 8):
         assert f"Gm={gm} " in binding.wg_plan_string(sp, group_merge=gm)
+
+
+def test_mark_event_can_be_cleared_without_device(lib):
+    # Setting and clearing the measurement hook touches no device state.
+    binding.wg_set_mark_event(None)
+    assert lib.wg_set_mark_event(None) == 0

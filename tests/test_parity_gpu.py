@@ -36,12 +36,12 @@ def to_dev(bits, dtype):
 _TDT = {"fp32": "float32", "bf16": "bfloat16", "fp16": "float16"}
 
 
-def run_gpu(sp, x, dy, split_k=0, mode="auto", gm=0, xd=None, dyd=None):
+def run_gpu(sp, x, dy, split_k=0, mode="auto", gm=0, xd=None, dyd=None, cluster=0):
     xd = to_dev(x, sp["in_dtype"]) if xd is None else xd
     dyd = to_dev(dy, sp["in_dtype"]) if dyd is None else dyd
     out = torch.full((sp["G"], sp["K"], *sp["filt"], sp["C"]), float("nan"),
                      dtype=getattr(torch, _TDT[sp["out_dtype"]]), device="cuda")
-    binding.conv_bwd_weight(sp, xd, dyd, split_k, mode, gm, out=out)
+    binding.conv_bwd_weight(sp, xd, dyd, split_k, mode, gm, out=out, cluster=cluster)
     binding.wg_check_status()
     return out.float().cpu().numpy().astype(np.float64)
 
@@ -62,31 +62,54 @@ def workload(name):
     return _WCACHE[name]
 
 
+# (workload, split_k, mode, group_merge, cluster)
 WORKLOAD_MODES = [
-    ("2d_tiny_n1_h8_c16_k32", 0, "auto", 0),
-    ("2d_dense_n32_h56_c64_k64", 1, "direct", 0),
-    ("2d_dense_n32_h56_c64_k64", 4, "deterministic", 0),
-    ("2d_dense_n32_h56_c64_k64", 0, "auto", 0),
-    ("2d_grouped_g32_c8_k8_n32_h28", 0, "auto", 0),
-    ("2d_grouped_g32_c8_k8_n32_h28", 0, "atomic", 0),
-    ("2d_depthwise_g512_n64_h28", 0, "auto", 1),
-    ("2d_depthwise_g512_n64_h28", 0, "auto", 2),
-    ("2d_depthwise_g512_n64_h28", 0, "auto", 4),
-    ("2d_depthwise_g512_n64_h28", 0, "auto", 8),
-    ("2d_depthwise_g512_n64_h28", 0, "atomic", 8),
-    ("2d_depthwise_g512_n64_h28", 1, "direct", 8),
-    ("3d_n4_d16_c128_k96_s2", 8, "atomic", 0),
-    ("3d_n4_d16_c128_k96_s2", 8, "deterministic", 0),
-    ("3d_n4_d16_c128_k96_s2", 0, "auto", 0),
+    ("2d_tiny_n1_h8_c16_k32", 0, "auto", 0, 0),
+    ("2d_tiny_n1_h8_c16_k32", 4, "direct", 0, 4),
+    ("2d_dense_n32_h56_c64_k64", 1, "direct", 0, 0),
+    ("2d_dense_n32_h56_c64_k64", 4, "deterministic", 0, 1),
+    ("2d_dense_n32_h56_c64_k64", 0, "auto", 0, 0),
+    ("2d_dense_n32_h56_c64_k64", 0, "auto", 0, 1),
+    ("2d_dense_n32_h56_c64_k64", 0, "auto", 0, 2),
+    ("2d_dense_n32_h56_c64_k64", 0, "auto", 0, 4),
+    ("2d_dense_n32_h56_c64_k64", 8, "direct", 0, 8),
+    ("2d_grouped_g32_c8_k8_n32_h28", 0, "auto", 0, 0),
+    ("2d_grouped_g32_c8_k8_n32_h28", 0, "atomic", 0, 0),
+    ("2d_grouped_g32_c8_k8_n32_h28", 32, "deterministic", 0, 4),
+    ("2d_grouped_g32_c8_k8_n32_h28", 16, "atomic", 0, 8),
+    ("2d_depthwise_g512_n64_h28", 0, "auto", 1, 0),
+    ("2d_depthwise_g512_n64_h28", 0, "auto", 2, 0),
+    ("2d_depthwise_g512_n64_h28", 0, "auto", 4, 0),
+    ("2d_depthwise_g512_n64_h28", 0, "auto", 8, 0),
+    ("2d_depthwise_g512_n64_h28", 0, "atomic", 8, 0),
+    ("2d_depthwise_g512_n64_h28", 1, "direct", 8, 0),
+    ("3d_n4_d16_c128_k96_s2", 8, "atomic", 0, 0),
+    ("3d_n4_d16_c128_k96_s2", 8, "deterministic", 0, 1),
+    ("3d_n4_d16_c128_k96_s2", 16, "deterministic", 0, 2),
+    ("3d_n4_d16_c128_k96_s2", 0, "auto", 0, 0),
 ]
 
 
-@pytest.mark.parametrize("name,split_k,mode,gm", WORKLOAD_MODES,
-                         ids=[f"{w[0]}-S{w[1]}-{w[2]}-gm{w[3]}" for w in WORKLOAD_MODES])
-def test_workload_full(name, split_k, mode, gm):
+@pytest.mark.parametrize("name,split_k,mode,gm,cluster", WORKLOAD_MODES,
+                         ids=[f"{w[0]}-S{w[1]}-{w[2]}-gm{w[3]}-cl{w[4]}" for w in WORKLOAD_MODES])
+def test_workload_full(name, split_k, mode, gm, cluster):
     sp, x, dy, (dw, A) = workload(name)
-    got = run_gpu(sp, x, dy, split_k, mode, gm)
-    assert_close(got, dw, A, sp["out_dtype"], f"{name} S={split_k} {mode} gm={gm}")
+    if not _supported(sp, split_k, mode, gm, cluster):
+        pytest.skip("the planner reports this combination as not supported")
+    got = run_gpu(sp, x, dy, split_k, mode, gm, cluster=cluster)
+    assert_close(got, dw, A, sp["out_dtype"], f"{name} S={split_k} {mode} gm={gm} cluster={cluster}")
+
+
+def _supported(sp, split_k, mode, gm, cluster):
+    """False where the planner answers WG_ERR_NOT_SUPPORTED (e.g. a cluster whose
+    partial sums do not fit shared memory); any other error propagates."""
+    try:
+        binding.wg_plan_string(sp, split_k, mode, gm, cluster=cluster)
+    except binding.WgradError as e:
+        if e.status == 2:
+            return False
+        raise
+    return True
 
 
 SMALL = [
@@ -112,7 +135,10 @@ SMALL = [
     spec(1, 24, 3, 1, 1, [40], [3], [1], [1], [1], [1]),
     spec(3, 8, 2, 1, 1, [5, 5, 5], [3, 3, 3], [1, 1, 1], [1, 1, 1], [1, 1, 1], [1, 1, 1]),
 ]
-MODES = [(0, "auto"), (1, "direct"), (3, "deterministic"), (5, "atomic"), (64, "deterministic")]
+# (split_k, mode, cluster): 0 = automatic; cluster > 1 adds splits on chip.
+MODES = [(0, "auto", 0), (1, "direct", 0), (3, "deterministic", 0), (5, "atomic", 0), (64, "deterministic", 1),
+         (64, "deterministic", 8), (8, "deterministic", 2), (4, "direct", 4), (8, "atomic", 8),
+         (16, "deterministic", 4)]
 
 
 def _ids(sp):
@@ -124,11 +150,11 @@ def _ids(sp):
 def test_small_problems_all_modes(sp):
     x, dy = make_inputs(sp, ("uniform", -1.0, 1.0), 7, 8)
     dw, A = ref(sp, x, dy)
-    for split_k, mode in MODES:
-        if mode == "atomic" and sp["out_dtype"] != "fp32":
+    for split_k, mode, cl in MODES:
+        if (mode == "atomic" and sp["out_dtype"] != "fp32") or not _supported(sp, split_k, mode, 0, cl):
             continue
-        got = run_gpu(sp, x, dy, split_k, mode)
-        assert_close(got, dw, A, sp["out_dtype"], f"{_ids(sp)} S={split_k} {mode}")
+        got = run_gpu(sp, x, dy, split_k, mode, cluster=cl)
+        assert_close(got, dw, A, sp["out_dtype"], f"{_ids(sp)} S={split_k} {mode} cluster={cl}")
 
 
 @pytest.mark.parametrize("sp", [SMALL[0], SMALL[3], SMALL[4], SMALL[10], SMALL[12], SMALL[14], SMALL[15]], ids=_ids)
@@ -136,9 +162,11 @@ def test_integer_inputs_bitwise(sp):
     x, dy = make_inputs(sp, ("int", -2, 2), 17, 18)
     dw, _ = ref(sp, x, dy)
     assert np.all(np.abs(dw) < 2 ** 24)
-    for split_k, mode in MODES:
-        got = run_gpu(sp, x, dy, split_k, mode)
-        np.testing.assert_array_equal(got, dw, err_msg=f"{_ids(sp)} S={split_k} {mode}")
+    for split_k, mode, cl in MODES:
+        if (mode == "atomic" and sp["out_dtype"] != "fp32") or not _supported(sp, split_k, mode, 0, cl):
+            continue
+        got = run_gpu(sp, x, dy, split_k, mode, cluster=cl)
+        np.testing.assert_array_equal(got, dw, err_msg=f"{_ids(sp)} S={split_k} {mode} cluster={cl}")
 
 
 @pytest.mark.parametrize("gm", [1, 2, 4, 8])
@@ -163,9 +191,10 @@ def test_more_splits_than_tiles():
     sp = spec(2, 1, 1, 16, 32, [8, 8], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])
     x, dy = make_inputs(sp, ("int", -2, 2), 37, 38)
     dw, _ = ref(sp, x, dy)
-    for mode in ("deterministic", "atomic"):
-        got = run_gpu(sp, x, dy, 7, mode)
-        np.testing.assert_array_equal(got, dw)
+    for split_k, mode, cl in ((7, "deterministic", 0), (7, "atomic", 0), (8, "direct", 8), (16, "deterministic", 4),
+                              (16, "atomic", 8)):
+        got = run_gpu(sp, x, dy, split_k, mode, cluster=cl)
+        np.testing.assert_array_equal(got, dw, err_msg=f"S={split_k} {mode} cluster={cl}")
 
 
 def test_status_clear_after_runs():

@@ -79,6 +79,6 @@ def test_noalloc_rejects_oversized_split():
     xd, dyd = _dev(x, sp["in_dtype"]), _dev(dy, sp["in_dtype"])
     out = _out(sp)
     with pytest.raises(binding.WgradError) as e:
-        binding.wg_conv_bwd_weight_noalloc(sp, xd, dyd, out, 200, "deterministic")
+        binding.wg_conv_bwd_weight_noalloc(sp, xd, dyd, out, 200, "deterministic", cluster=1)
     assert e.value.status == 4
     assert "scratch" in binding.wg_last_error()

@@ -33,7 +33,7 @@ struct DwParams {
     int stages, x_bytes_al, stage_bytes, x_tx, dy_tx;
     int mode, out_dtype;
     void* out;
-    long long split_stride;
+    WsLayout ws;  // split-K workspace layout (mode 3)
 };
 
 template <bool BF16, int GM>
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
 {
     constexpr int MAXT = 9;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = align_shared<uint8_t>(smem_raw, 1024);
     const int nthreads = blockDim.x - 32;
     const int red_bytes = nthreads * p.T * GM * 4;
     uint8_t* tail = smem + max(p.stages * p.stage_bytes, red_bytes);
@@ -124,6 +124,9 @@ __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
     const int ntl = max(0, min(p.per_split, p.total_tiles - t0));
     const int n_cwarps = nthreads >> 5;
 
+    // A split-reduction kernel launched after this one may take each SM as soon
+    // as this grid's CTA there exits (it waits for the whole grid's results).
+    pdl_launch_dependents();
     if (tid == 0) {
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(&full[i], 1);
@@ -257,7 +260,7 @@ __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
         if (p.mode == 2) {
             if (ntl > 0) red_add_f32(static_cast<float*>(p.out) + o, s);
         } else if (p.mode == 3) {
-            static_cast<float*>(p.out)[split * p.split_stride + o] = s;
+            static_cast<float*>(p.out)[ws_offset(p.ws, o, split)] = s;
         } else if (p.out_dtype == 2) {
             static_cast<float*>(p.out)[o] = s;
         } else if (p.out_dtype == 0) {

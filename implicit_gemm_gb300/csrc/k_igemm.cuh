@@ -40,6 +40,11 @@ namespace wg {
 // Most M-tiles one CTA accumulates (TMEM columns = M-tiles x Nt <= 512).
 constexpr int kMaxMt = 16;
 
+// Threads of igemm_wgrad_kernel: warp 0 lane 0 issues the TMA loads, warp 1
+// the MMAs; after the main loop all eight warps read the accumulators out of
+// TMEM (warp w reads lane quadrant w % 4, columns of half w / 4).
+constexpr int kIgThreads = 256;
+
 struct IgParams {
     int G, C, K, T, GC, GK;
     int X, Y;                // filter extents along w and h (tap = (z*Y + y)*X + x)
@@ -59,7 +64,7 @@ struct IgParams {
     int out_dtype;  // wg_dtype
     int clq;        // CTAs per cluster along the split (1: no cluster reduction)
     void* out;
-    long long split_stride;  // elements between the workspace slices of consecutive clusters
+    WsLayout ws;    // split-K workspace layout (mode 3): rows (g, k) of L = T * C, S / clq partials
     unsigned char patch_ph[32][4];
     unsigned int atom_off[256];
     unsigned short atom_tap[256];
@@ -70,43 +75,70 @@ struct IgParams {
     unsigned long long kd_table[16];
 };
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+// Issue a load of 16 consecutive 32-bit TMEM columns of this warp's 32 lanes
+// into r[0..15]; the registers are valid only after tmem_wait_fence.
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t* r)
 {
-    uint32_t r[16];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
+}
+
+// After tcgen05.wait::ld, mark r[0..15] as rewritten so that no use of them
+// is scheduled before the wait.
+__device__ __forceinline__ void reg_fence16(uint32_t* r)
+{
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]));
+}
+
+// Up to kEpiCols consecutive TMEM columns (n a multiple of 16) with one wait:
+// the loads are issued back to back, so their latencies overlap.
+constexpr int kEpiCols = 32;
+__device__ __forceinline__ void tmem_ld_batch(uint32_t taddr, int n, float (&v)[kEpiCols])
+{
+    uint32_t r[kEpiCols];
+#pragma unroll
+    for (int q = 0; q < kEpiCols / 16; ++q)
+        if (16 * q < n) tmem_ld16_issue(taddr + (uint32_t)(16 * q), r + 16 * q);
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    for (int q = 0; q < kEpiCols / 16; ++q)
+        if (16 * q < n) reg_fence16(r + 16 * q);
+#pragma unroll
+    for (int i = 0; i < kEpiCols; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Epilogue of one M-tile for one warp: TMEM -> registers -> global, in chunks
-// of 16 columns.  MODE 1 stores dW in OUT (fp32, bf16 or fp16), MODE 2 adds
-// to fp32 dW with global atomics, MODE 3 stores fp32 to the split's workspace
-// slice.  Each lane owns one row (tap, c); k runs over the chunk's columns.
+// of up to kEpiCols columns.  MODE 1 stores dW in OUT (fp32, bf16 or fp16), MODE 2
+// adds to fp32 dW with global atomics, MODE 3 stores fp32 to the split's
+// workspace slice.  Each lane owns one row (tap, c); k runs over the columns,
+// so a warp's store covers 32 consecutive channels.
 template <int MODE, typename OUT>
 __device__ __forceinline__ void epilogue_mtile(uint32_t taddr, int ncols, bool have_acc, bool vrow, int n_lo, int K,
                                                OUT* __restrict__ out, long long rowbase, long long kstride)
 {
-    for (int c16 = 0; c16 < ncols; c16 += 16) {
-        float v[16];
+    for (int cb = 0; cb < ncols; cb += kEpiCols) {
+        const int n = min(kEpiCols, ncols - cb);
+        float v[kEpiCols];
         if (have_acc) {
-            tmem_ld16(taddr + (uint32_t)c16, v);
+            tmem_ld_batch(taddr + (uint32_t)cb, n, v);
         } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+            for (int j = 0; j < kEpiCols; ++j) v[j] = 0.f;
         }
         if (!vrow) continue;
-        const int k0 = c16 - n_lo;
+        const int k0 = cb - n_lo;
         OUT* o = out + rowbase + (long long)k0 * kstride;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < kEpiCols; ++j) {
             const int k = k0 + j;
-            if (k >= 0 && k < K) {
+            if (j < n && k >= 0 && k < K) {
                 if constexpr (MODE == 2) {
                     red_add_f32(reinterpret_cast<float*>(o), v[j]);
                 } else if constexpr (sizeof(OUT) == 4) {
@@ -150,11 +182,14 @@ __device__ __forceinline__ RowMap map_row(const IgParams& p, int atom, int row64
     return r;
 }
 
-__device__ __forceinline__ void store_elem(int mode, int out_dtype, void* out, long long i, float v)
+__device__ __forceinline__ void store_elem(int mode, int out_dtype, void* out, long long i, float v,
+                                           const WsLayout& ws, int ws_s)
 {
     if (mode == 2) {
         red_add_f32(static_cast<float*>(out) + i, v);
-    } else if (mode == 3 || out_dtype == 2) {
+    } else if (mode == 3) {
+        static_cast<float*>(out)[ws_offset(ws, i, ws_s)] = v;
+    } else if (out_dtype == 2) {
         static_cast<float*>(out)[i] = v;
     } else if (out_dtype == 0) {
         static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
@@ -163,8 +198,8 @@ __device__ __forceinline__ void store_elem(int mode, int out_dtype, void* out, l
     }
 }
 
-// Cluster reduction of the split-K partial sums, run by the four epilogue
-// warps of every CTA of a cluster once each CTA has staged its accumulators in
+// Cluster reduction of the split-K partial sums, run by the eight warps of
+// every CTA of a cluster once each CTA has staged its accumulators in
 // its own shared memory, column-major (red[(m * Nt + col) * 128 + row]).  The
 // mtn * Nt columns are dealt out to the cluster's CTAs in contiguous ranges;
 // for each of its columns a warp reads the 128 rows (lane = rows lane,
@@ -173,7 +208,7 @@ __device__ __forceinline__ void store_elem(int mode, int out_dtype, void* out, l
 // result is reproducible -- and stores the sums (the dW values, or the
 // cluster's partial sums) as whole 128-byte rows of consecutive channels.
 __device__ __forceinline__ void cluster_reduce_store(const IgParams& p, uint32_t red_s, int mtn, int atom0, int c_al,
-                                                     int g0, int k_base, void* out, int ew, int lane)
+                                                     int g0, int k_base, void* out, int ws_s, int ew, int lane)
 {
     const int Q = p.clq, Nt = p.Nt, K = p.K, mode = p.mode, out_dtype = p.out_dtype;
     const long long kstride = (long long)p.T * p.C;
@@ -185,7 +220,7 @@ __device__ __forceinline__ void cluster_reduce_store(const IgParams& p, uint32_t
     for (int r = 0; r < 8; ++r) peer[r] = r < Q ? mapa_shared(red_s, (uint32_t)r) : 0u;
     int m_cur = -1;
     RowMap rm[4];
-    for (int u = u0 + ew; u < u1; u += 4) {
+    for (int u = u0 + ew; u < u1; u += kIgThreads / 32) {
         float v[8][4];
 #pragma unroll
         for (int r = 0; r < 8; ++r)
@@ -206,7 +241,8 @@ __device__ __forceinline__ void cluster_reduce_store(const IgParams& p, uint32_t
             for (int r = 1; r < 8; ++r)
                 if (r < Q) a += v[r][i];
             const int k = col - rm[i].n_lo;
-            if (rm[i].base >= 0 && k >= 0 && k < K) store_elem(mode, out_dtype, out, rm[i].base + k * kstride, a);
+            if (rm[i].base >= 0 && k >= 0 && k < K)
+                store_elem(mode, out_dtype, out, rm[i].base + k * kstride, a, p.ws, ws_s);
         }
     }
 }
@@ -258,12 +294,12 @@ __device__ __forceinline__ void mma_mainloop(const MmaArgs a, const uint64_t (&a
     __syncwarp();
 }
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kIgThreads, 1)
     igemm_wgrad_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
                        const __grid_constant__ IgParams p)
 {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = align_shared<uint8_t>(smem_raw, 1024);
     // [stages x stage_bytes][1 KB slack read by padding atoms][tail: barriers + tables]
     uint8_t* tail = smem + p.stages * p.stage_bytes + 1024;
     uint64_t* full = reinterpret_cast<uint64_t*>(tail);
@@ -285,6 +321,9 @@ __global__ void __launch_bounds__(192, 1)
     const int c_al = (g0 * p.C) & ~7;
     const int k_base = ((g0 * p.K) & ~7) + nt * p.Nt;
 
+    // A split-reduction kernel launched after this one may take each SM as soon
+    // as this grid's CTA there exits (it waits for the whole grid's results).
+    pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(&full[i], 1);
@@ -299,11 +338,12 @@ __global__ void __launch_bounds__(192, 1)
         tmem_relinquish();
         tc_fence_before();
     }
-    // The TMEM address is read after the allocation, which the MMA and epilogue
-    // warps wait for below; the producer does not need it.
+    // The TMEM address is read after the allocation by the MMA warp (and the
+    // warps that only wait for the epilogue); the producer starts at once and
+    // reads it after the main loop.
     uint32_t tbase = 0;
     if (warp != 0) {
-        named_bar_sync(1, 160);  // warps 1..5
+        named_bar_sync(1, kIgThreads - 32);  // warps 1..7
         tc_fence_after();
         tbase = *tslot;
     }
@@ -396,18 +436,26 @@ __global__ void __launch_bounds__(192, 1)
                 default: mma_mainloop<16>(MMA_ARGS); break;
             }
         }
-    } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
+    }
+    __syncwarp();
+    // ---------------------------------------------------- epilogue (all warps)
+    named_bar_sync(2, kIgThreads);  // the producer is done and may read tbase
+    tc_fence_after();
+    tbase = *tslot;
+    {
         if (nk > 0) {
             mbar_wait_sleep(accb, 0);
             tc_fence_after();
         }
         const int q = warp & 3;
         const int row = q * 32 + lane;
+        // Column half of this warp: [c_lo, c_hi), split at a multiple of 16.
+        const int c_mid = ((Nt >> 1) + 15) & ~15;
+        const int c_lo = warp < 4 ? 0 : c_mid, c_hi = warp < 4 ? c_mid : Nt;
         const int K = p.K, C = p.C, T = p.T, GC = p.GC, Gm = p.Gm, n_atoms = p.n_atoms, ncc = p.ncc, mode = p.mode;
         const int out_dtype = p.out_dtype;
         void* const out = p.out;
-        const long long split_off = (long long)(split / p.clq) * p.split_stride;
+        const int ws_s = split / p.clq;
         const uint32_t trow = tbase + ((uint32_t)(q * 32) << 16);
         const bool have_acc = nk > 0;
         if (p.clq > 1) {
@@ -416,16 +464,18 @@ __global__ void __launch_bounds__(192, 1)
             // consecutive words.
             float* red = reinterpret_cast<float*>(smem);
             for (int m = 0; m < mtn; ++m)
-                for (int c16 = 0; c16 < Nt; c16 += 16) {
-                    float v[16];
+                for (int cb = c_lo; cb < c_hi; cb += kEpiCols) {
+                    const int n = min(kEpiCols, c_hi - cb);
+                    float v[kEpiCols];
                     if (have_acc) {
-                        tmem_ld16(trow + (uint32_t)(m * Nt + c16), v);
+                        tmem_ld_batch(trow + (uint32_t)(m * Nt + cb), n, v);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                        for (int j = 0; j < kEpiCols; ++j) v[j] = 0.f;
                     }
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) red[(m * Nt + c16 + j) * 128 + row] = v[j];
+                    for (int j = 0; j < kEpiCols; ++j)
+                        if (j < n) red[(m * Nt + cb + j) * 128 + row] = v[j];
                 }
         }
         for (int m = 0; m < mtn && p.clq == 1; ++m) {
@@ -448,30 +498,31 @@ __global__ void __launch_bounds__(192, 1)
             const int n_lo = gr * K - k_base;
             const long long rowbase = ((long long)gr * K * T + tap) * C + c;
             const long long kstride = (long long)T * C;
-            const uint32_t ta = trow + (uint32_t)(m * Nt);
+            const uint32_t ta = trow + (uint32_t)(m * Nt + c_lo);
+            const int nc = c_hi - c_lo, nl = n_lo - c_lo;
             if (mode == 3) {
-                epilogue_mtile<3, float>(ta, Nt, have_acc, vrow, n_lo, K, static_cast<float*>(out) + split_off, rowbase,
-                                         kstride);
+                // Workspace: the row's first element (k = 0) and the step per k.
+                const long long x = (long long)tap * C + c;
+                const long long j = x / p.ws.W;
+                const long long wbase = (((long long)gr * K * p.ws.nj + j) * p.ws.S + ws_s) * p.ws.W + (x - j * p.ws.W);
+                epilogue_mtile<3, float>(ta, nc, have_acc, vrow, nl, K, static_cast<float*>(out), wbase,
+                                         (long long)p.ws.nj * p.ws.S * p.ws.W);
             } else if (mode == 2) {
                 if (have_acc)
-                    epilogue_mtile<2, float>(ta, Nt, true, vrow, n_lo, K, static_cast<float*>(out), rowbase, kstride);
+                    epilogue_mtile<2, float>(ta, nc, true, vrow, nl, K, static_cast<float*>(out), rowbase, kstride);
             } else if (out_dtype == 2) {
-                epilogue_mtile<1, float>(ta, Nt, have_acc, vrow, n_lo, K, static_cast<float*>(out), rowbase, kstride);
+                epilogue_mtile<1, float>(ta, nc, have_acc, vrow, nl, K, static_cast<float*>(out), rowbase, kstride);
             } else if (out_dtype == 0) {
-                epilogue_mtile<1, __nv_bfloat16>(ta, Nt, have_acc, vrow, n_lo, K, static_cast<__nv_bfloat16*>(out),
+                epilogue_mtile<1, __nv_bfloat16>(ta, nc, have_acc, vrow, nl, K, static_cast<__nv_bfloat16*>(out),
                                                  rowbase, kstride);
             } else {
-                epilogue_mtile<1, __half>(ta, Nt, have_acc, vrow, n_lo, K, static_cast<__half*>(out), rowbase, kstride);
+                epilogue_mtile<1, __half>(ta, nc, have_acc, vrow, nl, K, static_cast<__half*>(out), rowbase, kstride);
             }
         }
     }
     if (p.clq > 1) {
         cluster_sync_all();  // every CTA of the cluster has staged its partial sums
-        if (warp >= 2) {
-            void* out = p.mode == 3 ? (void*)(static_cast<float*>(p.out) + (long long)(split / p.clq) * p.split_stride)
-                                    : p.out;
-            cluster_reduce_store(p, smem_u32(smem), mtn, atom0, c_al, g0, k_base, out, warp - 2, lane);
-        }
+        cluster_reduce_store(p, smem_u32(smem), mtn, atom0, c_al, g0, k_base, p.out, split / p.clq, warp, lane);
         cluster_sync_all();  // no CTA leaves while another still reads its shared memory
     }
     tc_fence_before();
@@ -483,15 +534,18 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // Stage 2 of the deterministic split-K mode (the two-stage wgrad that PR
-// #11602 and PR #12359 refer to): dW = cast(sum over splits of ws[s]), each
-// element summed over s = 0, 1, ..., S-1 in that order, so the result is
-// bitwise reproducible.
+// #11602 and PR #12359 refer to): dW = cast(sum over splits of ws[s]) in a
+// fixed order that depends on S only: for S >= 8 the splits fall into four
+// contiguous ranges, each summed in index order, and the four range sums are
+// added in range order; for S < 8 one range.  The result is bitwise
+// reproducible.
 //
-// Bulk path (dW element count a multiple of 4): CTA b owns `chunk` consecutive
-// elements; one thread copies that slice of every split into shared memory
-// with cp.async.bulk (all S copies in flight at once), then each thread sums
-// its elements from shared memory.  Launched with programmatic dependent
-// launch: it waits for the split-K kernel's writes with griddepcontrol.wait.
+// Bulk path: CTA b owns workspace slice b (W consecutive elements of one dW
+// row), whose S partials are one contiguous block; one warp pulls it into
+// shared memory with a few large cp.async.bulk copies, then four threads per
+// element add the four split ranges.  Launched with programmatic dependent
+// launch: its set-up overlaps the split-K kernel's tail, and it waits for that
+// kernel's writes with griddepcontrol.wait.
 __device__ __forceinline__ void store_cast(void* dw, long long i, float a, int out_dtype)
 {
     if (out_dtype == 2)
@@ -503,54 +557,92 @@ __device__ __forceinline__ void store_cast(void* dw, long long i, float a, int o
 }
 
 constexpr int kRedThreads = 256;
+constexpr int kRedGroups = 4;
+constexpr uint32_t kRedPiece = 16384;  // bytes per bulk copy
+
+__host__ __device__ __forceinline__ int red_groups(int S) { return S >= 8 ? kRedGroups : 1; }
 
 __global__ void __launch_bounds__(kRedThreads)
-    reduce_splits_bulk_kernel(const float* __restrict__ ws, void* __restrict__ dw, long long E, int S, int out_dtype,
-                              int chunk)
+    reduce_splits_bulk_kernel(const float* __restrict__ ws, void* __restrict__ dw, const WsLayout w, int out_dtype)
 {
     extern __shared__ uint8_t red_raw[];
-    float* sm = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(red_raw) + 127) & ~uintptr_t(127));
+    float* sm = align_shared<float>(red_raw, 128);
     __shared__ uint64_t bar;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const long long e0 = (long long)blockIdx.x * chunk;
-    const int n = (int)min((long long)chunk, E - e0);
-    const uint32_t nbytes = (uint32_t)n * 4u;
+    const int S = w.S, W = w.W;
+    const long long r = blockIdx.x / w.nj;
+    const int j = (int)(blockIdx.x - r * w.nj);
+    const long long x0 = (long long)j * W;
+    const int n = (int)min((long long)W, w.L - x0);
+    const long long e0 = r * w.L + x0;
+    const uint32_t total = (uint32_t)S * (uint32_t)W * 4u;  // the whole slice, tail elements included
     if (threadIdx.x == 0) {
         mbar_init(&bar, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&bar, nbytes * (uint32_t)S);
+        mbar_arrive_expect_tx(&bar, total);
     }
     __syncthreads();
+    // Everything above may run while the split-K kernel is still finishing.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x < 32) {
-        // The copies are issued by a whole warp, one split per lane at a time.
-        for (int s = threadIdx.x; s < S; s += 32) {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(ws + (long long)blockIdx.x * S * W);
+        for (uint32_t off = threadIdx.x * kRedPiece; off < total; off += 32 * kRedPiece) {
+            const uint32_t size = min(kRedPiece, total - off);
             asm volatile(
                 "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    smem_u32(sm + (size_t)s * chunk)),
-                "l"(ws + (long long)s * E + e0), "r"(nbytes), "r"(smem_u32(&bar))
+                    smem_u32(sm) + off),
+                "l"(src + off), "r"(size), "r"(smem_u32(&bar))
                 : "memory");
         }
     }
     if (!mbar_wait(&bar, 0)) return;
+    const int G = red_groups(S);
+    float* part = sm + (size_t)S * W;  // [G][W]
+    // Each thread adds one split range for 4 consecutive elements (W is a
+    // multiple of 4): 16-byte shared-memory loads, four independent chains.
+    const int W4 = W >> 2;
+    for (int idx = threadIdx.x; idx < W4 * G; idx += kRedThreads) {
+        const int g = idx / W4, i4 = idx - g * W4;
+        const int s0 = S * g / G, s1 = S * (g + 1) / G;
+        const float4* q = reinterpret_cast<const float4*>(sm + (size_t)s0 * W) + i4;
+        float4 a = q[0];
+        q += W4;
+        int s = s0 + 1;
+        for (; s + 4 <= s1; s += 4, q += 4 * W4) {
+            float4 v[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) v[jj] = q[jj * W4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) a.x += v[jj].x, a.y += v[jj].y, a.z += v[jj].z, a.w += v[jj].w;
+        }
+        for (; s < s1; ++s, q += W4) a.x += q[0].x, a.y += q[0].y, a.z += q[0].z, a.w += q[0].w;
+        reinterpret_cast<float4*>(part + (size_t)g * W)[i4] = a;
+    }
+    __syncthreads();
     for (int i = threadIdx.x; i < n; i += kRedThreads) {
-        const float* col = sm + i;
-        float a = col[0];
-#pragma unroll 8
-        for (int s = 1; s < S; ++s) a += col[(size_t)s * chunk];
+        float a = part[i];
+        for (int g = 1; g < G; ++g) a += part[g * W + i];
         store_cast(dw, e0 + i, a, out_dtype);
     }
 }
 
-// Fallback for element counts that are not a multiple of 4: one thread per
-// element, same summation order.
+// Fallback for split counts whose slice block does not fit shared memory: one
+// thread per element, same layout and summation order.
 __global__ void __launch_bounds__(kRedThreads)
-    reduce_splits_kernel(const float* __restrict__ ws, void* __restrict__ dw, long long E, int S, int out_dtype)
+    reduce_splits_kernel(const float* __restrict__ ws, void* __restrict__ dw, long long E, const WsLayout w,
+                         int out_dtype)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long i = (long long)blockIdx.x * kRedThreads + threadIdx.x;
     if (i >= E) return;
-    float a = ws[i];
-    for (int s = 1; s < S; ++s) a += ws[(long long)s * E + i];
+    const int S = w.S, G = red_groups(S);
+    const long long o0 = ws_offset(w, i, 0);
+    float a = 0.f;
+    for (int g = 0; g < G; ++g) {
+        const int s0 = S * g / G, s1 = S * (g + 1) / G;
+        float q = ws[o0 + (long long)s0 * w.W];
+        for (int s = s0 + 1; s < s1; ++s) q += ws[o0 + (long long)s * w.W];
+        a = g == 0 ? q : a + q;
+    }
     store_cast(dw, i, a, out_dtype);
 }
 

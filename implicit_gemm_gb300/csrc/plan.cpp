@@ -323,7 +323,7 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
     pl->grid[0] = (unsigned)(ig.n_mranges * ig.n_ntiles);
     pl->grid[1] = (unsigned)ig.n_gblocks;
     pl->grid[2] = (unsigned)S;
-    pl->block = 192;
+    pl->block = 256;  // the kernel's thread count (kIgThreads)
     return WG_OK;
 }
 
@@ -511,7 +511,28 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
         pl->mode = MODE_DIRECT;
     else
         pl->mode = MODE_DETERMINISTIC;
-    pl->ws_bytes = pl->mode == MODE_DETERMINISTIC ? (size_t)n_out * (size_t)pb.dw_elems * 4 : 0;
+    // Workspace rows: one per (g, k) of T*C elements for the tensor-core kernel
+    // (its epilogue walks dW rows), the whole of dW as one row for the
+    // depthwise kernel.  Slices of at most 128 elements, a multiple of 4: the
+    // whole row when it is that short, else the widest such width from 64 to
+    // 128 that divides the row (no padding), else 128.
+    pl->n_out = n_out;
+    pl->ws_rows = pl->kind == KIND_IGEMM ? (long long)pb.G * pb.K : 1;
+    pl->ws_L = pb.dw_elems / pl->ws_rows;
+    if (pl->ws_L <= 128) {
+        pl->ws_W = round_up((int)pl->ws_L, 4);
+    } else {
+        pl->ws_W = 128;
+        for (int w = 128; w >= 64; w -= 4)
+            if (pl->ws_L % w == 0) {
+                pl->ws_W = w;
+                break;
+            }
+    }
+    pl->ws_nj = (int)cdiv(pl->ws_L, pl->ws_W);
+    pl->ws_bytes = pl->mode == MODE_DETERMINISTIC
+                       ? (size_t)pl->ws_rows * pl->ws_nj * (size_t)n_out * pl->ws_W * 4
+                       : 0;
     return WG_OK;
 }
 

@@ -90,12 +90,18 @@ struct DwPlan {
     int sliding;      // 1: register sliding window along W (stride 1, dilation 1 in W)
 };
 
+// Split-K workspace (deterministic mode): dW viewed as ws_rows rows of ws_L
+// elements, each row cut into ws_nj slices of ws_W elements; the n_out
+// partials of a slice are stored together (see WsLayout in ptx.cuh).
 struct Plan {
     Problem pb;
     int kind;
     int mode;
     int S;              // split degree of GemmK
     long long per_split;  // K-tiles (igemm) or row tiles (depthwise) per split
+    int n_out;          // partial sums per dW element that reach memory (S / cluster)
+    long long ws_rows, ws_L;
+    int ws_W, ws_nj;
     size_t ws_bytes;
     unsigned grid[3];
     unsigned block;

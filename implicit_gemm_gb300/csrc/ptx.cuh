@@ -21,11 +21,45 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// `raw` (a dynamic __shared__ array) advanced to the next multiple of `align`
+// bytes of the shared address space.  The result is derived from the shared
+// array by pointer arithmetic, so the compiler keeps accesses through it as
+// shared-memory instructions (a round trip through an integer would make them
+// generic loads and stores).
+template <typename T>
+__device__ __forceinline__ T* align_shared(uint8_t* raw, uint32_t align)
+{
+    const uint32_t pad = (align - (smem_u32(raw) & (align - 1u))) & (align - 1u);
+    return reinterpret_cast<T*>(raw + pad);
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns()
 {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// ---------------------------------------------------------------- split-K workspace
+// fp32 partial sums.  dW is viewed as R rows of L elements (e = r * L + x);
+// each row is cut into nj = ceil(L / W) slices of W elements, and the S
+// partials of one slice are stored together:
+//   offset(e, s) = ((r * nj + x / W) * S + s) * W + x % W
+// so the reduction of a slice reads one contiguous block of S * W floats, and
+// along a row of dW (fixed x, r stepping) the offset steps by nj * S * W.
+// Size: R * nj * S * W floats.
+struct WsLayout {
+    long long L;  // row length
+    int W;        // slice width, a multiple of 4
+    int nj;       // slices per row
+    int S;        // partials
+};
+
+__host__ __device__ __forceinline__ long long ws_offset(const WsLayout& w, long long e, int s)
+{
+    const long long r = e / w.L, x = e - r * w.L;
+    const long long j = x / w.W;
+    return ((r * w.nj + j) * w.S + s) * w.W + (x - j * w.W);
 }
 
 // ---------------------------------------------------------------- mbarrier
@@ -226,6 +260,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Programmatic dependent launch: allow the next kernel on the stream (launched
+// with the programmatic-serialization attribute) to be scheduled now.  Its
+// griddepcontrol.wait still waits for this whole grid to complete and for its
+// memory operations to be visible.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- clusters

@@ -116,7 +116,7 @@ wg::DeviceCaps device_caps()
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             cfg.gridDim = dim3(1, 1, (unsigned)q);
-            cfg.blockDim = dim3(192);
+            cfg.blockDim = dim3(wg::kIgThreads);
             cfg.dynamicSmemBytes = (size_t)smem;
             int n = 0;
             if (cudaOccupancyMaxActiveClusters(&n, wg::igemm_wgrad_kernel, &cfg) == cudaSuccess && n > 0)
@@ -186,6 +186,16 @@ int encode(CUtensorMap* tm, int in_dtype, void* base, const cuuint64_t dims[5], 
         return set_err(WG_ERR_CUDA, buf);
     }
     return WG_OK;
+}
+
+wg::WsLayout ws_layout(const wg::Plan& pl)
+{
+    wg::WsLayout w;
+    w.L = pl.ws_L;
+    w.W = pl.ws_W;
+    w.nj = pl.ws_nj;
+    w.S = pl.n_out;
+    return w;
 }
 
 // Encoded tensor maps and kernel parameters of one (plan, buffers) pair, kept
@@ -264,7 +274,7 @@ int prepare_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, v
     prm.mode = pl.mode, prm.out_dtype = pb.out_dtype;
     prm.clq = ig.cluster;
     prm.out = pl.mode == wg::MODE_DETERMINISTIC ? ws : dw;
-    prm.split_stride = pb.dw_elems;
+    prm.ws = ws_layout(pl);
     // K-step descriptor parts: pixel row r of the tile (w fastest) sits at patch
     // row ((in*PD + id)*PH + ih)*PW + iw of a halo patch, at row r of a per-tap box.
     for (int ks = 0; ks < 16 && ks < ig.KT / 16; ++ks) {
@@ -295,11 +305,12 @@ int prepare_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, v
 
 // Stage 2 of deterministic split-K, launched as a programmatic dependent of the
 // split-K kernel just before it on the stream.
-int launch_reduce(const wg::Problem& pb, int S, void* ws, void* dw, cudaStream_t stream)
+int launch_reduce(const wg::Plan& pl, void* ws, void* dw, cudaStream_t stream)
 {
-    const long long E = pb.dw_elems;
-    constexpr int kRedSmem = 200 * 1024;
-    int chunk = (int)std::min<long long>(4096, (kRedSmem / (4LL * S)) & ~3LL);
+    const wg::Problem& pb = pl.pb;
+    const wg::WsLayout w = ws_layout(pl);
+    // One CTA per workspace slice: S partial rows of W plus the range sums.
+    const long long smem = (long long)(w.S + wg::kRedGroups) * w.W * 4 + 128;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -310,17 +321,16 @@ int launch_reduce(const wg::Problem& pb, int S, void* ws, void* dw, cudaStream_t
     cfg.blockDim = dim3(wg::kRedThreads);
     cudaError_t e;
     const float* wsf = static_cast<const float*>(ws);
-    if ((E & 3) == 0 && chunk >= 4) {
-        chunk = (int)std::min<long long>(chunk, E);
-        const int smem = chunk * 4 * S + 128;
-        const int st = ensure_smem(wg::reduce_splits_bulk_kernel, smem);
+    const long long n_slices = pl.ws_rows * w.nj;
+    if (smem <= wg::kMaxSmemPerCta && n_slices < (1LL << 31)) {
+        const int st = ensure_smem(wg::reduce_splits_bulk_kernel, (int)smem);
         if (st) return st;
-        cfg.gridDim = dim3((unsigned)((E + chunk - 1) / chunk));
+        cfg.gridDim = dim3((unsigned)n_slices);
         cfg.dynamicSmemBytes = (size_t)smem;
-        e = cudaLaunchKernelEx(&cfg, wg::reduce_splits_bulk_kernel, wsf, dw, E, S, pb.out_dtype, chunk);
+        e = cudaLaunchKernelEx(&cfg, wg::reduce_splits_bulk_kernel, wsf, dw, w, pb.out_dtype);
     } else {
-        cfg.gridDim = dim3((unsigned)((E + wg::kRedThreads - 1) / wg::kRedThreads));
-        e = cudaLaunchKernelEx(&cfg, wg::reduce_splits_kernel, wsf, dw, E, S, pb.out_dtype);
+        cfg.gridDim = dim3((unsigned)((pb.dw_elems + wg::kRedThreads - 1) / wg::kRedThreads));
+        e = cudaLaunchKernelEx(&cfg, wg::reduce_splits_kernel, wsf, dw, pb.dw_elems, w, pb.out_dtype);
     }
     if (e != cudaSuccess) return cuda_fail("reduce_splits launch", e);
     return WG_OK;
@@ -360,7 +370,7 @@ int launch_igemm(const wg::Plan& pl, const Prepared& pr, void* dw, void* ws, cud
     if (e != cudaSuccess) return cuda_fail("igemm_wgrad_kernel launch", e);
     if (g_mark && (e = cudaEventRecord(g_mark, stream)) != cudaSuccess) return cuda_fail("cudaEventRecord(mark)", e);
     if (pl.mode == wg::MODE_DETERMINISTIC) {
-        st = launch_reduce(pb, pl.S / ig.cluster, ws, dw, stream);
+        st = launch_reduce(pl, ws, dw, stream);
         if (st) return st;
     }
     return WG_OK;
@@ -432,7 +442,7 @@ int prepare_depthwise(const wg::Plan& pl, const void* x, const void* dy, void* d
     prm.x_tx = d.x_bytes, prm.dy_tx = d.dy_bytes;
     prm.mode = pl.mode, prm.out_dtype = pb.out_dtype;
     prm.out = pl.mode == wg::MODE_DETERMINISTIC ? ws : dw;
-    prm.split_stride = pb.dw_elems;
+    prm.ws = ws_layout(pl);
     return WG_OK;
 }
 
@@ -451,7 +461,7 @@ int launch_depthwise(const wg::Plan& pl, const Prepared& pr, void* dw, void* ws,
         if (e != cudaSuccess) return cuda_fail("cudaEventRecord(mark)", e);
     }
     if (pl.mode == wg::MODE_DETERMINISTIC) {
-        st = launch_reduce(pb, pl.S, ws, dw, stream);
+        st = launch_reduce(pl, ws, dw, stream);
         if (st) return st;
     }
     return WG_OK;
@@ -630,7 +640,14 @@ int wg_conv_bwd_weight_noalloc(const wg_problem* p, const void* x, const void* d
         wg::Problem pb;
         std::string err;
         if (wg::normalize(p, &pb, &err)) return set_err(WG_ERR_INVALID_ARGUMENT, err);
-        const size_t per_split = (size_t)pb.dw_elems * 4;
+        // Workspace bytes per partial (rows of whole 4-element-aligned slices).
+        wg::Plan pl1;
+        wg_options o1 = o;
+        o1.split_k = 1;
+        o1.mode = WG_MODE_DETERMINISTIC;
+        o1.cluster = 1;
+        if (plan_for(p, &o1, &pl1)) return WG_ERR_INVALID_ARGUMENT;
+        const size_t per_split = (size_t)pl1.ws_rows * pl1.ws_nj * pl1.ws_W * 4;
         const size_t fit = kNoAllocScratchBytes / per_split;
         if (o.split_k != 0 || fit < 2) {
             char buf[256];

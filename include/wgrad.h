@@ -54,8 +54,10 @@ typedef enum { WG_BF16 = 0, WG_FP16 = 1, WG_FP32 = 2 } wg_dtype;
  *                 CK page), then every split adds its fp32 partial with a
  *                 global atomic.  fp32 dW only.  Not bitwise reproducible.
  *  DETERMINISTIC: two-stage: every split writes an fp32 partial to the
- *                 workspace, then a second kernel sums the splits in index
- *                 order s = 0..S-1 and casts (round to nearest even) to dW.
+ *                 workspace, then a second kernel sums the splits in a fixed
+ *                 order (for S >= 8: four contiguous ranges of splits, each in
+ *                 index order, then the range sums in range order; for S < 8:
+ *                 index order) and casts (round to nearest even) to dW.
  *                 Bitwise reproducible for a given problem and split degree.
  *  AUTO:          DIRECT when the chosen split degree is 1, else DETERMINISTIC. */
 typedef enum {

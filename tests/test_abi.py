@@ -80,7 +80,7 @@ def test_not_supported_paths():
 
 def test_workspace_sizes():
     sp = WORKLOADS["2d_dense_n32_h56_c64_k64"][0]
-    E = 1 * 64 * 9 * 64
+    E = 1 * 64 * 9 * 64  # rows of 576 = 6 slices of 96: no padding
     assert binding.wg_workspace_size(sp, split_k=1) == 0
     assert binding.wg_workspace_size(sp, split_k=4, mode="deterministic", cluster=1) == 4 * E * 4
     # Clusters add their splits on chip: one partial sum per cluster reaches memory.
@@ -92,6 +92,12 @@ def test_workspace_sizes():
     sp5 = WORKLOADS["3d_n4_d16_c128_k96_s2"][0]
     assert binding.wg_workspace_size(sp5, split_k=8, mode="atomic") == 0
     assert binding.wg_workspace_size(sp5, split_k=8, mode="deterministic", cluster=1) == 8 * 96 * 27 * 128 * 4
+    # Rows (g, k) of T*C = 9*12 = 108 elements, one slice of 108 each.
+    sp6 = spec(2, 2, 1, 12, 8, [9, 9], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])
+    assert binding.wg_workspace_size(sp6, split_k=5, mode="deterministic") == 5 * 2 * 8 * 108 * 4
+    # Rows of 37*4 = 148 elements: no multiple of 4 in 64..128 divides 148 -> two slices of 128.
+    sp7 = spec(1, 2, 1, 4, 8, [50], [37], [1], [1], [0], [0])
+    assert binding.wg_workspace_size(sp7, split_k=5, mode="deterministic") == 5 * 16 * 256 * 4
 
 
 def test_cluster_option_checks():

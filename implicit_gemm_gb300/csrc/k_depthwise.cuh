@@ -36,74 +36,104 @@ struct DwParams {
     WsLayout ws;  // split-K workspace layout (mode 3)
 };
 
-template <bool BF16, int GM>
-struct VecLoad;
 
+// The arithmetic works on the 16-bit inputs as loaded: a packed register holds
+// two channels, and the mixed-precision FMA (fp32 accumulator, bf16 or fp16
+// factors) multiplies them without converting first.  The product of two
+// 16-bit floats is exact in fp32, so the result equals fmaf on the converted
+// values bit for bit.
 template <bool BF16>
-__device__ __forceinline__ void cvt2(uint32_t u, float& a, float& b)
+__device__ __forceinline__ void fma2(float& a0, float& a1, uint32_t x, uint32_t y)
 {
-    if (BF16) {
-        a = __uint_as_float(u << 16);
-        b = __uint_as_float(u & 0xFFFF0000u);
-    } else {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u));
-        a = f.x;
-        b = f.y;
-    }
+    if constexpr (BF16)
+        asm("{\n\t.reg .b16 xl, xh, yl, yh;\n\tmov.b32 {xl, xh}, %2;\n\tmov.b32 {yl, yh}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, xl, yl, %0;\n\tfma.rn.f32.bf16 %1, xh, yh, %1;\n\t}"
+            : "+f"(a0), "+f"(a1)
+            : "r"(x), "r"(y));
+    else
+        asm("{\n\t.reg .b16 xl, xh, yl, yh;\n\tmov.b32 {xl, xh}, %2;\n\tmov.b32 {yl, yh}, %3;\n\t"
+            "fma.rn.f32.f16 %0, xl, yl, %0;\n\tfma.rn.f32.f16 %1, xh, yh, %1;\n\t}"
+            : "+f"(a0), "+f"(a1)
+            : "r"(x), "r"(y));
 }
 
-template <bool BF16, int GM>
-__device__ __forceinline__ void load_vec(const uint16_t* p, float (&v)[GM])
+template <bool BF16>
+__device__ __forceinline__ void fma1(float& a0, uint32_t x, uint32_t y)
+{
+    if constexpr (BF16)
+        asm("{\n\t.reg .b16 xl, xh, yl, yh;\n\tmov.b32 {xl, xh}, %1;\n\tmov.b32 {yl, yh}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, xl, yl, %0;\n\t}"
+            : "+f"(a0)
+            : "r"(x), "r"(y));
+    else
+        asm("{\n\t.reg .b16 xl, xh, yl, yh;\n\tmov.b32 {xl, xh}, %1;\n\tmov.b32 {yl, yh}, %2;\n\t"
+            "fma.rn.f32.f16 %0, xl, yl, %0;\n\t}"
+            : "+f"(a0)
+            : "r"(x), "r"(y));
+}
+
+// A vector of GM channels as packed pairs (GM = 1: the low half of one word).
+template <int GM>
+struct Packed {
+    static constexpr int N = GM >= 2 ? GM / 2 : 1;
+    uint32_t w[N];
+};
+
+template <int GM>
+__device__ __forceinline__ void load_vec(const uint16_t* p, Packed<GM>& v)
 {
     if constexpr (GM == 8) {
         const uint4 u = *reinterpret_cast<const uint4*>(p);
-        cvt2<BF16>(u.x, v[0], v[1]);
-        cvt2<BF16>(u.y, v[2], v[3]);
-        cvt2<BF16>(u.z, v[4], v[5]);
-        cvt2<BF16>(u.w, v[6], v[7]);
+        v.w[0] = u.x, v.w[1] = u.y, v.w[2] = u.z, v.w[3] = u.w;
     } else if constexpr (GM == 4) {
         const uint2 u = *reinterpret_cast<const uint2*>(p);
-        cvt2<BF16>(u.x, v[0], v[1]);
-        cvt2<BF16>(u.y, v[2], v[3]);
+        v.w[0] = u.x, v.w[1] = u.y;
     } else if constexpr (GM == 2) {
-        cvt2<BF16>(*reinterpret_cast<const uint32_t*>(p), v[0], v[1]);
+        v.w[0] = *reinterpret_cast<const uint32_t*>(p);
     } else {
-        const uint32_t u = *p;
-        float dummy;
-        cvt2<BF16>(u, v[0], dummy);
-        (void)dummy;
+        v.w[0] = *p;
+    }
+}
+
+// acc[t][j] += x[j] * dy[j] over the vector's channels.
+template <bool BF16, int GM>
+__device__ __forceinline__ void fma_vec(float (&acc)[GM], const Packed<GM>& x, const Packed<GM>& dy)
+{
+    if constexpr (GM == 1) {
+        fma1<BF16>(acc[0], x.w[0], dy.w[0]);
+    } else {
+#pragma unroll
+        for (int q = 0; q < GM / 2; ++q) fma2<BF16>(acc[2 * q], acc[2 * q + 1], x.w[q], dy.w[q]);
     }
 }
 
 // One window column: the X vectors of the three filter rows at one input column.
-template <bool BF16, int GM>
+template <int GM>
 __device__ __forceinline__ void load_col3(const uint16_t* r0, const uint16_t* r1, const uint16_t* r2, int off,
-                                          float (&w)[3][GM])
+                                          Packed<GM> (&w)[3])
 {
-    load_vec<BF16, GM>(r0 + off, w[0]);
-    load_vec<BF16, GM>(r1 + off, w[1]);
-    load_vec<BF16, GM>(r2 + off, w[2]);
+    load_vec<GM>(r0 + off, w[0]);
+    load_vec<GM>(r1 + off, w[1]);
+    load_vec<GM>(r2 + off, w[2]);
 }
 
 // acc[y*3 + x] += dY(pixel) * X(row y, column x of the window (c0, c1, c2)).
 template <bool BF16, int GM>
-__device__ __forceinline__ void fma_col3(const uint16_t* dyp, const float (&c0)[3][GM], const float (&c1)[3][GM],
-                                         const float (&c2)[3][GM], float (&acc)[9][GM])
+__device__ __forceinline__ void fma_col3(const uint16_t* dyp, const Packed<GM> (&c0)[3], const Packed<GM> (&c1)[3],
+                                         const Packed<GM> (&c2)[3], float (&acc)[9][GM])
 {
-    float dy[GM];
-    load_vec<BF16, GM>(dyp, dy);
+    Packed<GM> dy;
+    load_vec<GM>(dyp, dy);
 #pragma unroll
-    for (int y = 0; y < 3; ++y)
-#pragma unroll
-        for (int j = 0; j < GM; ++j) {
-            acc[y * 3 + 0][j] = fmaf(dy[j], c0[y][j], acc[y * 3 + 0][j]);
-            acc[y * 3 + 1][j] = fmaf(dy[j], c1[y][j], acc[y * 3 + 1][j]);
-            acc[y * 3 + 2][j] = fmaf(dy[j], c2[y][j], acc[y * 3 + 2][j]);
-        }
+    for (int y = 0; y < 3; ++y) {
+        fma_vec<BF16, GM>(acc[y * 3 + 0], c0[y], dy);
+        fma_vec<BF16, GM>(acc[y * 3 + 1], c1[y], dy);
+        fma_vec<BF16, GM>(acc[y * 3 + 2], c2[y], dy);
+    }
 }
 
-// Vectors of 8 channels hold 72 accumulators plus a 72-register window: one CTA
-// per SM.  Narrower vectors fit two CTAs per SM.
+// Vectors of 8 channels hold 72 accumulators plus a 36-register window of
+// packed pairs: one CTA per SM.  Narrower vectors fit two CTAs per SM.
 template <bool BF16, int GM, bool SLIDE3>
 __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
     depthwise_wgrad_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
@@ -189,23 +219,23 @@ __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
                     const uint16_t* xr1 = xr0 + dh * xw * CBv;
                     const uint16_t* xr2 = xr1 + dh * xw * CBv;
                     const uint16_t* yr = ys + (r * Wo) * CBv + cv;
-                    float wa[3][GM], wb[3][GM], wc[3][GM];
-                    load_col3<BF16, GM>(xr0, xr1, xr2, wo_a * CBv, wa);
-                    load_col3<BF16, GM>(xr0, xr1, xr2, (wo_a + 1) * CBv, wb);
+                    Packed<GM> wa[3], wb[3], wc[3];
+                    load_col3<GM>(xr0, xr1, xr2, wo_a * CBv, wa);
+                    load_col3<GM>(xr0, xr1, xr2, (wo_a + 1) * CBv, wb);
                     int wo = wo_a;
                     for (; wo + 3 <= wo_b; wo += 3) {
-                        load_col3<BF16, GM>(xr0, xr1, xr2, (wo + 2) * CBv, wc);
+                        load_col3<GM>(xr0, xr1, xr2, (wo + 2) * CBv, wc);
                         fma_col3<BF16, GM>(yr + wo * CBv, wa, wb, wc, acc);
-                        load_col3<BF16, GM>(xr0, xr1, xr2, (wo + 3) * CBv, wa);
+                        load_col3<GM>(xr0, xr1, xr2, (wo + 3) * CBv, wa);
                         fma_col3<BF16, GM>(yr + (wo + 1) * CBv, wb, wc, wa, acc);
-                        load_col3<BF16, GM>(xr0, xr1, xr2, (wo + 4) * CBv, wb);
+                        load_col3<GM>(xr0, xr1, xr2, (wo + 4) * CBv, wb);
                         fma_col3<BF16, GM>(yr + (wo + 2) * CBv, wc, wa, wb, acc);
                     }
                     if (wo < wo_b) {
-                        load_col3<BF16, GM>(xr0, xr1, xr2, (wo + 2) * CBv, wc);
+                        load_col3<GM>(xr0, xr1, xr2, (wo + 2) * CBv, wc);
                         fma_col3<BF16, GM>(yr + wo * CBv, wa, wb, wc, acc);
                         if (wo + 1 < wo_b) {
-                            load_col3<BF16, GM>(xr0, xr1, xr2, (wo + 3) * CBv, wa);
+                            load_col3<GM>(xr0, xr1, xr2, (wo + 3) * CBv, wa);
                             fma_col3<BF16, GM>(yr + (wo + 1) * CBv, wb, wc, wa, acc);
                         }
                     }
@@ -218,16 +248,15 @@ __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
                         tap_off[t] = (ty * p.dh * p.xw + tx * p.dw) * p.CB;
                     }
                     for (int wo = wo_a; wo < wo_b; ++wo) {
-                        float dy[GM];
-                        load_vec<BF16, GM>(ys + (r * p.Wo + wo) * p.CB + cv, dy);
+                        Packed<GM> dy;
+                        load_vec<GM>(ys + (r * p.Wo + wo) * p.CB + cv, dy);
                         const uint16_t* xb = xs + ((r * p.sh) * p.xw + wo * p.sw) * p.CB + cv;
 #pragma unroll
                         for (int t = 0; t < MAXT; ++t) {
                             if (t < p.T) {
-                                float xv[GM];
-                                load_vec<BF16, GM>(xb + tap_off[t], xv);
-#pragma unroll
-                                for (int j = 0; j < GM; ++j) acc[t][j] = fmaf(dy[j], xv[j], acc[t][j]);
+                                Packed<GM> xv;
+                                load_vec<GM>(xb + tap_off[t], xv);
+                                fma_vec<BF16, GM>(acc[t], xv, dy);
                             }
                         }
                     }

@@ -33,7 +33,7 @@ class WgProblem(ctypes.Structure):
 
 class WgOptions(ctypes.Structure):
     _fields_ = [("split_k", ctypes.c_int), ("mode", ctypes.c_int), ("group_merge", ctypes.c_int),
-                ("cluster", ctypes.c_int)]
+                ("cluster", ctypes.c_int), ("kernel", ctypes.c_int)]
 
 
 class WgradError(RuntimeError):
@@ -104,8 +104,12 @@ def make_problem(spec: dict) -> WgProblem:
     return p
 
 
-def make_options(split_k: int = 0, mode: str = "auto", group_merge: int = 0, cluster: int = 0) -> WgOptions:
-    return WgOptions(int(split_k), MODES[mode], int(group_merge), int(cluster))
+KERNELS = {"auto": 0, "igemm": 1, "depthwise": 2}
+
+
+def make_options(split_k: int = 0, mode: str = "auto", group_merge: int = 0, cluster: int = 0,
+                 kernel: str = "auto") -> WgOptions:
+    return WgOptions(int(split_k), MODES[mode], int(group_merge), int(cluster), KERNELS[kernel])
 
 
 def _addr(t) -> int:
@@ -124,25 +128,25 @@ def wg_problem_normalize(spec: dict) -> list:
 
 
 def wg_workspace_size(spec: dict, split_k: int = 0, mode: str = "auto", group_merge: int = 0, *,
-                      cluster: int = 0) -> int:
-    p, o, n = make_problem(spec), make_options(split_k, mode, group_merge, cluster), ctypes.c_size_t(0)
+                      cluster: int = 0, kernel: str = "auto") -> int:
+    p, o, n = make_problem(spec), make_options(split_k, mode, group_merge, cluster, kernel), ctypes.c_size_t(0)
     _check(load().wg_workspace_size(ctypes.byref(p), ctypes.byref(o), ctypes.byref(n)))
     return int(n.value)
 
 
 def wg_plan_string(spec: dict, split_k: int = 0, mode: str = "auto", group_merge: int = 0, *,
-                   cluster: int = 0) -> str:
-    p, o = make_problem(spec), make_options(split_k, mode, group_merge, cluster)
+                   cluster: int = 0, kernel: str = "auto") -> str:
+    p, o = make_problem(spec), make_options(split_k, mode, group_merge, cluster, kernel)
     buf = ctypes.create_string_buffer(2048)
     _check(load().wg_plan_string(ctypes.byref(p), ctypes.byref(o), buf, len(buf)))
     return buf.value.decode()
 
 
 def wg_conv_bwd_weight(spec: dict, x, dy, dw, split_k: int = 0, mode: str = "auto", group_merge: int = 0,
-                       workspace=None, ws_bytes: int | None = None, stream=None, *, cluster: int = 0) -> None:
+                       workspace=None, ws_bytes: int | None = None, stream=None, *, cluster: int = 0, kernel: str = "auto") -> None:
     """Launch the weight gradient on `stream` (torch stream, raw handle int, or None for
     torch's current stream when torch is loaded, else the legacy default stream)."""
-    p, o = make_problem(spec), make_options(split_k, mode, group_merge, cluster)
+    p, o = make_problem(spec), make_options(split_k, mode, group_merge, cluster, kernel)
     if ws_bytes is None:
         ws_bytes = 0 if workspace is None else (workspace.numel() * workspace.element_size()
                                                 if hasattr(workspace, "numel") else 0)
@@ -155,9 +159,9 @@ class PreparedCall:
     ctypes call.  Keeps references to the tensors it was built from."""
 
     def __init__(self, spec: dict, x, dy, dw, split_k: int = 0, mode: str = "auto", group_merge: int = 0,
-                 workspace=None, ws_bytes: int | None = None, *, cluster: int = 0):
+                 workspace=None, ws_bytes: int | None = None, *, cluster: int = 0, kernel: str = "auto"):
         self._keep = (x, dy, dw, workspace)
-        self.p, self.o = make_problem(spec), make_options(split_k, mode, group_merge, cluster)
+        self.p, self.o = make_problem(spec), make_options(split_k, mode, group_merge, cluster, kernel)
         if ws_bytes is None:
             ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
         self.fn = load().wg_conv_bwd_weight
@@ -172,10 +176,10 @@ class PreparedCall:
 
 
 def wg_conv_bwd_weight_noalloc(spec: dict, x, dy, dw, split_k: int = 0, mode: str = "auto", group_merge: int = 0,
-                               stream=None, *, cluster: int = 0) -> None:
+                               stream=None, *, cluster: int = 0, kernel: str = "auto") -> None:
     """wg_conv_bwd_weight for callers that cannot allocate: the split-K workspace comes
     from the library's own 16 MiB device array (see include/wgrad.h)."""
-    p, o = make_problem(spec), make_options(split_k, mode, group_merge, cluster)
+    p, o = make_problem(spec), make_options(split_k, mode, group_merge, cluster, kernel)
     _check(load().wg_conv_bwd_weight_noalloc(ctypes.byref(p), _addr(x), _addr(dy), _addr(dw), ctypes.byref(o),
                                              _stream_handle(stream)))
 
@@ -215,7 +219,7 @@ def _stream_handle(stream):
 
 
 def conv_bwd_weight(spec: dict, x, dy, split_k: int = 0, mode: str = "auto", group_merge: int = 0, out=None,
-                    stream=None, *, cluster: int = 0):
+                    stream=None, *, cluster: int = 0, kernel: str = "auto"):
     """Convenience wrapper over wg_conv_bwd_weight for torch CUDA tensors: allocates dW
     (G, K, *filt, C) in spec['out_dtype'] and the workspace it needs with torch, then calls
     the library."""
@@ -223,7 +227,8 @@ def conv_bwd_weight(spec: dict, x, dy, split_k: int = 0, mode: str = "auto", gro
     tdt = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}[spec.get("out_dtype", "fp32")]
     if out is None:
         out = torch.empty((spec["G"], spec["K"], *spec["filt"], spec["C"]), dtype=tdt, device=x.device)
-    nbytes = wg_workspace_size(spec, split_k, mode, group_merge, cluster=cluster)
+    nbytes = wg_workspace_size(spec, split_k, mode, group_merge, cluster=cluster, kernel=kernel)
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=x.device) if nbytes else None
-    wg_conv_bwd_weight(spec, x, dy, out, split_k, mode, group_merge, ws, nbytes, stream, cluster=cluster)
+    wg_conv_bwd_weight(spec, x, dy, out, split_k, mode, group_merge, ws, nbytes, stream, cluster=cluster,
+                       kernel=kernel)
     return out

@@ -131,9 +131,17 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
             return fail(err, WG_ERR_NOT_SUPPORTED, "stride above 8 (TMA element strides are at most 8)");
     // Channel / k windows.  A group whose first channel is not 8-aligned can
     // start up to 7 channels into the window (TMA coordinates must be 16-byte aligned).
-    const int cmis = (pb.C % 8) ? 7 : 0, kmis = (pb.K % 8) ? 7 : 0;
-    int Gm = 1;
-    if (pb.C + cmis <= 64 && pb.K + kmis <= 256)
+    // The widest fold whose windows start 8-aligned (Gm*C and Gm*K multiples of
+    // 8) is preferred; failing that, any width, with windows that may start up
+    // to 7 channels early.
+    int Gm = 1, cmis = (pb.C % 8) ? 7 : 0, kmis = (pb.K % 8) ? 7 : 0;
+    for (int g = std::min(pb.G, 64); g >= 2; --g)
+        if (g * pb.C <= 64 && g * pb.K <= 256 && (g * pb.C) % 8 == 0 && (g * pb.K) % 8 == 0) {
+            Gm = g;
+            cmis = kmis = 0;
+            break;
+        }
+    if (Gm == 1 && pb.C + cmis <= 64 && pb.K + kmis <= 256)
         while (Gm < pb.G && (Gm + 1) * pb.C + cmis <= 64 && (Gm + 1) * pb.K + kmis <= 256) ++Gm;
     ig.Gm = Gm;
     ig.n_gblocks = (int)cdiv(pb.G, Gm);
@@ -468,7 +476,7 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
     int st = normalize(p, &pl->pb, err);
     if (st) return st;
     const Problem& pb = pl->pb;
-    wg_options o{0, WG_MODE_AUTO, 0, 0};
+    wg_options o{0, WG_MODE_AUTO, 0, 0, WG_KERNEL_AUTO};
     if (opt) o = *opt;
     DeviceCaps caps = caps_in;
     if (caps.num_sms <= 0) caps = default_caps(0);
@@ -481,6 +489,8 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
         return fail(err, WG_ERR_INVALID_ARGUMENT, "group_merge must be 0, 1, 2, 4 or 8");
     if (o.cluster != 0 && o.cluster != 1 && o.cluster != 2 && o.cluster != 4 && o.cluster != 8)
         return fail(err, WG_ERR_INVALID_ARGUMENT, "cluster must be 0, 1, 2, 4 or 8");
+    if (o.kernel < WG_KERNEL_AUTO || o.kernel > WG_KERNEL_DEPTHWISE)
+        return fail(err, WG_ERR_INVALID_ARGUMENT, "bad kernel selector");
     if (o.mode == WG_MODE_DIRECT && o.split_k > 1 && o.split_k != o.cluster)
         return fail(err, WG_ERR_INVALID_ARGUMENT,
                     "mode DIRECT takes no split, or exactly one cluster of splits (split_k %d, cluster %d)", o.split_k,
@@ -492,7 +502,11 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
     const bool depthwise = pb.C == 1 && pb.K == 1;
     if (o.group_merge > 1 && !depthwise)
         return fail(err, WG_ERR_NOT_SUPPORTED, "group_merge > 1 is for depthwise problems (C = K = 1) only");
-    if (depthwise && dw_eligible(pb)) {
+    const bool use_dw = depthwise && dw_eligible(pb) && o.kernel != WG_KERNEL_IGEMM;
+    if (o.kernel == WG_KERNEL_DEPTHWISE && !use_dw)
+        return fail(err, WG_ERR_NOT_SUPPORTED,
+                    "the depthwise kernel needs C = K = 1, 1-D or 2-D, <= 9 taps and G %% 8 == 0");
+    if (use_dw) {
         pl->kind = KIND_DEPTHWISE;
         st = plan_depthwise(pl, o, num_sms, err);
     } else {

@@ -140,7 +140,7 @@ int plan_for(const wg_problem* p, const wg_options* opt, wg::Plan* pl, std::stri
     const wg::DeviceCaps caps = device_caps();
     std::string key;
     if (p) {
-        wg_options o{0, WG_MODE_AUTO, 0, 0};
+        wg_options o{0, WG_MODE_AUTO, 0, 0, WG_KERNEL_AUTO};
         if (opt) o = *opt;
         key.assign(reinterpret_cast<const char*>(p), sizeof *p);
         key.append(reinterpret_cast<const char*>(&o), sizeof o);
@@ -631,7 +631,7 @@ int wg_conv_bwd_weight_noalloc(const wg_problem* p, const void* x, const void* d
     void* scratch = nullptr;
     int st = noalloc_scratch(&scratch);
     if (st) return st;
-    wg_options o{0, WG_MODE_AUTO, 0, 0};
+    wg_options o{0, WG_MODE_AUTO, 0, 0, WG_KERNEL_AUTO};
     if (opt) o = *opt;
     size_t need = 0;
     st = wg_workspace_size(p, &o, &need);

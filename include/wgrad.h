@@ -93,6 +93,17 @@ typedef struct {
     wg_dtype out_dtype;    /* dW: WG_FP32, WG_BF16 or WG_FP16 */
 } wg_problem;
 
+/* Which kernel computes the contraction.
+ *  AUTO:       the depthwise kernel where it applies (C = K = 1, 1-D or 2-D,
+ *              at most 9 taps, G a multiple of 8), else the tensor-core kernel.
+ *  IGEMM:      the tensor-core implicit GEMM for every problem.  For small C
+ *              and K it folds several groups into one tile and keeps only the
+ *              diagonal blocks (the merged-tile design of the CK page's group
+ *              merging), so depthwise problems run on it too.
+ *  DEPTHWISE:  the CUDA-core depthwise kernel; WG_ERR_NOT_SUPPORTED where it
+ *              does not apply. */
+typedef enum { WG_KERNEL_AUTO = 0, WG_KERNEL_IGEMM = 1, WG_KERNEL_DEPTHWISE = 2 } wg_kernel;
+
 /* Per-call options (the CK page's k_batch, plus the two ways of combining splits).
  *  split_k:     0 = choose automatically, 1 = no split, S > 1 = S splits of GemmK.
  *  mode:        see wg_mode.
@@ -108,12 +119,14 @@ typedef struct {
  *               slower than the two-stage path on every workload measured).
  *               Must divide split_k; must be 0 or 1 for the depthwise kernel.
  *               With S == cluster the sums are final: mode DIRECT then accepts
- *               the split, and no workspace is needed. */
+ *               the split, and no workspace is needed.
+ *  kernel:      see wg_kernel. */
 typedef struct {
     int split_k;
     wg_mode mode;
     int group_merge;
     int cluster;
+    wg_kernel kernel;
 } wg_options;
 
 /* Validate `p` and fill p->out[] with the derived output lengths

@@ -158,3 +158,23 @@ def test_mark_event_can_be_cleared_without_device(lib):
     # Setting and clearing the measurement hook touches no device state.
     binding.wg_set_mark_event(None)
     assert lib.wg_set_mark_event(None) == 0
+
+
+def test_kernel_selector():
+    dw = WORKLOADS["2d_depthwise_g512_n64_h28"][0]
+    assert "kernel=depthwise" in binding.wg_plan_string(dw)
+    ps = binding.wg_plan_string(dw, kernel="igemm")
+    # Block-diagonal tensor-core plan: 64 groups per tile, windows 8-aligned.
+    assert "kernel=igemm_tcgen05" in ps and " Gm=64 " in ps and "gblocks=8 " in ps
+    dense = WORKLOADS["2d_dense_n32_h56_c64_k64"][0]
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_plan_string(dense, kernel="depthwise")
+    assert e.value.status == 2
+    with pytest.raises(binding.WgradError) as e:
+        lib_opts = binding.make_options()
+        lib_opts.kernel = 3
+        p = binding.make_problem(dense)
+        import ctypes
+        buf = ctypes.create_string_buffer(256)
+        binding._check(binding.load().wg_plan_string(ctypes.byref(p), ctypes.byref(lib_opts), buf, len(buf)))
+    assert e.value.status == 1

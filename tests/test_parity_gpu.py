@@ -36,12 +36,12 @@ def to_dev(bits, dtype):
 _TDT = {"fp32": "float32", "bf16": "bfloat16", "fp16": "float16"}
 
 
-def run_gpu(sp, x, dy, split_k=0, mode="auto", gm=0, xd=None, dyd=None, cluster=0):
+def run_gpu(sp, x, dy, split_k=0, mode="auto", gm=0, xd=None, dyd=None, cluster=0, kernel="auto"):
     xd = to_dev(x, sp["in_dtype"]) if xd is None else xd
     dyd = to_dev(dy, sp["in_dtype"]) if dyd is None else dyd
     out = torch.full((sp["G"], sp["K"], *sp["filt"], sp["C"]), float("nan"),
                      dtype=getattr(torch, _TDT[sp["out_dtype"]]), device="cuda")
-    binding.conv_bwd_weight(sp, xd, dyd, split_k, mode, gm, out=out, cluster=cluster)
+    binding.conv_bwd_weight(sp, xd, dyd, split_k, mode, gm, out=out, cluster=cluster, kernel=kernel)
     binding.wg_check_status()
     return out.float().cpu().numpy().astype(np.float64)
 
@@ -199,3 +199,28 @@ def test_more_splits_than_tiles():
 
 def test_status_clear_after_runs():
     binding.wg_check_status()
+
+
+# The depthwise problems again on the tensor-core kernel (block-diagonal tiles).
+DW_SMALL = [sp for sp in SMALL if sp["C"] == 1 and sp["K"] == 1]
+
+
+@pytest.mark.parametrize("sp", DW_SMALL, ids=_ids)
+def test_depthwise_on_tensor_cores(sp):
+    x, dy = make_inputs(sp, ("uniform", -1.0, 1.0), 47, 48)
+    dw, A = ref(sp, x, dy)
+    for split_k, mode in ((0, "auto"), (1, "direct"), (5, "deterministic"), (3, "atomic")):
+        if mode == "atomic" and sp["out_dtype"] != "fp32":
+            continue
+        got = run_gpu(sp, x, dy, split_k, mode, kernel="igemm")
+        assert_close(got, dw, A, sp["out_dtype"], f"{_ids(sp)} igemm S={split_k} {mode}")
+    xi, dyi = make_inputs(sp, ("int", -2, 2), 57, 58)
+    dwi, _ = ref(sp, xi, dyi)
+    np.testing.assert_array_equal(run_gpu(sp, xi, dyi, 4, "deterministic", kernel="igemm"), dwi)
+
+
+@pytest.mark.parametrize("split_k,mode", [(0, "auto"), (0, "atomic")])
+def test_depthwise_workload_on_tensor_cores(split_k, mode):
+    sp, x, dy, (dw, A) = workload("2d_depthwise_g512_n64_h28")
+    got = run_gpu(sp, x, dy, split_k, mode, kernel="igemm")
+    assert_close(got, dw, A, sp["out_dtype"], f"depthwise igemm S={split_k} {mode}")

@@ -6,17 +6,18 @@
 A step is one call of wg_conv_bwd_weight -- the whole path: every launch it makes
 (split-K stage 1, the stage-2 reduce or the atomic-mode memset) -- over one batch
 of synthetic, seeded inputs already resident in HBM.  The device-side value
-times each call between CUDA events on its stream; the L2 flush in front of
-every step keeps the GPU busy long enough for the host to enqueue the call, so
-host-side time is not inside the events (--graph replays a captured CUDA graph
-of the call instead).  The e2e value times the same call with host buffers.  The headline workload is
-the 2-D dense 56x56, C = K = 64, N = 32, 3x3 problem with bf16 inputs and bf16
-dW; the other workloads are reported under "workloads".  No step finds its
-inputs in L2: each step reads the next of several copies of X and dY whose
+times each call between CUDA events on its stream (--graph replays a captured
+CUDA graph of the call instead).  The e2e value times the same call with host
+buffers.  The headline workload is the 2-D dense 56x56, C = K = 64, N = 32, 3x3
+problem with bf16 inputs and bf16 dW; the other workloads, and the other plans
+the measurement table lists for each (split degrees, modes, merge widths, the
+tensor-core depthwise variant), are reported under "workloads".  No step finds
+its inputs in L2: each step reads the next of several copies of X and dY whose
 total exceeds twice the L2; inputs too small for that (the 8x8 problem) are
 evicted instead by an L2 flush before every step (a 256 MiB write, then a
 256 MiB read of another buffer so the write's dirty lines are written back
-before the timed events).
+before the timed events).  The roofline's kernel time comes from a second pass
+over the same steps with an event recorded right after the main kernel.
 
 Prints one JSON line on rank 0.  Multi-GPU runs (torchrun) are independent
 replicas (weak scaling): the path has no exchange step on one node.
@@ -61,6 +62,24 @@ WORKLOADS = {
                                    [1, 1, 1], "fp16", "fp32"), ("normal", 0.0, 0.5), 5, 8, "atomic", 0),
 }
 HEADLINE = "2d_dense_n32_h56_c64_k64"
+
+# Plans reported under "workloads": (label, workload, split_k, mode, group_merge, kernel).
+VARIANTS = [
+    ("2d_tiny_n1_h8_c16_k32", "2d_tiny_n1_h8_c16_k32", 0, "auto", 0, "auto"),
+    ("2d_dense_n32_h56_c64_k64/S1_direct", "2d_dense_n32_h56_c64_k64", 1, "direct", 0, "auto"),
+    ("2d_dense_n32_h56_c64_k64/S4_deterministic", "2d_dense_n32_h56_c64_k64", 4, "deterministic", 0, "auto"),
+    ("2d_grouped_g32_c8_k8_n32_h28", "2d_grouped_g32_c8_k8_n32_h28", 0, "auto", 0, "auto"),
+    ("2d_grouped_g32_c8_k8_n32_h28/atomic", "2d_grouped_g32_c8_k8_n32_h28", 0, "atomic", 0, "auto"),
+    ("2d_depthwise_g512_n64_h28", "2d_depthwise_g512_n64_h28", 0, "auto", 8, "auto"),
+    ("2d_depthwise_g512_n64_h28/gm1", "2d_depthwise_g512_n64_h28", 0, "auto", 1, "auto"),
+    ("2d_depthwise_g512_n64_h28/gm2", "2d_depthwise_g512_n64_h28", 0, "auto", 2, "auto"),
+    ("2d_depthwise_g512_n64_h28/gm4", "2d_depthwise_g512_n64_h28", 0, "auto", 4, "auto"),
+    ("2d_depthwise_g512_n64_h28/gm4_atomic", "2d_depthwise_g512_n64_h28", 0, "atomic", 4, "auto"),
+    ("2d_depthwise_g512_n64_h28/tensor_core", "2d_depthwise_g512_n64_h28", 0, "auto", 0, "igemm"),
+    ("3d_n4_d16_c128_k96_s2", "3d_n4_d16_c128_k96_s2", 8, "atomic", 0, "auto"),
+    ("3d_n4_d16_c128_k96_s2/S8_deterministic", "3d_n4_d16_c128_k96_s2", 8, "deterministic", 0, "auto"),
+    ("3d_n4_d16_c128_k96_s2/auto", "3d_n4_d16_c128_k96_s2", 0, "auto", 0, "auto"),
+]
 
 
 def out_dims(sp):
@@ -181,14 +200,15 @@ def run_reference(args, ws, rank):
 
 
 def cpu_baseline(name):
-    """The oracle timed on this host's cores on the full workload (about a second per run)."""
+    """The oracle timed on this host's cores on the full workload: whole runs until about
+    10 s of CPU work have been timed."""
     import oracle
     sp, dist, seed = WORKLOADS[name][0], WORKLOADS[name][1], WORKLOADS[name][2]
     s = sizes(sp)
     x = oracle.decode(synth.tensor_bits(1000 + seed, s["nx"], sp["in_dtype"], *dist), sp["in_dtype"])
     dy = oracle.decode(synth.tensor_bits(2000 + seed, s["ndy"], sp["in_dtype"], *dist), sp["in_dtype"])
     runs, t0 = 0, time.perf_counter()
-    while runs < 1 or time.perf_counter() - t0 < 1.5:
+    while runs < 1 or time.perf_counter() - t0 < 10.0:
         oracle.wgrad(sp, x, dy)
         runs += 1
     dt = (time.perf_counter() - t0) / runs
@@ -200,7 +220,12 @@ L2_BYTES = 129 * 1000 * 1000
 # DRAM bytes (read + write) of one launch of the workload's main kernel from an
 # ncu capture of the kernel as it now stands (summaries under profiles/); a
 # workload without such a capture reports null.
-TRAFFIC = {}
+TRAFFIC = {
+    # igemm_wgrad_kernel: 25,785,344 B read + 135,424 B written (one launch, full size).
+    "2d_dense_n32_h56_c64_k64": 25_920_768,
+    # depthwise_wgrad_kernel<bf16, 8, sliding>: 103,158,784 B read + 3,442,176 B written.
+    "2d_depthwise_g512_n64_h28": 106_600_960,
+}
 MAX_COPIES = 512
 
 
@@ -212,10 +237,13 @@ class Workload:
     was last read more than 129 MB of other input ago).  Inputs too small for
     that within MAX_COPIES fall back to flushing L2 before every step."""
 
-    def __init__(self, torch, name, rotate=True):
+    def __init__(self, torch, name, rotate=True, plan=None):
         self.torch = torch
         self.name = name
         sp, dist, seed, self.split_k, self.mode, self.gm = WORKLOADS[name]
+        self.kernel = "auto"
+        if plan is not None:
+            self.split_k, self.mode, self.gm, self.kernel = plan
         self.sp = sp
         self.s = sizes(sp)
         tdt = torch.bfloat16 if sp["in_dtype"] == "bf16" else torch.float16
@@ -228,12 +256,15 @@ class Workload:
         odt = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}[sp["out_dtype"]]
         self.dw = torch.empty(self.s["ndw"], dtype=odt, device="cuda")
         self.dw_host = torch.empty(self.s["ndw"], dtype=odt).pin_memory()
-        self.ws_bytes = binding.wg_workspace_size(sp, self.split_k, self.mode, self.gm)
+        kw = {"kernel": self.kernel}
+        self.ws_bytes = binding.wg_workspace_size(sp, self.split_k, self.mode, self.gm, **kw)
         self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device="cuda")
-        self.plan = binding.wg_plan_string(sp, self.split_k, self.mode, self.gm)
+        self.plan = binding.wg_plan_string(sp, self.split_k, self.mode, self.gm, **kw)
+        # This library's kernels per call: the main kernel, plus the split reduction
+        # in deterministic mode (the atomic mode's memset is a runtime call).
         self.launches_per_step = 1 + (1 if "mode=deterministic" in self.plan else 0)
         self.call = binding.PreparedCall(sp, self.x, self.dy, self.dw, self.split_k, self.mode, self.gm, self.ws,
-                                         self.ws_bytes)
+                                         self.ws_bytes, **kw)
         self.graph = None
         in_bytes = 2 * (self.s["nx"] + self.s["ndy"])
         need = -(-2 * L2_BYTES // in_bytes)
@@ -244,7 +275,7 @@ class Workload:
             xc, dyc = self.x.clone(), self.dy.clone()
             self.inputs.append((xc, dyc))
             self.calls.append(binding.PreparedCall(sp, xc, dyc, self.dw, self.split_k, self.mode, self.gm, self.ws,
-                                                   self.ws_bytes))
+                                                   self.ws_bytes, **kw))
         self.next = 0
         self.rotating = self.copies > 1
 
@@ -421,10 +452,10 @@ def main():
 
     extra = {}
     if rank == 0 and not args.no_extra:
-        for name in WORKLOADS:
-            if name == args.workload:
+        for label, name, *plan in VARIANTS:
+            if name == args.workload and label == name:
                 continue
-            w2 = Workload(torch, name)
+            w2 = Workload(torch, name, plan=tuple(plan))
             if args.graph:
                 w2.capture(stream)
             tt = time_steps(torch, w2, 300, 10, flush, stream)
@@ -432,7 +463,7 @@ def main():
             kms = ms if args.graph else float(np.mean(time_steps(torch, w2, 300, 10, flush, stream, mark=True)))
             s2 = w2.s
             tf, tb = s2["flops"] / (pk["bf16"] * 1e12), s2["bytes"] / (pk["hbm"] * 1e9)
-            extra[name] = {"ms_per_step": ms, "tflops": s2["flops"] / (ms * 1e-3) / 1e12,
+            extra[label] = {"ms_per_step": ms, "tflops": s2["flops"] / (ms * 1e-3) / 1e12,
                            "gbs": s2["bytes"] / (ms * 1e-3) / 1e9, "roofline_us": max(tf, tb) * 1e6,
                            "bound": "hbm" if tb >= tf else "tensor",
                            "roofline_frac": max(tf, tb) / (ms * 1e-3), "kernel_ms": kms,

@@ -61,6 +61,10 @@ WORKLOADS = {
     "3d_n4_d16_c128_k96_s2": (spec(3, 1, 4, 128, 96, [16, 16, 16], [3, 3, 3], [2, 2, 2], [1, 1, 1], [1, 1, 1],
                                    [1, 1, 1], "fp16", "fp32"), ("normal", 0.0, 0.5), 5, 8, "atomic", 0),
 }
+WORKLOADS["2d_1x1_n32_h56_c64_k256"] = (spec(2, 1, 32, 64, 256, [56, 56], [1, 1], [1, 1], [1, 1], [0, 0], [0, 0],
+                                             "bf16", "fp32"), ("uniform", -1.0, 1.0), 6, 0, "auto", 0)
+WORKLOADS["2d_1x1s2_n32_h56_c256_k128"] = (spec(2, 1, 32, 256, 128, [56, 56], [1, 1], [2, 2], [1, 1], [0, 0], [0, 0],
+                                                "bf16", "fp32"), ("uniform", -1.0, 1.0), 7, 0, "auto", 0)
 HEADLINE = "2d_dense_n32_h56_c64_k64"
 
 # Plans reported under "workloads": (label, workload, split_k, mode, group_merge, kernel).
@@ -79,6 +83,8 @@ VARIANTS = [
     ("3d_n4_d16_c128_k96_s2", "3d_n4_d16_c128_k96_s2", 8, "atomic", 0, "auto"),
     ("3d_n4_d16_c128_k96_s2/S8_deterministic", "3d_n4_d16_c128_k96_s2", 8, "deterministic", 0, "auto"),
     ("3d_n4_d16_c128_k96_s2/auto", "3d_n4_d16_c128_k96_s2", 0, "auto", 0, "auto"),
+    ("2d_1x1_n32_h56_c64_k256", "2d_1x1_n32_h56_c64_k256", 0, "auto", 0, "auto"),
+    ("2d_1x1s2_n32_h56_c256_k128", "2d_1x1s2_n32_h56_c256_k128", 0, "auto", 0, "auto"),
 ]
 
 
@@ -361,6 +367,55 @@ def time_steps(torch, wl, steps, warmup, flush, stream, e2e=False, mark=False):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+# Depthwise shapes for --sweep, in the style of the inverted-residual networks'
+# depthwise layers (synthetic: the pages' 197-shape corpus is not available):
+# (G, N, H = W, filter, stride).  5x5 filters exceed the CUDA-core kernel's 9
+# taps and run on the tensor-core kernel.
+SWEEP_SHAPES = [
+    (32, 32, 112, 3, 1), (96, 32, 112, 3, 2), (144, 32, 56, 3, 1), (144, 32, 56, 3, 2), (192, 32, 28, 3, 1),
+    (192, 32, 28, 3, 2), (384, 32, 14, 3, 1), (576, 32, 14, 3, 1), (576, 32, 14, 3, 2), (960, 32, 7, 3, 1),
+    (512, 64, 28, 3, 1), (64, 16, 64, 3, 1), (240, 32, 28, 5, 1), (480, 32, 14, 5, 1), (672, 32, 14, 5, 2),
+    (1152, 32, 7, 5, 1),
+]
+
+
+def run_sweep(torch, stream, flush, steps, warmup):
+    """Automatic plan against the fixed merge widths and split choices on each shape."""
+    rows = []
+    for i, (G, N, H, F, st) in enumerate(SWEEP_SHAPES):
+        name = f"sweep_dw_g{G}_n{N}_h{H}_f{F}_s{st}"
+        sp = spec(2, G, N, 1, 1, [H, H], [F, F], [st, st], [1, 1], [F // 2, F // 2], [F // 2, F // 2], "bf16", "fp32")
+        WORKLOADS[name] = (sp, ("uniform", -1.0, 1.0), 100 + i, 0, "auto", 0)
+        dw = F * F <= 9
+        plans = [("auto", (0, "auto", 0, "auto"))]
+        if dw:
+            plans += [(f"gm{g}", (0, "auto", g, "depthwise")) for g in (1, 2, 4, 8)]
+            plans += [(f"gm{g}_atomic", (0, "atomic", g, "depthwise")) for g in (2, 4, 8)]
+        plans += [("tensor_core", (0, "auto", 0, "igemm")), ("tensor_core_atomic", (0, "atomic", 0, "igemm"))]
+        res = {}
+        for label, plan in plans:
+            try:
+                wl = Workload(torch, name, plan=plan)
+            except binding.WgradError:
+                continue
+            res[label] = float(np.mean(time_steps(torch, wl, steps, warmup, flush, stream))) * 1e3
+            del wl
+        best = min(res, key=res.get)
+        row = {"shape": name, "auto_us": res["auto"], "best": best, "best_us": res[best],
+               "auto_vs_best": res[best] / res["auto"]}
+        if "gm1" in res:
+            row["gm1_us"] = res["gm1"]
+            row["auto_speedup_vs_gm1"] = res["gm1"] / res["auto"]
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+    gm = [r["auto_speedup_vs_gm1"] for r in rows if "auto_speedup_vs_gm1" in r]
+    ab = [r["auto_vs_best"] for r in rows]
+    geo = lambda v: float(np.exp(np.mean(np.log(v))))
+    print(json.dumps({"sweep": "depthwise policy", "shapes": len(rows),
+                      "geomean_auto_speedup_vs_gm1": geo(gm), "geomean_auto_vs_best": geo(ab),
+                      "min_auto_vs_best": min(ab)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -370,6 +425,8 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=list(WORKLOADS))
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads and the CPU baseline")
     ap.add_argument("--graph", action="store_true", help="replay a CUDA graph of the call instead of calling it")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the automatic plan against fixed merge widths on a depthwise shape sweep")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -392,6 +449,10 @@ def main():
     stream = torch.cuda.Stream()
     flush = L2Flush(torch)
     pk = peaks()
+    if args.sweep:
+        if rank == 0:
+            run_sweep(torch, stream, flush, min(args.steps, 200), args.warmup)
+        return
 
     wl = Workload(torch, args.workload)
     if args.graph:

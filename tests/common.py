@@ -34,6 +34,11 @@ WORKLOADS = {
                                        "fp32"), ("uniform", -1.0, 1.0), 4),
     "3d_n4_d16_c128_k96_s2": (spec(3, 1, 4, 128, 96, [16, 16, 16], [3, 3, 3], [2, 2, 2], [1, 1, 1], [1, 1, 1],
                                    [1, 1, 1], "fp16", "fp32"), ("normal", 0.0, 0.5), 5),
+    # 1x1 filters: stride 1 pad 0 (a plain batched GEMM) and stride 2 pad 0 (a strided GEMM).
+    "2d_1x1_n32_h56_c64_k256": (spec(2, 1, 32, 64, 256, [56, 56], [1, 1], [1, 1], [1, 1], [0, 0], [0, 0], "bf16",
+                                     "fp32"), ("uniform", -1.0, 1.0), 6),
+    "2d_1x1s2_n32_h56_c256_k128": (spec(2, 1, 32, 256, 128, [56, 56], [1, 1], [2, 2], [1, 1], [0, 0], [0, 0],
+                                        "bf16", "fp32"), ("uniform", -1.0, 1.0), 7),
 }
 
 

@@ -87,6 +87,10 @@ WORKLOAD_MODES = [
     ("3d_n4_d16_c128_k96_s2", 8, "deterministic", 0, 1),
     ("3d_n4_d16_c128_k96_s2", 16, "deterministic", 0, 2),
     ("3d_n4_d16_c128_k96_s2", 0, "auto", 0, 0),
+    ("2d_1x1_n32_h56_c64_k256", 0, "auto", 0, 0),
+    ("2d_1x1_n32_h56_c64_k256", 0, "atomic", 0, 0),
+    ("2d_1x1s2_n32_h56_c256_k128", 0, "auto", 0, 0),
+    ("2d_1x1s2_n32_h56_c256_k128", 1, "direct", 0, 0),
 ]
 
 
@@ -128,6 +132,10 @@ SMALL = [
     spec(3, 1, 2, 32, 16, [5, 6, 7], [3, 3, 3], [1, 1, 1], [1, 1, 1], [1, 1, 1], [1, 1, 1]),
     spec(3, 2, 1, 8, 8, [7, 6, 9], [2, 3, 3], [2, 1, 2], [1, 2, 1], [0, 1, 1], [1, 1, 0]),
     spec(3, 1, 3, 128, 96, [9, 9, 9], [3, 3, 3], [2, 2, 2], [1, 1, 1], [1, 1, 1], [1, 1, 1], in_dtype="fp16"),
+    # 1x1: stride 2 pad 0 (strided GEMM), wide channels with a ragged pixel count, 3-D
+    spec(2, 1, 2, 48, 40, [11, 9], [1, 1], [2, 2]),
+    spec(2, 1, 3, 256, 96, [7, 5], [1, 1], out_dtype="bf16"),
+    spec(3, 2, 2, 16, 24, [3, 5, 4], [1, 1, 1], [1, 2, 1], in_dtype="fp16"),
     # depthwise: fast 3x3 window, generic taps, stride, ragged channel block, 1-D
     spec(2, 64, 2, 1, 1, [9, 13], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
     spec(2, 72, 3, 1, 1, [10, 7], [3, 2], [2, 1], [1, 2], [1, 0], [0, 1]),
@@ -157,7 +165,7 @@ def test_small_problems_all_modes(sp):
         assert_close(got, dw, A, sp["out_dtype"], f"{_ids(sp)} S={split_k} {mode} cluster={cl}")
 
 
-@pytest.mark.parametrize("sp", [SMALL[0], SMALL[3], SMALL[4], SMALL[10], SMALL[12], SMALL[14], SMALL[15]], ids=_ids)
+@pytest.mark.parametrize("sp", [SMALL[i] for i in (0, 3, 4, 10, 12, 14, 16, 17, 18)], ids=_ids)
 def test_integer_inputs_bitwise(sp):
     x, dy = make_inputs(sp, ("int", -2, 2), 17, 18)
     dw, _ = ref(sp, x, dy)

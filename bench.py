@@ -57,7 +57,7 @@ WORKLOADS = {
     "2d_grouped_g32_c8_k8_n32_h28": (spec(2, 32, 32, 8, 8, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16",
                                           "fp32"), ("normal", 0.0, 1.0), 3, 0, "auto", 0),
     "2d_depthwise_g512_n64_h28": (spec(2, 512, 64, 1, 1, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16",
-                                       "fp32"), ("uniform", -1.0, 1.0), 4, 0, "auto", 8),
+                                       "fp32"), ("uniform", -1.0, 1.0), 4, 0, "auto", 0),
     "3d_n4_d16_c128_k96_s2": (spec(3, 1, 4, 128, 96, [16, 16, 16], [3, 3, 3], [2, 2, 2], [1, 1, 1], [1, 1, 1],
                                    [1, 1, 1], "fp16", "fp32"), ("normal", 0.0, 0.5), 5, 8, "atomic", 0),
 }
@@ -74,9 +74,9 @@ VARIANTS = [
     ("2d_dense_n32_h56_c64_k64/S4_deterministic", "2d_dense_n32_h56_c64_k64", 4, "deterministic", 0, "auto"),
     ("2d_grouped_g32_c8_k8_n32_h28", "2d_grouped_g32_c8_k8_n32_h28", 0, "auto", 0, "auto"),
     ("2d_grouped_g32_c8_k8_n32_h28/atomic", "2d_grouped_g32_c8_k8_n32_h28", 0, "atomic", 0, "auto"),
-    ("2d_depthwise_g512_n64_h28", "2d_depthwise_g512_n64_h28", 0, "auto", 8, "auto"),
+    ("2d_depthwise_g512_n64_h28/gm8", "2d_depthwise_g512_n64_h28", 0, "auto", 8, "auto"),
     ("2d_depthwise_g512_n64_h28/gm1", "2d_depthwise_g512_n64_h28", 0, "auto", 1, "auto"),
-    ("2d_depthwise_g512_n64_h28/gm2", "2d_depthwise_g512_n64_h28", 0, "auto", 2, "auto"),
+    ("2d_depthwise_g512_n64_h28", "2d_depthwise_g512_n64_h28", 0, "auto", 0, "auto"),
     ("2d_depthwise_g512_n64_h28/gm4", "2d_depthwise_g512_n64_h28", 0, "auto", 4, "auto"),
     ("2d_depthwise_g512_n64_h28/gm4_atomic", "2d_depthwise_g512_n64_h28", 0, "atomic", 4, "auto"),
     ("2d_depthwise_g512_n64_h28/tensor_core", "2d_depthwise_g512_n64_h28", 0, "auto", 0, "igemm"),
@@ -229,8 +229,6 @@ L2_BYTES = 129 * 1000 * 1000
 TRAFFIC = {
     # igemm_wgrad_kernel: 25,785,344 B read + 135,424 B written (one launch, full size).
     "2d_dense_n32_h56_c64_k64": 25_920_768,
-    # depthwise_wgrad_kernel<bf16, 8, sliding>: 103,158,784 B read + 3,442,176 B written.
-    "2d_depthwise_g512_n64_h28": 106_600_960,
 }
 MAX_COPIES = 512
 

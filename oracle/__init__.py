@@ -4,8 +4,9 @@ TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()`` an
 the CPU-baseline leg of ``bench.py``, never by the product package.  It shares no
 code with the CUDA path.
 
-The C file ``wgrad_oracle.c`` holds the arithmetic (a direct loop over the
-definition of the weight gradient, see its header).  This module compiles it
+The C file ``wgrad_oracle.c`` holds the arithmetic (direct loops over the
+definitions of the weight gradient, the forward convolution and the
+backward-data gradient, see its header).  This module compiles it
 with gcc + OpenMP into ``oracle/_lib/liboracle.so`` and wraps it for numpy.
 
 A problem is a dict with keys ``ndim`` (1, 2 or 3), ``G``, ``N``, ``C``, ``K``
@@ -61,6 +62,7 @@ def _load():
         lib.orc_wgrad_at.argtypes = [ctypes.POINTER(_OProblem), dp, dp, ctypes.c_void_p, ctypes.c_long,
                                      dp, dp]
         lib.orc_conv_fwd.argtypes = [ctypes.POINTER(_OProblem), dp, dp, dp]
+        lib.orc_dgrad.argtypes = [ctypes.POINTER(_OProblem), dp, dp, dp, dp]
         _lib = lib
     return _lib
 
@@ -144,3 +146,15 @@ def conv_fwd(p: dict, x: np.ndarray, w: np.ndarray) -> np.ndarray:
     y = np.empty(sh["dy"], dtype=np.float64)
     _load().orc_conv_fwd(ctypes.byref(_struct(p)), _dp(x), _dp(w), _dp(y))
     return y
+
+
+def dgrad(p: dict, dy: np.ndarray, w: np.ndarray):
+    """Backward-data: dX (N,*in,G,C) from dY (N,*out,G,K) and W (G,K,*filt,C), and
+    A = sum |dY*W| over the same terms (float64)."""
+    sh = shapes(p)
+    dy = np.ascontiguousarray(dy, dtype=np.float64).reshape(sh["dy"])
+    w = np.ascontiguousarray(w, dtype=np.float64).reshape(sh["dw"])
+    dx = np.empty(sh["x"], dtype=np.float64)
+    ab = np.empty(sh["x"], dtype=np.float64)
+    _load().orc_dgrad(ctypes.byref(_struct(p)), _dp(dy), _dp(w), _dp(dx), _dp(ab))
+    return dx, ab

@@ -32,6 +32,10 @@
  *
  * Besides dW the oracle returns A = sum of |dY * X| over the same terms, the
  * scale that the tolerance of a floating-point comparison is stated in.
+ *
+ * It also holds the forward convolution with the same geometry and the
+ * backward-data gradient dX (the adjoint of the forward convolution in X),
+ * each written out the same way (see orc_conv_fwd and orc_dgrad).
  */
 #include <math.h>
 #include <stdint.h>
@@ -228,6 +232,64 @@ void orc_conv_fwd(const orc_problem* p, const double* x, const double* w, double
                     }
                 }
                 yout[(pix * G + g) * K + k] = s;
+            }
+    }
+}
+
+/* Backward-data (dgrad) of the same grouped convolution, the adjoint of
+ * orc_conv_fwd in X: each input position gathers every (output position, tap)
+ * pair that reads it,
+ *   dX[n,id,ih,iw,g,c] = sum over k, z, y, x with
+ *       od = (id + pld - z*dd) / sd, oh = (ih + plh - y*dh) / sh, ow = (iw + plw - x*dw) / sw
+ *       integral and inside the output
+ *   of dY[n,od,oh,ow,g,k] * W[g,k,z,y,x,c].
+ * Also returns A = sum of |dY * W| over the same terms. */
+void orc_dgrad(const orc_problem* p, const double* dy, const double* w, double* dx, double* absacc)
+{
+    int o[3];
+    out_dims(p, o);
+    const int G = p->G, N = p->N, C = p->C, K = p->K;
+    const int D = p->in[0], H = p->in[1], W = p->in[2];
+    const int Z = p->filt[0], Y = p->filt[1], X = p->filt[2];
+    long pix;
+    const long P = (long)N * D * H * W;
+#pragma omp parallel for schedule(static)
+    for (pix = 0; pix < P; ++pix) {
+        long r = pix;
+        const int iw = (int)(r % W); r /= W;
+        const int ih = (int)(r % H); r /= H;
+        const int id = (int)(r % D); r /= D;
+        const int n = (int)r;
+        for (int g = 0; g < G; ++g)
+            for (int c = 0; c < C; ++c) {
+                double s = 0.0, a = 0.0;
+                for (int z = 0; z < Z; ++z) {
+                    const int td = id + p->pad_l[0] - z * p->dil[0];
+                    if (td < 0 || td % p->stride[0]) continue;
+                    const int od = td / p->stride[0];
+                    if (od >= o[0]) continue;
+                    for (int y = 0; y < Y; ++y) {
+                        const int th = ih + p->pad_l[1] - y * p->dil[1];
+                        if (th < 0 || th % p->stride[1]) continue;
+                        const int oh = th / p->stride[1];
+                        if (oh >= o[1]) continue;
+                        for (int xx = 0; xx < X; ++xx) {
+                            const int tw = iw + p->pad_l[2] - xx * p->dil[2];
+                            if (tw < 0 || tw % p->stride[2]) continue;
+                            const int ow = tw / p->stride[2];
+                            if (ow >= o[2]) continue;
+                            const long yo = ((((long)n * o[0] + od) * o[1] + oh) * o[2] + ow) * G + g;
+                            for (int k = 0; k < K; ++k) {
+                                const double t = dy[yo * K + k] * w[(((((long)g * K + k) * Z + z) * Y + y) * X + xx) * C + c];
+                                s += t;
+                                a += fabs(t);
+                            }
+                        }
+                    }
+                }
+                const long xo = ((pix * G) + g) * C + c;
+                dx[xo] = s;
+                absacc[xo] = a;
             }
     }
 }

@@ -233,3 +233,93 @@ def test_decode_exact():
     np.testing.assert_array_equal(np.isnan(hf), np.isnan(ref))
     ok = ~np.isnan(ref)
     np.testing.assert_array_equal(hf[ok], ref[ok])
+
+
+# ----------------------------------------------------------------- backward-data
+def _rand_w(p, seed):
+    sh = oracle.shapes(p)
+    return synth.values(seed, int(np.prod(sh["dw"])), "uniform").reshape(sh["dw"])
+
+
+def torch_dgrad(p, dy, w):
+    """PyTorch's fp64 CPU autograd input gradient of the padded grouped convolution."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    nd, G, N, C, K = p["ndim"], p["G"], p["N"], p["C"], p["K"]
+    x0 = torch.zeros(N, G * C, *p["in"], dtype=torch.float64, requires_grad=True)
+    pad = []
+    for i in reversed(range(nd)):
+        pad += [p["pad_l"][i], p["pad_r"][i]]
+    wt = torch.from_numpy(np.ascontiguousarray(np.moveaxis(w, -1, 2))).reshape(G * K, C, *p["filt"])
+    conv = {1: F.conv1d, 2: F.conv2d, 3: F.conv3d}[nd]
+    yt = conv(F.pad(x0, pad), wt, stride=p["stride"], dilation=p["dil"], groups=G)
+    out = oracle.out_dims(p)
+    perm_in = (0, nd + 1, nd + 2) + tuple(range(1, nd + 1))
+    dyt = torch.from_numpy(np.ascontiguousarray(dy)).permute(*perm_in).reshape(N, G * K, *out)
+    yt.backward(dyt)
+    g = x0.grad.reshape(N, G, C, *p["in"]).numpy()
+    return np.moveaxis(np.moveaxis(g, 1, -1), 1, -1)  # (N, *in, G, C)
+
+
+def scatter_dgrad(p, dy, w):
+    """Pure-Python scatter form: every (output position, tap) adds dY * W to the
+    input position it reads."""
+    nd, G, N, C, K = p["ndim"], p["G"], p["N"], p["C"], p["K"]
+    out = oracle.out_dims(p)
+    dx = np.zeros((N, *p["in"], G, C))
+    for n in range(N):
+        for o in itertools.product(*[range(v) for v in out]):
+            for t in itertools.product(*[range(f) for f in p["filt"]]):
+                i = tuple(o[j] * p["stride"][j] - p["pad_l"][j] + t[j] * p["dil"][j] for j in range(nd))
+                if any(i[j] < 0 or i[j] >= p["in"][j] for j in range(nd)):
+                    continue
+                for g in range(G):
+                    dx[(n, *i, g)] += dy[(n, *o, g)] @ w[(g, slice(None), *t)]
+    return dx
+
+
+@pytest.mark.parametrize("p", SMALL, ids=lambda p: f"{p['ndim']}d_G{p['G']}")
+def test_dgrad_matches_torch_autograd(p):
+    _, dy = _rand(p, 61)
+    w = _rand_w(p, 63)
+    dx, _ = oracle.dgrad(p, dy, w)
+    np.testing.assert_allclose(dx, torch_dgrad(p, dy, w), rtol=1e-11, atol=1e-11)
+
+
+@pytest.mark.parametrize("p", SMALL[:5], ids=lambda p: f"{p['ndim']}d_G{p['G']}")
+def test_dgrad_matches_scatter(p):
+    _, dy = _rand(p, 71)
+    w = _rand_w(p, 73)
+    dx, _ = oracle.dgrad(p, dy, w)
+    np.testing.assert_allclose(dx, scatter_dgrad(p, dy, w), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("p", SMALL, ids=lambda p: f"{p['ndim']}d_G{p['G']}")
+def test_dgrad_adjoint_of_forward(p):
+    # <dgrad(dY, W), X'> = <dY, conv_fwd(X', W)> for any X'; conv_fwd is pinned to PyTorch above.
+    xp, dy = _rand(p, 81)
+    w = _rand_w(p, 83)
+    dx, _ = oracle.dgrad(p, dy, w)
+    lhs = float(np.sum(dx * xp))
+    rhs = float(np.sum(dy * oracle.conv_fwd(p, xp, w)))
+    assert abs(lhs - rhs) <= 1e-12 * max(1.0, abs(rhs))
+
+
+def test_dgrad_one_by_one_is_matmul():
+    p = _prob(2, 3, 2, 5, 4, [3, 4], [1, 1])
+    _, dy = _rand(p, 91)
+    w = _rand_w(p, 93)
+    dx, _ = oracle.dgrad(p, dy, w)
+    for g in range(3):
+        ref = dy[..., g, :].reshape(-1, 4) @ w[g].reshape(4, 5)
+        np.testing.assert_allclose(dx[..., g, :].reshape(-1, 5), ref, rtol=1e-13, atol=1e-13)
+
+
+def test_dgrad_abs_sum():
+    p = SMALL[3]
+    _, dy = _rand(p, 95)
+    w = _rand_w(p, 97)
+    dx, a = oracle.dgrad(p, dy, w)
+    a2, _ = oracle.dgrad(p, np.abs(dy), np.abs(w))
+    np.testing.assert_allclose(a, a2, rtol=1e-13, atol=1e-13)
+    assert np.all(a + 1e-15 >= np.abs(dx))

@@ -44,7 +44,7 @@ class WgradError(RuntimeError):
 
 EXPORTS = ("wg_problem_normalize", "wg_workspace_size", "wg_conv_bwd_weight", "wg_check_status",
            "wg_plan_string", "wg_status_string", "wg_last_error", "wg_conv_bwd_weight_noalloc",
-           "wg_set_mark_event")
+           "wg_set_mark_event", "wg_conv_bwd_data", "wg_bwd_data_plan_string")
 
 _lib = None
 _lock = threading.Lock()
@@ -72,6 +72,8 @@ def load():
                                                        ctypes.c_void_p]
             lib.wg_check_status.argtypes = [ctypes.c_void_p]
             lib.wg_set_mark_event.argtypes = [ctypes.c_void_p]
+            lib.wg_conv_bwd_data.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+            lib.wg_bwd_data_plan_string.argtypes = [P, ctypes.c_char_p, ctypes.c_size_t]
             lib.wg_plan_string.argtypes = [P, O, ctypes.c_char_p, ctypes.c_size_t]
             lib.wg_status_string.argtypes = [ctypes.c_int]
             lib.wg_status_string.restype = ctypes.c_char_p
@@ -182,6 +184,46 @@ def wg_conv_bwd_weight_noalloc(spec: dict, x, dy, dw, split_k: int = 0, mode: st
     p, o = make_problem(spec), make_options(split_k, mode, group_merge, cluster, kernel)
     _check(load().wg_conv_bwd_weight_noalloc(ctypes.byref(p), _addr(x), _addr(dy), _addr(dw), ctypes.byref(o),
                                              _stream_handle(stream)))
+
+
+def wg_conv_bwd_data(spec: dict, dy, w, dx, stream=None) -> None:
+    """Backward-data: dX (spec's out_dtype) from dY and W (spec's in_dtype); see include/wgrad.h."""
+    p = make_problem(spec)
+    _check(load().wg_conv_bwd_data(ctypes.byref(p), _addr(dy), _addr(w), _addr(dx), _stream_handle(stream)))
+
+
+def wg_bwd_data_plan_string(spec: dict) -> str:
+    p = make_problem(spec)
+    buf = ctypes.create_string_buffer(1024)
+    _check(load().wg_bwd_data_plan_string(ctypes.byref(p), buf, len(buf)))
+    return buf.value.decode()
+
+
+class PreparedDgradCall:
+    """wg_conv_bwd_data with its arguments marshalled once."""
+
+    def __init__(self, spec: dict, dy, w, dx):
+        self._keep = (dy, w, dx)
+        self.p = make_problem(spec)
+        self.fn = load().wg_conv_bwd_data
+        self.args = (ctypes.byref(self.p), ctypes.c_void_p(_addr(dy)), ctypes.c_void_p(_addr(w)),
+                     ctypes.c_void_p(_addr(dx)))
+
+    def __call__(self, stream_handle: int | None = None) -> None:
+        st = self.fn(*self.args, stream_handle)
+        if st:
+            _check(st)
+
+
+def conv_bwd_data(spec: dict, dy, w, out=None, stream=None):
+    """Convenience wrapper over wg_conv_bwd_data for torch CUDA tensors: allocates dX
+    (N, *in, G, C) in spec['out_dtype'] with torch, then calls the library."""
+    import torch
+    tdt = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}[spec.get("out_dtype", "fp32")]
+    if out is None:
+        out = torch.empty((spec["N"], *spec["in"], spec["G"], spec["C"]), dtype=tdt, device=dy.device)
+    wg_conv_bwd_data(spec, dy, w, out, stream)
+    return out
 
 
 def wg_set_mark_event(event) -> None:

@@ -593,4 +593,85 @@ std::string plan_string(const Plan& pl)
     return buf;
 }
 
+int make_dgrad_plan(const wg_problem* p, const DeviceCaps& caps, DgPlan* pl, std::string* err)
+{
+    std::memset(pl, 0, sizeof *pl);
+    int st = normalize(p, &pl->pb, err);
+    if (st) return st;
+    const Problem& pb = pl->pb;
+    (void)caps;
+    for (int j = 0; j < 3; ++j)
+        if (pb.stride[j] != 1)
+            return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: strides above 1 are not supported");
+    if (pb.C % 8) return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: C must be a multiple of 8 (16-byte W rows)");
+    if (pb.G > 1 && pb.K % 8)
+        return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: K must be a multiple of 8 when G > 1");
+    if (((long long)pb.G * pb.K) % 8)
+        return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: G*K must be a multiple of 8 (16-byte dY rows)");
+    if (pb.G > 65535) return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: too many groups");
+    DgPlan& d = *pl;
+    if (pb.ndim == 1) {
+        d.bw = 128, d.bh = 1;
+    } else {
+        d.bw = 8, d.bh = 16;
+    }
+    const int X = pb.filt[2], Y = pb.filt[1], Z = pb.filt[0];
+    d.PW = d.bw + (X - 1) * pb.dil[2];
+    d.PH = d.bh + (Y - 1) * pb.dil[1];
+    if (d.PW > 256 || d.PH > 256)
+        return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: dilated filter too wide for a 256-row patch");
+    d.XY = X * Y;
+    d.patch_bytes = round_up(d.PW * d.PH * 128, 1024);
+    d.n_kc = (int)cdiv(pb.K, 64);
+    // N-tile and taps per stage: the widest N-tile (up to 256 channels) with
+    // every tap of a plane in one stage and two stages in shared memory; else
+    // 64 channels and the plane's taps in groups.
+    const int avail = kMaxSmemPerCta - 2048;
+    const int cmax = round_up(pb.C, 16);
+    d.Nt = 0;
+    for (int nt = 256; nt >= 16; nt /= 2) {
+        if (nt > cmax && nt > 16) continue;
+        const int na = (int)cdiv(nt, 64);
+        if (2 * (d.patch_bytes + d.XY * na * 8192) <= avail) {
+            d.Nt = nt;
+            d.TG = d.XY;
+            break;
+        }
+    }
+    if (!d.Nt) {
+        d.Nt = std::min(64, cmax);
+        d.TG = (avail / 2 - d.patch_bytes) / 8192;
+        if (d.TG < 1) return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: the dY patch does not fit shared memory");
+    }
+    d.n_catoms = (int)cdiv(d.Nt, 64);
+    d.n_ctiles = (int)cdiv(pb.C, d.Nt);
+    d.n_tg = (int)cdiv(d.XY, d.TG);
+    d.stage_bytes = d.patch_bytes + d.TG * d.n_catoms * 8192;
+    d.stages = std::min(4, avail / d.stage_bytes);
+    d.smem_bytes = d.stages * d.stage_bytes + 2048;
+    d.tmem_cols = std::max(32, pow2_at_least(d.Nt));
+    d.n_tw = (int)cdiv(pb.in[2], d.bw);
+    d.n_th = (int)cdiv(pb.in[1], d.bh);
+    d.n_tiles = (long long)d.n_tw * d.n_th * pb.in[0] * pb.N;
+    d.n_iters = d.n_kc * Z * d.n_tg;
+    if (d.n_tiles > (1ll << 31) - 1) return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: too many pixel tiles");
+    d.grid[0] = (unsigned)d.n_tiles;
+    d.grid[1] = (unsigned)d.n_ctiles;
+    d.grid[2] = (unsigned)pb.G;
+    d.block = 256;
+    return WG_OK;
+}
+
+std::string dgrad_plan_string(const DgPlan& d)
+{
+    char buf[512];
+    snprintf(buf, sizeof buf,
+             "kernel=dgrad_tcgen05 box=(w%d,h%d) patch=(w%d,h%d) Nt=%d catoms=%d ctiles=%d kchunks=%d taps/plane=%d "
+             "taps/stage=%d stages/tile=%d patch_bytes=%d stage_bytes=%d ring=%d smem=%d tmem_cols=%d "
+             "grid=(%u,%u,%u) block=%u",
+             d.bw, d.bh, d.PW, d.PH, d.Nt, d.n_catoms, d.n_ctiles, d.n_kc, d.XY, d.TG, d.n_iters, d.patch_bytes,
+             d.stage_bytes, d.stages, d.smem_bytes, d.tmem_cols, d.grid[0], d.grid[1], d.grid[2], d.block);
+    return buf;
+}
+
 }  // namespace wg

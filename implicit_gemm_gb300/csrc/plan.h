@@ -128,4 +128,30 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
 
 std::string plan_string(const Plan& pl);
 
+// Backward-data (dgrad) on the tensor cores: dX[pixel, c] = sum over (k, tap)
+// of dY[pixel shifted by the tap, k] * W[k, tap, c].  A CTA owns a box of 128
+// input pixels of one image and depth slice (8 x 16, or 128 along W for 1-D
+// problems), an N-tile of C and one group; it walks (K chunk of 64, filter
+// plane z, tap group) stages, each a dY halo patch (one row-shifted view per
+// tap) plus the W tiles of the group's taps.
+struct DgPlan {
+    Problem pb;
+    int bw, bh;           // pixel box along (w, h)
+    int PW, PH;           // dY patch extent along (w, h)
+    int Nt, n_catoms, n_ctiles;
+    int n_kc;             // 64-channel chunks of K
+    int XY, TG, n_tg;     // taps per filter plane, taps per stage, tap groups per plane
+    int patch_bytes;      // dY patch bytes (1024-aligned)
+    int stage_bytes, stages, smem_bytes, tmem_cols;
+    int n_tw, n_th;       // boxes along w and h
+    long long n_tiles;    // n_tw * n_th * D * N
+    int n_iters;          // n_kc * Z * n_tg stages per tile
+    unsigned grid[3];
+    unsigned block;
+};
+
+int make_dgrad_plan(const wg_problem* p, const DeviceCaps& caps, DgPlan* out, std::string* err);
+
+std::string dgrad_plan_string(const DgPlan& pl);
+
 }  // namespace wg

@@ -12,6 +12,7 @@
 
 #include "../../include/wgrad.h"
 #include "k_depthwise.cuh"
+#include "k_dgrad.cuh"
 #include "k_igemm.cuh"
 #include "plan.h"
 
@@ -663,6 +664,139 @@ int wg_conv_bwd_weight_noalloc(const wg_problem* p, const void* x, const void* d
         if (need > kNoAllocScratchBytes) return set_err(WG_ERR_WORKSPACE, "split-K workspace does not fit the scratch array");
     }
     return wg_conv_bwd_weight(p, x, dy, dw, &o, need ? scratch : nullptr, need ? kNoAllocScratchBytes : 0, stream);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward-data (dgrad).
+namespace {
+
+struct DgPrepared {
+    CUtensorMap tmy, tmw;
+    wg::DgParams prm;
+};
+
+int dgrad_plan_for(const wg_problem* p, wg::DgPlan* pl, std::string* key_out)
+{
+    static std::mutex mu;
+    static std::map<std::string, wg::DgPlan> cache;
+    const wg::DeviceCaps caps = device_caps();
+    std::string key;
+    if (p) {
+        key.assign(reinterpret_cast<const char*>(p), sizeof *p);
+        key.append(reinterpret_cast<const char*>(&caps), sizeof caps);
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            *pl = it->second;
+            *key_out = key;
+            return WG_OK;
+        }
+    }
+    std::string err;
+    const int st = wg::make_dgrad_plan(p, caps, pl, &err);
+    if (st) return set_err(st, err);
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache.size() > 1024) cache.clear();
+    cache.emplace(key, *pl);
+    *key_out = key;
+    return WG_OK;
+}
+
+int prepare_dgrad(const wg::DgPlan& d, const void* dy, const void* w, void* dx, DgPrepared* out)
+{
+    const wg::Problem& pb = d.pb;
+    {
+        const cuuint64_t dims[5] = {(cuuint64_t)pb.G * pb.K, (cuuint64_t)pb.out[2], (cuuint64_t)pb.out[1],
+                                    (cuuint64_t)pb.out[0], (cuuint64_t)pb.N};
+        const cuuint32_t box[5] = {64, (cuuint32_t)d.PW, (cuuint32_t)d.PH, 1, 1};
+        const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        const int st = encode(&out->tmy, pb.in_dtype, const_cast<void*>(dy), dims, box, estr, CU_TENSOR_MAP_SWIZZLE_128B,
+                              "dY");
+        if (st) return st;
+    }
+    {
+        // W viewed as (C, taps, K, G): k beyond the group's K is out of bounds and reads zero.
+        const cuuint64_t dims[5] = {(cuuint64_t)pb.C, (cuuint64_t)pb.T, (cuuint64_t)pb.K, (cuuint64_t)pb.G, 1};
+        const cuuint32_t box[5] = {64, 1, 64, 1, 1};
+        const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        const int st = encode(&out->tmw, pb.in_dtype, const_cast<void*>(w), dims, box, estr, CU_TENSOR_MAP_SWIZZLE_128B,
+                              "W");
+        if (st) return st;
+    }
+    wg::DgParams& q = out->prm;
+    memset(&q, 0, sizeof q);
+    q.G = pb.G, q.C = pb.C, q.K = pb.K;
+    q.X = pb.filt[2], q.Y = pb.filt[1], q.Z = pb.filt[0], q.XY = d.XY;
+    q.dw = pb.dil[2], q.dh = pb.dil[1], q.dd = pb.dil[0];
+    q.plw = pb.pad_l[2], q.plh = pb.pad_l[1], q.pld = pb.pad_l[0];
+    q.Wi = pb.in[2], q.Hi = pb.in[1], q.Di = pb.in[0];
+    q.bw = d.bw, q.bh = d.bh, q.PW = d.PW, q.PH = d.PH;
+    q.Nt = d.Nt, q.n_catoms = d.n_catoms;
+    q.n_kc = d.n_kc, q.TG = d.TG, q.n_tg = d.n_tg, q.n_iters = d.n_iters;
+    q.n_tw = d.n_tw, q.n_th = d.n_th;
+    q.patch_bytes = d.patch_bytes, q.stage_bytes = d.stage_bytes, q.stages = d.stages, q.tmem_cols = d.tmem_cols;
+    q.idesc = wg::make_idesc_f16(pb.in_dtype == WG_BF16, false, true, 128, d.Nt);
+    q.out_dtype = pb.out_dtype;
+    q.out = dx;
+    return WG_OK;
+}
+
+std::mutex g_dg_mu;
+std::map<std::string, DgPrepared>& dg_cache()
+{
+    static std::map<std::string, DgPrepared> m;
+    return m;
+}
+
+}  // namespace
+
+extern "C" {
+
+int wg_bwd_data_plan_string(const wg_problem* p, char* buf, size_t n)
+{
+    if (!buf || n == 0) return set_err(WG_ERR_INVALID_ARGUMENT, "buffer is NULL or empty");
+    wg::DgPlan d;
+    std::string key;
+    const int st = dgrad_plan_for(p, &d, &key);
+    if (st) return st;
+    snprintf(buf, n, "%s", wg::dgrad_plan_string(d).c_str());
+    return WG_OK;
+}
+
+int wg_conv_bwd_data(const wg_problem* p, const void* dy, const void* w, void* dx, void* stream)
+{
+    wg::DgPlan d;
+    std::string pkey;
+    int st = dgrad_plan_for(p, &d, &pkey);
+    if (st) return st;
+    if (!dy || !w || !dx) return set_err(WG_ERR_INVALID_ARGUMENT, "dy, w and dx must be non-NULL device pointers");
+    if (!aligned16(dy) || !aligned16(w) || !aligned16(dx))
+        return set_err(WG_ERR_MISALIGNED, "dy, w and dx must be 16-byte aligned");
+    const std::string key = prep_key(pkey, dy, w, dx, nullptr);
+    DgPrepared pr;
+    bool hit = false;
+    {
+        std::lock_guard<std::mutex> lk(g_dg_mu);
+        auto it = dg_cache().find(key);
+        if (it != dg_cache().end()) pr = it->second, hit = true;
+    }
+    if (!hit) {
+        st = prepare_dgrad(d, dy, w, dx, &pr);
+        if (st) return st;
+        std::lock_guard<std::mutex> lk(g_dg_mu);
+        if (dg_cache().size() > 4096) dg_cache().clear();
+        dg_cache().emplace(key, pr);
+    }
+    st = ensure_smem(wg::dgrad_kernel, d.smem_bytes);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    wg::dgrad_kernel<<<dim3(d.grid[0], d.grid[1], d.grid[2]), d.block, d.smem_bytes, s>>>(pr.tmy, pr.tmw, pr.prm);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail("dgrad_kernel launch", e);
+    if (g_mark && (e = cudaEventRecord(g_mark, s)) != cudaSuccess) return cuda_fail("cudaEventRecord(mark)", e);
+    return WG_OK;
 }
 
 }  // extern "C"

@@ -201,6 +201,29 @@ WG_API int wg_conv_bwd_weight_noalloc(const wg_problem* p, const void* x, const 
  * with it set is slightly slower.  NULL turns it off.  Returns WG_OK.  Host only. */
 WG_API int wg_set_mark_event(void* event);
 
+/* Backward-data (dgrad) of the same grouped convolution, the step beside the
+ * weight gradient in training (the pages' "dgrad" section: dY, NHWGK, read
+ * with its contiguous K channels as the reduction axis; W read as KYXC):
+ *
+ *   dX[n,(d),(h),w,g,c] = sum over k and taps (z,y,x) with
+ *       (d + pad_l - z*dil, h + pad_l - y*dil, w + pad_l - x*dil) / stride integral
+ *       and inside the output, of dY[n, that position, g, k] * W[g,k,z,y,x,c]
+ *
+ *  p:  the convolution, as for wg_conv_bwd_weight; here in_dtype is the dtype
+ *      of dY and W (WG_BF16 or WG_FP16) and out_dtype that of dX (WG_FP32,
+ *      WG_BF16 or WG_FP16).
+ *  dy: N(Do)(Ho)WoGK, w: GK(Z)(Y)XC (in_dtype), dx: N(D)(H)WGC (out_dtype),
+ *      device pointers, 16-byte aligned, owned by the caller.  dX is
+ *      overwritten (every element is written once; no workspace).
+ * Supported: stride 1 in every dimension, any dilation and pads, C a multiple
+ * of 8, K a multiple of 8 when G > 1; otherwise WG_ERR_NOT_SUPPORTED.
+ * Returns WG_OK or an error status; nothing is launched on an error.  The
+ * kernel runs on `stream` (a cudaStream_t). */
+WG_API int wg_conv_bwd_data(const wg_problem* p, const void* dy, const void* w, void* dx, void* stream);
+
+/* Human-readable plan of wg_conv_bwd_data for p.  Host only. */
+WG_API int wg_bwd_data_plan_string(const wg_problem* p, char* buf, size_t n);
+
 #ifdef __cplusplus
 }
 #endif

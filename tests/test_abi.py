@@ -178,3 +178,27 @@ def test_kernel_selector():
         buf = ctypes.create_string_buffer(256)
         binding._check(binding.load().wg_plan_string(ctypes.byref(p), ctypes.byref(lib_opts), buf, len(buf)))
     assert e.value.status == 1
+
+
+def test_dgrad_plans_and_limits():
+    dense = WORKLOADS["2d_dense_n32_h56_c64_k64"][0]
+    ps = binding.wg_bwd_data_plan_string(dense)
+    assert "kernel=dgrad_tcgen05" in ps and "box=(w8,h16)" in ps
+    one_d = spec(1, 1, 2, 16, 24, [300], [5], [1], [2], [4], [4])
+    assert "box=(w128,h1)" in binding.wg_bwd_data_plan_string(one_d)
+    for bad, status in ((spec(2, 1, 1, 16, 16, [9, 9], [3, 3], [2, 2]), 2),      # stride 2
+                        (spec(2, 2, 1, 4, 8, [9, 9], [3, 3]), 2),                # C not a multiple of 8
+                        (spec(2, 1, 1, 0, 8, [9, 9], [3, 3]), 1)):               # C = 0
+        with pytest.raises(binding.WgradError) as e:
+            binding.wg_bwd_data_plan_string(bad)
+        assert e.value.status == status
+
+
+def test_dgrad_launch_checks_before_device(lib):
+    sp = spec(2, 1, 1, 16, 16, [8, 8], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_conv_bwd_data(sp, 0, 4096, 8192)
+    assert e.value.status == 1
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_conv_bwd_data(sp, 4096, 8192 + 4, 12288)
+    assert e.value.status == 3

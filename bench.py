@@ -315,6 +315,38 @@ class Workload:
         self.dw_host.copy_(self.dw, non_blocking=True)
 
 
+class DgradWorkload:
+    """Backward-data on a workload's geometry: dY and W resident (dY rotated through
+    copies larger than 2x L2, like the weight-gradient inputs), dX written."""
+
+    def __init__(self, torch, name):
+        self.torch = torch
+        sp, dist, seed = WORKLOADS[name][:3]
+        self.sp = sp
+        s = sizes(sp)
+        tdt = torch.bfloat16 if sp["in_dtype"] == "bf16" else torch.float16
+        odt = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}[sp["out_dtype"]]
+        dyb = synth.tensor_bits(2000 + seed, s["ndy"], sp["in_dtype"], *dist)
+        wb = synth.tensor_bits(3000 + seed, s["ndw"], sp["in_dtype"], *dist)
+        self.dy = torch.from_numpy(dyb.view(np.int16)).view(tdt).cuda()
+        self.w = torch.from_numpy(wb.view(np.int16)).view(tdt).cuda()
+        self.dx = torch.empty(s["nx"], dtype=odt, device="cuda")
+        self.flops = s["flops"]
+        self.bytes = 2 * (s["ndy"] + s["ndw"]) + s["nx"] * (4 if sp["out_dtype"] == "fp32" else 2)
+        self.plan = binding.wg_bwd_data_plan_string(sp)
+        need = -(-2 * L2_BYTES // (2 * s["ndy"]))
+        self.copies = max(2, need) if need <= MAX_COPIES else 1
+        self.dys = [self.dy] + [self.dy.clone() for _ in range(self.copies - 1)]
+        self.calls = [binding.PreparedDgradCall(sp, d, self.w, self.dx) for d in self.dys]
+        self.next = 0
+        self.rotating = self.copies > 1
+        self.graph = None
+
+    def step(self, stream):
+        self.calls[self.next](stream.cuda_stream)
+        self.next = (self.next + 1) % self.copies
+
+
 class L2Flush:
     """Evicts the inputs from L2 between timed steps: writes a 256 MiB buffer (twice
     the L2), then reads another 256 MiB buffer so that the write-back of the dirty
@@ -529,6 +561,18 @@ def main():
                            "kernel_roofline_frac": max(tf, tb) / (kms * 1e-3), "traffic": TRAFFIC.get(name),
                            "l2": w2.l2_note(), "plan": w2.plan}
             del w2
+        # Backward-data (dgrad) on the dense and 1x1 geometries.
+        for name in ("2d_dense_n32_h56_c64_k64", "2d_1x1_n32_h56_c64_k256"):
+            w3 = DgradWorkload(torch, name)
+            ms = float(np.mean(time_steps(torch, w3, 300, 10, flush, stream)))
+            tf, tb = w3.flops / (pk["bf16"] * 1e12), w3.bytes / (pk["hbm"] * 1e9)
+            extra["dgrad/" + name] = {"ms_per_step": ms, "tflops": w3.flops / (ms * 1e-3) / 1e12,
+                                      "gbs": w3.bytes / (ms * 1e-3) / 1e9, "roofline_us": max(tf, tb) * 1e6,
+                                      "bound": "hbm" if tb >= tf else "tensor",
+                                      "roofline_frac": max(tf, tb) / (ms * 1e-3), "kernel_ms": ms,
+                                      "kernel_roofline_frac": max(tf, tb) / (ms * 1e-3), "traffic": None,
+                                      "l2": f"dY rotates through {w3.copies} copies", "plan": w3.plan}
+            del w3
 
     if rank == 0:
         line = {"metric": "wgrad TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,

@@ -226,10 +226,7 @@ L2_BYTES = 129 * 1000 * 1000
 # DRAM bytes (read + write) of one launch of the workload's main kernel from an
 # ncu capture of the kernel as it now stands (summaries under profiles/); a
 # workload without such a capture reports null.
-TRAFFIC = {
-    # igemm_wgrad_kernel: 25,785,344 B read + 135,424 B written (one launch, full size).
-    "2d_dense_n32_h56_c64_k64": 25_920_768,
-}
+TRAFFIC = {}
 MAX_COPIES = 512
 
 

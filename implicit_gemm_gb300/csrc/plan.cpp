@@ -120,6 +120,19 @@ long long epilogue_clk(long long dw_bytes, int n_out, int Q, long long red_bytes
 
 int cap_index(int q) { return q == 1 ? 0 : q == 2 ? 1 : q == 4 ? 2 : 3; }
 
+// Split degree without clusters: the caller's, 1 for mode DIRECT, else enough
+// splits of the K-tiles to fill the device once, evened out so that no split
+// is short by more than one K-tile.
+long long split_for(const wg_options& o, long long base, long long ktiles, const DeviceCaps& caps)
+{
+    if (o.split_k > 0) return o.split_k;
+    if (o.mode == WG_MODE_DIRECT) return o.cluster > 1 ? o.cluster : 1;
+    long long s = std::max(1LL, caps.cluster_ctas[0] / std::max(1LL, base));
+    s = std::min(s, std::max(1LL, ktiles));
+    const long long per = cdiv(ktiles, s);
+    return cdiv(ktiles, per);
+}
+
 int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::string* err)
 {
     const int num_sms = caps.num_sms;
@@ -201,15 +214,29 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
                 if (stage > avail) continue;
                 const int stages = std::min(8, (int)(avail / stage));
                 if (stages < 2) continue;
-                // Per K-tile and CTA: tensor-core cycles (M128 x N x K16 ~ N/2
-                // cycles) against shared-memory fill at ~64 B/cycle, plus a fixed
-                // overhead; fewer than 3 stages exposes latency.
+                // Per K-tile and CTA: the MMAs -- each the longer of the tensor
+                // pipe (N/2 cycles) and its shared-memory reads (A 4 KB + B 32*N
+                // bytes at ~128 B/cycle) -- against the stage's fill at ~40
+                // B/cycle (every SM loading at once; calibrated on the 56x56
+                // workload, where 2, 3 and 5 M-tiles per CTA measured 27.6,
+                // 24.7 and 26.5 us), plus a fixed overhead; fewer than 3 stages
+                // exposes latency.
                 const long long mranges = cdiv(ig.n_mtiles, mt);
-                const long long mma_clk = (long long)mt * (c.KT / 16) * (ig.Nt / 2);
-                const long long load_clk = stage / 64;
+                const long long mma_one = std::max<long long>(ig.Nt / 2, 32 + ig.Nt / 4);
+                const long long mma_clk = (long long)mt * (c.KT / 16) * mma_one;
+                const long long load_clk = stage / 40;
                 long long tile_clk = std::max(mma_clk, load_clk) + 64;
                 if (stages < 3) tile_clk = tile_clk * 13 / 10;
-                const long long cost = mranges * ig.n_ntiles * ig.n_gblocks * ktiles * tile_clk;
+                // Whole-call estimate: the split degree this tiling gets (the
+                // caller's, or enough to fill the device once), the K-tiles of
+                // one split in waves of resident CTAs, and the partial sums that
+                // the splits write and the reduction reads back.
+                const long long base = mranges * ig.n_ntiles * ig.n_gblocks;
+                const long long S = split_for(o, base, ktiles, caps);
+                const long long waves = cdiv(base * S, caps.cluster_ctas[0]);
+                const long long red_bytes = (long long)mt * ig.Nt * 512;
+                const long long cost = waves * cdiv(ktiles, S) * tile_clk +
+                                       epilogue_clk(pb.dw_elems * 4, (int)S, 1, red_bytes, o.mode == WG_MODE_ATOMIC);
                 if (best.cost < 0 || cost < best.cost) {
                     c.mt = mt;
                     c.stages = stages;
@@ -219,7 +246,6 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
                     c.tile_clk = tile_clk;
                     best = c;
                 }
-                if (stages >= 3) break;  // smaller mt only re-reads more
             }
         }
     }

@@ -1,10 +1,13 @@
-// Backward-data (dgrad) of the grouped convolution on the tensor cores, for
-// stride 1:
+// Backward-data (dgrad) of the grouped convolution on the tensor cores:
 //
-//   dX[n, i, g, c] = sum over k and taps t of dY[n, i + pl - t*dil, g, k] * W[g, k, t, c]
+//   dX[n, i, g, c] = sum over k and taps t with (i + pl - t*dil) / stride integral
+//                    of dY[n, (i + pl - t*dil) / stride, g, k] * W[g, k, t, c]
 //
 // with dY positions outside the output reading zero (the adjoint of the forward
-// convolution in X).  The pages' dgrad keeps dY (NHWGK) M-outer, its reduction
+// convolution in X).  Strides split each dim's input positions into phases
+// i = r + stride * j; within a phase the contributing taps read dY at j plus a
+// fixed offset, so each phase is a stride-1 problem over its own tap list
+// (tables in DgParams::dim, built on the host).  The pages' dgrad keeps dY (NHWGK) M-outer, its reduction
 // axis k already contiguous, and reads W as KYXC; here the GEMM is
 // D[pixel, c] += dY[pixel, k] * W[k, c] per tap, with:
 //
@@ -27,23 +30,22 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "plan.h"
 #include "ptx.cuh"
 
 namespace wg {
 
 struct DgParams {
-    int G, C, K, X, Y, Z, XY;
-    int dw, dh, dd;     // dilation along w, h, d
-    int plw, plh, pld;  // left pad along w, h, d
+    int G, C, K, X, Y;
     int Wi, Hi, Di;     // dX extents
     int bw, bh, PW, PH;
-    int Nt, n_catoms;
-    int n_kc, TG, n_tg, n_iters;
-    int n_tw, n_th;
+    int Nt, n_catoms, n_kc, TG;
+    int n_tw, n_th, n_td;
     int patch_bytes, stage_bytes, stages, tmem_cols;
     uint32_t idesc;
     int out_dtype;  // wg_dtype of dX
     void* out;
+    DgDim dim[3];   // stride phases along (w, h, d): positions, dY offsets, taps and their row shifts
 };
 
 constexpr int kDgThreads = 256;
@@ -104,18 +106,34 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(accb + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Tile: stride phase (pw, ph, pd), box (tw, th) of phase positions, depth
+    // position td and image n.
     long long t = blockIdx.x;
+    const DgDim& DW = p.dim[0];
+    const DgDim& DH = p.dim[1];
+    const DgDim& DD = p.dim[2];
+    const int pw = (int)(t % DW.nph);
+    t /= DW.nph;
+    const int ph = (int)(t % DH.nph);
+    t /= DH.nph;
+    const int pd = (int)(t % DD.nph);
+    t /= DD.nph;
     const int tw = (int)(t % p.n_tw);
     t /= p.n_tw;
     const int th = (int)(t % p.n_th);
     t /= p.n_th;
-    const int di = (int)(t % p.Di);
-    const int n = (int)(t / p.Di);
+    const int td = (int)(t % p.n_td);
+    const int n = (int)(t / p.n_td);
     const int ct = blockIdx.y, g = blockIdx.z;
-    const int w0 = tw * p.bw, h0 = th * p.bh, c0 = ct * p.Nt;
-    const int nk = p.n_iters;
+    const int j0w = tw * p.bw, j0h = th * p.bh, c0 = ct * p.Nt;
+    const int nx = DW.ntap[pw], ny = DH.ntap[ph], nz = DD.ntap[pd];
+    const int nyx = nx * ny, TG = p.TG;
+    const int n_tg = (nyx + TG - 1) / TG;
+    // A tile with no position in its phase, or a phase no tap reaches, does no MMAs.
+    const bool any = j0w < DW.J[pw] && j0h < DH.J[ph] && td < DD.J[pd];
+    const int nk = any ? p.n_kc * nz * n_tg : 0;
     const int stages = p.stages, stage_bytes = p.stage_bytes, patch_bytes = p.patch_bytes;
-    const int n_catoms = p.n_catoms, TG = p.TG, n_tg = p.n_tg, XY = p.XY, X = p.X;
+    const int n_catoms = p.n_catoms, X = p.X;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < stages; ++i) {
@@ -146,20 +164,24 @@ __global__ void __launch_bounds__(kDgThreads, 1)
             const uint32_t patch_tx = (uint32_t)(p.PW * p.PH * 128);
             for (int i = 0; i < nk; ++i) {
                 const int st = i % stages;
-                const uint32_t ph = (uint32_t)(i / stages) & 1u;
-                if (i >= stages && !mbar_wait(&empty[st], ph ^ 1u)) break;
+                const uint32_t ph2 = (uint32_t)(i / stages) & 1u;
+                if (i >= stages && !mbar_wait(&empty[st], ph2 ^ 1u)) break;
                 const int tg = i % n_tg, rest = i / n_tg;
-                const int z = rest % p.Z, kc = rest / p.Z;
-                const int tap0 = tg * TG, ntap = min(TG, XY - tap0);
+                const int zi = rest % nz, kc = rest / nz;
+                const int y0 = tg * TG, ntap = min(TG, nyx - y0);
+                const int z = DD.tap[pd][zi];
                 uint8_t* sb = smem + st * stage_bytes;
                 mbar_arrive_expect_tx(&full[st], patch_tx + (uint32_t)(ntap * n_catoms) * kDgWTile);
-                // The dY rows the box's pixels read for every tap of plane z.
-                tma_load_5d(sb, &tmy, &full[st], g * p.K + kc * 64, w0 + p.plw - (X - 1) * p.dw,
-                            h0 + p.plh - (p.Y - 1) * p.dh, di + p.pld - z * p.dd, n);
-                for (int j = 0; j < ntap; ++j)
+                // The dY rows the box's positions read for every (y, x) tap of plane z.
+                tma_load_5d(sb, &tmy, &full[st], g * p.K + kc * 64, j0w + DW.qmin[pw], j0h + DH.qmin[ph],
+                            td + DD.qmin[pd] + DD.shift[pd][zi], n);
+                for (int j = 0; j < ntap; ++j) {
+                    const int yi = (y0 + j) / nx, xi = (y0 + j) - yi * nx;
+                    const int tap = (z * p.Y + DH.tap[ph][yi]) * X + DW.tap[pw][xi];
                     for (int a = 0; a < n_catoms; ++a)
                         tma_load_5d(sb + patch_bytes + (uint32_t)(j * n_catoms + a) * kDgWTile, &tmw, &full[st],
-                                    c0 + 64 * a, z * XY + tap0 + j, kc * 64, g, 0);
+                                    c0 + 64 * a, tap, kc * 64, g, 0);
+                }
             }
         }
         __syncwarp();
@@ -169,17 +191,16 @@ __global__ void __launch_bounds__(kDgThreads, 1)
         const uint32_t sbo = (uint32_t)((p.bw == 8 ? p.PW : 8) * 128);
         const uint32_t idesc = p.idesc;
         int st = 0;
-        uint32_t ph = 0;
+        uint32_t par = 0;
         for (int i = 0; i < nk; ++i) {
-            if (!mbar_wait(&full[st], ph)) break;
+            if (!mbar_wait(&full[st], par)) break;
             tc_fence_after();
             const int tg = i % n_tg;
-            const int tap0 = tg * TG, ntap = min(TG, XY - tap0);
+            const int y0 = tg * TG, ntap = min(TG, nyx - y0);
             const uint32_t sst = sbase + (uint32_t)(st * stage_bytes);
             for (int j = 0; j < ntap; ++j) {
-                const int tap = tap0 + j;
-                const int y = tap / X, x = tap - (tap / X) * X;
-                const int shift = (p.Y - 1 - y) * p.dh * p.PW + (X - 1 - x) * p.dw;
+                const int yi = (y0 + j) / nx, xi = (y0 + j) - yi * nx;
+                const int shift = DH.shift[ph][yi] * p.PW + DW.shift[pw][xi];
                 const uint64_t a0 = make_sdesc(sst + (uint32_t)shift * 128u, 16u, sbo, 2u, 0u);
                 const uint64_t b0 =
                     make_sdesc(sst + (uint32_t)patch_bytes + (uint32_t)(j * n_catoms) * kDgWTile, kDgWTile, 1024u, 2u, 0u);
@@ -192,9 +213,9 @@ __global__ void __launch_bounds__(kDgThreads, 1)
             }
             if (elect_one()) umma_commit(&empty[st]);
             __syncwarp();
-            if (++st == stages) st = 0, ph ^= 1u;
+            if (++st == stages) st = 0, par ^= 1u;
         }
-        if (elect_one()) umma_commit(accb);
+        if (nk > 0 && elect_one()) umma_commit(accb);
         __syncwarp();
     }
     // ---------------------------------------------------- epilogue (all warps)
@@ -202,12 +223,15 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     tc_fence_after();
     tbase = *tslot;
     {
-        mbar_wait_sleep(accb, 0);
-        tc_fence_after();
+        if (nk > 0) {
+            mbar_wait_sleep(accb, 0);
+            tc_fence_after();
+        }
         const int q = warp & 3;
         const int row = q * 32 + lane;
-        const int w = w0 + row % p.bw, h = h0 + row / p.bw;
-        const bool valid = w < p.Wi && h < p.Hi;
+        const int jw = j0w + row % p.bw, jh = j0h + row / p.bw;
+        const bool valid = jw < DW.J[pw] && jh < DH.J[ph] && td < DD.J[pd];
+        const int w = pw + DW.nph * jw, h = ph + DH.nph * jh, di = pd + DD.nph * td;
         const long long pix = (((long long)n * p.Di + di) * p.Hi + h) * p.Wi + w;
         const long long obase = (pix * p.G + g) * p.C + c0;
         const int Nt = p.Nt;
@@ -216,7 +240,12 @@ __global__ void __launch_bounds__(kDgThreads, 1)
         const uint32_t trow = tbase + ((uint32_t)(q * 32) << 16);
         for (int cb = c_lo; cb < c_hi; cb += 32) {
             float v[32];
-            dg_ld(trow + (uint32_t)cb, min(32, c_hi - cb), v);
+            if (nk > 0) {
+                dg_ld(trow + (uint32_t)cb, min(32, c_hi - cb), v);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
             if (!valid) continue;
 #pragma unroll
             for (int j = 0; j < 32; j += 8)

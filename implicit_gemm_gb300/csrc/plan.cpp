@@ -619,6 +619,37 @@ std::string plan_string(const Plan& pl)
     return buf;
 }
 
+namespace {
+
+// Phases of one spatial dim of the backward-data problem (see DgDim).
+bool dg_dim(int in, int F, int s, int dil, int pl, DgDim* o, int* span)
+{
+    if (s > kDgMaxPhases || F > kDgMaxTaps) return false;
+    std::memset(o, 0, sizeof *o);
+    o->nph = s;
+    *span = 0;
+    for (int r = 0; r < s; ++r) {
+        o->J[r] = in > r ? (int)cdiv(in - r, s) : 0;
+        int qmin = 0, qmax = 0, n = 0;
+        int q[kDgMaxTaps];
+        for (int t = 0; t < F; ++t) {
+            const int v = r + pl - t * dil;
+            if (((v % s) + s) % s) continue;
+            q[t] = (v - ((v % s) + s) % s) / s;  // exact: v is a multiple of s
+            if (n == 0 || q[t] < qmin) qmin = q[t];
+            if (n == 0 || q[t] > qmax) qmax = q[t];
+            o->tap[r][n++] = (unsigned char)t;
+        }
+        o->ntap[r] = n;
+        o->qmin[r] = qmin;
+        for (int i = 0; i < n; ++i) o->shift[r][i] = (unsigned char)(q[o->tap[r][i]] - qmin);
+        if (n) *span = std::max(*span, qmax - qmin);
+    }
+    return true;
+}
+
+}  // namespace
+
 int make_dgrad_plan(const wg_problem* p, const DeviceCaps& caps, DgPlan* pl, std::string* err)
 {
     std::memset(pl, 0, sizeof *pl);
@@ -626,9 +657,6 @@ int make_dgrad_plan(const wg_problem* p, const DeviceCaps& caps, DgPlan* pl, std
     if (st) return st;
     const Problem& pb = pl->pb;
     (void)caps;
-    for (int j = 0; j < 3; ++j)
-        if (pb.stride[j] != 1)
-            return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: strides above 1 are not supported");
     if (pb.C % 8) return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: C must be a multiple of 8 (16-byte W rows)");
     if (pb.G > 1 && pb.K % 8)
         return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: K must be a multiple of 8 when G > 1");
@@ -641,26 +669,38 @@ int make_dgrad_plan(const wg_problem* p, const DeviceCaps& caps, DgPlan* pl, std
     } else {
         d.bw = 8, d.bh = 16;
     }
-    const int X = pb.filt[2], Y = pb.filt[1], Z = pb.filt[0];
-    d.PW = d.bw + (X - 1) * pb.dil[2];
-    d.PH = d.bh + (Y - 1) * pb.dil[1];
+    int span[3];
+    for (int j = 0; j < 3; ++j) {
+        // dim[0] = w, dim[1] = h, dim[2] = d; the problem holds (D, H, W).
+        const int k = 2 - j;
+        if (!dg_dim(pb.in[k], pb.filt[k], pb.stride[k], pb.dil[k], pb.pad_l[k], &d.dim[j], &span[j]))
+            return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: stride above 8 or more than 32 taps along a dim");
+    }
+    d.PW = d.bw + span[0];
+    d.PH = d.bh + span[1];
     if (d.PW > 256 || d.PH > 256)
         return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: dilated filter too wide for a 256-row patch");
-    d.XY = X * Y;
+    int mx[3] = {0, 0, 0}, mJ[3] = {0, 0, 0};
+    for (int j = 0; j < 3; ++j)
+        for (int r = 0; r < d.dim[j].nph; ++r) {
+            mx[j] = std::max(mx[j], d.dim[j].ntap[r]);
+            mJ[j] = std::max(mJ[j], d.dim[j].J[r]);
+        }
+    d.max_yx = std::max(1, mx[0] * mx[1]);
     d.patch_bytes = round_up(d.PW * d.PH * 128, 1024);
     d.n_kc = (int)cdiv(pb.K, 64);
     // N-tile and taps per stage: the widest N-tile (up to 256 channels) with
-    // every tap of a plane in one stage and two stages in shared memory; else
-    // 64 channels and the plane's taps in groups.
+    // every (y, x) tap of a phase's plane in one stage and two stages in shared
+    // memory; else 64 channels and the taps in groups.
     const int avail = kMaxSmemPerCta - 2048;
     const int cmax = round_up(pb.C, 16);
     d.Nt = 0;
     for (int nt = 256; nt >= 16; nt /= 2) {
         if (nt > cmax && nt > 16) continue;
         const int na = (int)cdiv(nt, 64);
-        if (2 * (d.patch_bytes + d.XY * na * 8192) <= avail) {
+        if (2 * (d.patch_bytes + d.max_yx * na * 8192) <= avail) {
             d.Nt = nt;
-            d.TG = d.XY;
+            d.TG = d.max_yx;
             break;
         }
     }
@@ -671,15 +711,15 @@ int make_dgrad_plan(const wg_problem* p, const DeviceCaps& caps, DgPlan* pl, std
     }
     d.n_catoms = (int)cdiv(d.Nt, 64);
     d.n_ctiles = (int)cdiv(pb.C, d.Nt);
-    d.n_tg = (int)cdiv(d.XY, d.TG);
     d.stage_bytes = d.patch_bytes + d.TG * d.n_catoms * 8192;
     d.stages = std::min(4, avail / d.stage_bytes);
     d.smem_bytes = d.stages * d.stage_bytes + 2048;
     d.tmem_cols = std::max(32, pow2_at_least(d.Nt));
-    d.n_tw = (int)cdiv(pb.in[2], d.bw);
-    d.n_th = (int)cdiv(pb.in[1], d.bh);
-    d.n_tiles = (long long)d.n_tw * d.n_th * pb.in[0] * pb.N;
-    d.n_iters = d.n_kc * Z * d.n_tg;
+    d.n_tw = (int)cdiv(std::max(1, mJ[0]), d.bw);
+    d.n_th = (int)cdiv(std::max(1, mJ[1]), d.bh);
+    d.n_td = std::max(1, mJ[2]);
+    d.n_phases = d.dim[0].nph * d.dim[1].nph * d.dim[2].nph;
+    d.n_tiles = (long long)d.n_phases * d.n_tw * d.n_th * d.n_td * pb.N;
     if (d.n_tiles > (1ll << 31) - 1) return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: too many pixel tiles");
     d.grid[0] = (unsigned)d.n_tiles;
     d.grid[1] = (unsigned)d.n_ctiles;
@@ -692,10 +732,10 @@ std::string dgrad_plan_string(const DgPlan& d)
 {
     char buf[512];
     snprintf(buf, sizeof buf,
-             "kernel=dgrad_tcgen05 box=(w%d,h%d) patch=(w%d,h%d) Nt=%d catoms=%d ctiles=%d kchunks=%d taps/plane=%d "
-             "taps/stage=%d stages/tile=%d patch_bytes=%d stage_bytes=%d ring=%d smem=%d tmem_cols=%d "
+             "kernel=dgrad_tcgen05 phases=%d box=(w%d,h%d) patch=(w%d,h%d) Nt=%d catoms=%d ctiles=%d kchunks=%d "
+             "max_yx_taps=%d taps/stage=%d patch_bytes=%d stage_bytes=%d ring=%d smem=%d tmem_cols=%d "
              "grid=(%u,%u,%u) block=%u",
-             d.bw, d.bh, d.PW, d.PH, d.Nt, d.n_catoms, d.n_ctiles, d.n_kc, d.XY, d.TG, d.n_iters, d.patch_bytes,
+             d.n_phases, d.bw, d.bh, d.PW, d.PH, d.Nt, d.n_catoms, d.n_ctiles, d.n_kc, d.max_yx, d.TG, d.patch_bytes,
              d.stage_bytes, d.stages, d.smem_bytes, d.tmem_cols, d.grid[0], d.grid[1], d.grid[2], d.block);
     return buf;
 }

@@ -134,18 +134,36 @@ std::string plan_string(const Plan& pl);
 // problems), an N-tile of C and one group; it walks (K chunk of 64, filter
 // plane z, tap group) stages, each a dY halo patch (one row-shifted view per
 // tap) plus the W tiles of the group's taps.
+// Strides: the input positions of one dim split into `stride` phases
+// i = r + stride * j.  In phase r only the taps t with (r + pad_l - t*dil)
+// divisible by the stride contribute, each reading dY at j + q_t,
+// q_t = (r + pad_l - t*dil) / stride; per phase the taps are listed with their
+// row shift q_t - min q.  Stride 1 is the single phase r = 0 with every tap.
+constexpr int kDgMaxPhases = 8;
+constexpr int kDgMaxTaps = 32;
+struct DgDim {
+    int nph;                                          // phases (= stride)
+    int J[kDgMaxPhases];                              // positions in each phase
+    int qmin[kDgMaxPhases];                           // dY offset of the phase's first patch row
+    int ntap[kDgMaxPhases];                           // contributing taps
+    unsigned char tap[kDgMaxPhases][kDgMaxTaps];      // their filter index
+    unsigned char shift[kDgMaxPhases][kDgMaxTaps];    // their row shift in the patch
+};
+
 struct DgPlan {
     Problem pb;
-    int bw, bh;           // pixel box along (w, h)
+    int bw, bh;           // pixel box along (w, h), in phase positions
     int PW, PH;           // dY patch extent along (w, h)
     int Nt, n_catoms, n_ctiles;
     int n_kc;             // 64-channel chunks of K
-    int XY, TG, n_tg;     // taps per filter plane, taps per stage, tap groups per plane
+    int TG;               // taps per stage (of one plane's (y, x) taps)
+    int max_yx;           // most (y, x) taps of any phase
     int patch_bytes;      // dY patch bytes (1024-aligned)
     int stage_bytes, stages, smem_bytes, tmem_cols;
-    int n_tw, n_th;       // boxes along w and h
-    long long n_tiles;    // n_tw * n_th * D * N
-    int n_iters;          // n_kc * Z * n_tg stages per tile
+    int n_tw, n_th, n_td; // boxes along w and h, depth positions, per phase (the largest phase)
+    int n_phases;         // nph_w * nph_h * nph_d
+    long long n_tiles;    // n_phases * n_tw * n_th * n_td * N
+    DgDim dim[3];         // (w, h, d)
     unsigned grid[3];
     unsigned block;
 };

@@ -728,15 +728,13 @@ int prepare_dgrad(const wg::DgPlan& d, const void* dy, const void* w, void* dx, 
     wg::DgParams& q = out->prm;
     memset(&q, 0, sizeof q);
     q.G = pb.G, q.C = pb.C, q.K = pb.K;
-    q.X = pb.filt[2], q.Y = pb.filt[1], q.Z = pb.filt[0], q.XY = d.XY;
-    q.dw = pb.dil[2], q.dh = pb.dil[1], q.dd = pb.dil[0];
-    q.plw = pb.pad_l[2], q.plh = pb.pad_l[1], q.pld = pb.pad_l[0];
+    q.X = pb.filt[2], q.Y = pb.filt[1];
     q.Wi = pb.in[2], q.Hi = pb.in[1], q.Di = pb.in[0];
     q.bw = d.bw, q.bh = d.bh, q.PW = d.PW, q.PH = d.PH;
-    q.Nt = d.Nt, q.n_catoms = d.n_catoms;
-    q.n_kc = d.n_kc, q.TG = d.TG, q.n_tg = d.n_tg, q.n_iters = d.n_iters;
-    q.n_tw = d.n_tw, q.n_th = d.n_th;
+    q.Nt = d.Nt, q.n_catoms = d.n_catoms, q.n_kc = d.n_kc, q.TG = d.TG;
+    q.n_tw = d.n_tw, q.n_th = d.n_th, q.n_td = d.n_td;
     q.patch_bytes = d.patch_bytes, q.stage_bytes = d.stage_bytes, q.stages = d.stages, q.tmem_cols = d.tmem_cols;
+    for (int j = 0; j < 3; ++j) q.dim[j] = d.dim[j];
     q.idesc = wg::make_idesc_f16(pb.in_dtype == WG_BF16, false, true, 128, d.Nt);
     q.out_dtype = pb.out_dtype;
     q.out = dx;

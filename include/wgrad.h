@@ -215,8 +215,10 @@ WG_API int wg_set_mark_event(void* event);
  *  dy: N(Do)(Ho)WoGK, w: GK(Z)(Y)XC (in_dtype), dx: N(D)(H)WGC (out_dtype),
  *      device pointers, 16-byte aligned, owned by the caller.  dX is
  *      overwritten (every element is written once; no workspace).
- * Supported: stride 1 in every dimension, any dilation and pads, C a multiple
- * of 8, K a multiple of 8 when G > 1; otherwise WG_ERR_NOT_SUPPORTED.
+ * Supported: strides up to 8, any dilation and pads, up to 32 taps per
+ * dimension, C a multiple of 8, K a multiple of 8 when G > 1; otherwise
+ * WG_ERR_NOT_SUPPORTED.  Input positions that no (output position, tap) pair
+ * reaches (a stride larger than the dilated filter) get 0.
  * Returns WG_OK or an error status; nothing is launched on an error.  The
  * kernel runs on `stream` (a cudaStream_t). */
 WG_API int wg_conv_bwd_data(const wg_problem* p, const void* dy, const void* w, void* dx, void* stream);

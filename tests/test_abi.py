@@ -186,7 +186,8 @@ def test_dgrad_plans_and_limits():
     assert "kernel=dgrad_tcgen05" in ps and "box=(w8,h16)" in ps
     one_d = spec(1, 1, 2, 16, 24, [300], [5], [1], [2], [4], [4])
     assert "box=(w128,h1)" in binding.wg_bwd_data_plan_string(one_d)
-    for bad, status in ((spec(2, 1, 1, 16, 16, [9, 9], [3, 3], [2, 2]), 2),      # stride 2
+    assert "phases=4 " in binding.wg_bwd_data_plan_string(spec(2, 1, 1, 16, 16, [9, 9], [3, 3], [2, 2]))
+    for bad, status in ((spec(2, 1, 1, 16, 16, [40, 9], [3, 3], [9, 1]), 2),     # stride above 8
                         (spec(2, 2, 1, 4, 8, [9, 9], [3, 3]), 2),                # C not a multiple of 8
                         (spec(2, 1, 1, 0, 8, [9, 9], [3, 3]), 1)):               # C = 0
         with pytest.raises(binding.WgradError) as e:

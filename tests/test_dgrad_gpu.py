@@ -5,7 +5,10 @@ by element, through the C ABI.
   below, at and above one 64-channel chunk, filters whose taps do not all fit
   one stage, 16-bit outputs and both input dtypes;
 * integer-valued inputs: the result must equal the oracle bit for bit;
-* the 56x56, C = K = 64 shape of the dense weight-gradient workload at full size;
+* strides (each dim's positions split into phases with their own taps), including
+  phases no tap reaches, which must come out zero;
+* the 56x56, C = K = 64 and 3-D stride-2 shapes of the weight-gradient workloads at
+  full size;
 * dX pre-filled with NaN must come back fully written.
 """
 import numpy as np
@@ -67,6 +70,15 @@ SMALL = [
     spec(2, 1, 2, 24, 16, [9, 10], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], in_dtype="fp16", out_dtype="fp16"),
     spec(2, 1, 1, 64, 256, [12, 12], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
     spec(2, 1, 2, 256, 64, [9, 8], [1, 1]),
+    # strides: phases with different tap lists, strides beyond the filter
+    # (phases no tap reaches must come out zero), stride with dilation, 1-D, 3-D
+    spec(2, 1, 2, 16, 32, [13, 11], [3, 3], [2, 2], [1, 1], [1, 1], [1, 1]),
+    spec(2, 1, 2, 64, 48, [14, 15], [1, 1], [2, 2]),
+    spec(2, 2, 1, 8, 16, [10, 9], [3, 2], [2, 1], [1, 2], [0, 1], [2, 0]),
+    spec(2, 1, 1, 16, 16, [11, 10], [1, 2], [3, 3], [1, 1], [0, 0], [0, 0]),
+    spec(2, 1, 2, 24, 8, [12, 12], [3, 3], [2, 2], [2, 2], [2, 1], [1, 2], in_dtype="fp16", out_dtype="fp16"),
+    spec(1, 1, 2, 16, 24, [100], [5], [3], [2], [4], [1]),
+    spec(3, 1, 2, 16, 16, [7, 8, 9], [3, 3, 3], [2, 2, 2], [1, 1, 1], [1, 1, 1], [1, 1, 1]),
 ]
 
 
@@ -84,7 +96,7 @@ def test_dgrad_small(sp):
     assert_close(got, dx, A, sp["out_dtype"], _ids(sp))
 
 
-@pytest.mark.parametrize("sp", [SMALL[i] for i in (0, 3, 4, 5, 7, 10, 12)], ids=_ids)
+@pytest.mark.parametrize("sp", [SMALL[i] for i in (0, 3, 4, 5, 7, 10, 12, 14, 16, 17, 19, 20)], ids=_ids)
 def test_dgrad_integer_bitwise(sp):
     sp = dict(sp, out_dtype="fp32")
     _, dy = make_inputs(sp, ("int", -2, 2), 311, 312)
@@ -109,3 +121,14 @@ def test_dgrad_repeats_bitwise():
     w = _w_bits(sp, ("uniform", -1.0, 1.0), 333)
     a, b = run_gpu(sp, dy, w), run_gpu(sp, dy, w)
     assert np.array_equal(a.view(np.int64), b.view(np.int64))
+
+
+def test_dgrad_3d_stride2_full():
+    # The geometry of the 3-D weight-gradient workload (16^3, C 128, K 96, stride 2).
+    sp = spec(3, 1, 4, 128, 96, [16, 16, 16], [3, 3, 3], [2, 2, 2], [1, 1, 1], [1, 1, 1], [1, 1, 1],
+              in_dtype="fp16", out_dtype="fp32")
+    _, dy = make_inputs(sp, ("normal", 0.0, 0.5), 341, 342)
+    w = _w_bits(sp, ("normal", 0.0, 0.5), 343)
+    dx, A = ref(sp, dy, w)
+    got = run_gpu(sp, dy, w)
+    assert_close(got, dx, A, sp["out_dtype"], "dgrad 3-D stride 2")

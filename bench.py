@@ -334,7 +334,9 @@ class DgradWorkload:
         need = -(-2 * L2_BYTES // (2 * s["ndy"]))
         self.copies = max(2, need) if need <= MAX_COPIES else 1
         self.dys = [self.dy] + [self.dy.clone() for _ in range(self.copies - 1)]
-        self.calls = [binding.PreparedDgradCall(sp, d, self.w, self.dx) for d in self.dys]
+        nb = binding.wg_bwd_data_workspace_size(sp)
+        self.ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
+        self.calls = [binding.PreparedDgradCall(sp, d, self.w, self.dx, self.ws, nb) for d in self.dys]
         self.next = 0
         self.rotating = self.copies > 1
         self.graph = None

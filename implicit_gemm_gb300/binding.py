@@ -44,7 +44,7 @@ class WgradError(RuntimeError):
 
 EXPORTS = ("wg_problem_normalize", "wg_workspace_size", "wg_conv_bwd_weight", "wg_check_status",
            "wg_plan_string", "wg_status_string", "wg_last_error", "wg_conv_bwd_weight_noalloc",
-           "wg_set_mark_event", "wg_conv_bwd_data", "wg_bwd_data_plan_string")
+           "wg_set_mark_event", "wg_conv_bwd_data", "wg_bwd_data_plan_string", "wg_bwd_data_workspace_size")
 
 _lib = None
 _lock = threading.Lock()
@@ -72,7 +72,9 @@ def load():
                                                        ctypes.c_void_p]
             lib.wg_check_status.argtypes = [ctypes.c_void_p]
             lib.wg_set_mark_event.argtypes = [ctypes.c_void_p]
-            lib.wg_conv_bwd_data.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+            lib.wg_conv_bwd_data.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_size_t, ctypes.c_void_p]
+            lib.wg_bwd_data_workspace_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
             lib.wg_bwd_data_plan_string.argtypes = [P, ctypes.c_char_p, ctypes.c_size_t]
             lib.wg_plan_string.argtypes = [P, O, ctypes.c_char_p, ctypes.c_size_t]
             lib.wg_status_string.argtypes = [ctypes.c_int]
@@ -186,10 +188,19 @@ def wg_conv_bwd_weight_noalloc(spec: dict, x, dy, dw, split_k: int = 0, mode: st
                                              _stream_handle(stream)))
 
 
-def wg_conv_bwd_data(spec: dict, dy, w, dx, stream=None) -> None:
+def wg_conv_bwd_data(spec: dict, dy, w, dx, workspace=None, ws_bytes: int | None = None, stream=None) -> None:
     """Backward-data: dX (spec's out_dtype) from dY and W (spec's in_dtype); see include/wgrad.h."""
     p = make_problem(spec)
-    _check(load().wg_conv_bwd_data(ctypes.byref(p), _addr(dy), _addr(w), _addr(dx), _stream_handle(stream)))
+    if ws_bytes is None:
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().wg_conv_bwd_data(ctypes.byref(p), _addr(dy), _addr(w), _addr(dx), _addr(workspace), int(ws_bytes),
+                                   _stream_handle(stream)))
+
+
+def wg_bwd_data_workspace_size(spec: dict) -> int:
+    p, n = make_problem(spec), ctypes.c_size_t(0)
+    _check(load().wg_bwd_data_workspace_size(ctypes.byref(p), ctypes.byref(n)))
+    return int(n.value)
 
 
 def wg_bwd_data_plan_string(spec: dict) -> str:
@@ -202,12 +213,12 @@ def wg_bwd_data_plan_string(spec: dict) -> str:
 class PreparedDgradCall:
     """wg_conv_bwd_data with its arguments marshalled once."""
 
-    def __init__(self, spec: dict, dy, w, dx):
-        self._keep = (dy, w, dx)
+    def __init__(self, spec: dict, dy, w, dx, workspace=None, ws_bytes: int = 0):
+        self._keep = (dy, w, dx, workspace)
         self.p = make_problem(spec)
         self.fn = load().wg_conv_bwd_data
         self.args = (ctypes.byref(self.p), ctypes.c_void_p(_addr(dy)), ctypes.c_void_p(_addr(w)),
-                     ctypes.c_void_p(_addr(dx)))
+                     ctypes.c_void_p(_addr(dx)), ctypes.c_void_p(_addr(workspace)), ctypes.c_size_t(int(ws_bytes)))
 
     def __call__(self, stream_handle: int | None = None) -> None:
         st = self.fn(*self.args, stream_handle)
@@ -222,7 +233,9 @@ def conv_bwd_data(spec: dict, dy, w, out=None, stream=None):
     tdt = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}[spec.get("out_dtype", "fp32")]
     if out is None:
         out = torch.empty((spec["N"], *spec["in"], spec["G"], spec["C"]), dtype=tdt, device=dy.device)
-    wg_conv_bwd_data(spec, dy, w, out, stream)
+    nbytes = wg_bwd_data_workspace_size(spec)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dy.device) if nbytes else None
+    wg_conv_bwd_data(spec, dy, w, out, ws, nbytes, stream)
     return out
 
 

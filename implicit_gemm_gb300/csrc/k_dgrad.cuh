@@ -36,7 +36,9 @@
 namespace wg {
 
 struct DgParams {
-    int G, C, K, X, Y;
+    int G, C, K, X, Y;  // groups, channels as the kernel sees them (folded: G blocks of C and K)
+    int ch_pix;         // channels of one dX pixel (all groups)
+    int ch_lim;         // channel bound of a block's stores (the real G*C)
     int Wi, Hi, Di;     // dX extents
     int bw, bh, PW, PH;
     int Nt, n_catoms, n_kc, TG;
@@ -91,6 +93,31 @@ __device__ __forceinline__ void dg_ld(uint32_t taddr, int n, float (&v)[32])
     if (n > 16) reg_fence16(r + 16);
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = i < 16 || n > 16 ? __uint_as_float(r[i]) : 0.f;
+}
+
+// Block-diagonal copy of W for a group fold of Gm: for block b,
+//   We[b][k'][t][c'] = W[b*Gm + k'/K][k' % K][t][c' % C] where k'/K == c'/C and
+//                      that group exists, else 0
+// (16-bit words copied as they are).
+__global__ void __launch_bounds__(256)
+    dgrad_fold_w_kernel(const uint16_t* __restrict__ w, uint16_t* __restrict__ we, int G, int K, int C, int T, int Gm,
+                        long long n)
+{
+    const int Km = Gm * K, Cm = Gm * C;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        long long r = i;
+        const int cp = (int)(r % Cm);
+        r /= Cm;
+        const int t = (int)(r % T);
+        r /= T;
+        const int kp = (int)(r % Km);
+        const long long b = r / Km;
+        const int gl = kp / K;
+        const long long g = b * Gm + gl;
+        uint16_t v = 0;
+        if (cp / C == gl && g < G) v = w[((g * K + kp % K) * T + t) * C + cp % C];
+        we[i] = v;
+    }
 }
 
 __global__ void __launch_bounds__(kDgThreads, 1)
@@ -233,7 +260,8 @@ __global__ void __launch_bounds__(kDgThreads, 1)
         const bool valid = jw < DW.J[pw] && jh < DH.J[ph] && td < DD.J[pd];
         const int w = pw + DW.nph * jw, h = ph + DH.nph * jh, di = pd + DD.nph * td;
         const long long pix = (((long long)n * p.Di + di) * p.Hi + h) * p.Wi + w;
-        const long long obase = (pix * p.G + g) * p.C + c0;
+        const long long obase = pix * p.ch_pix + (long long)g * p.C + c0;
+        const int cblk = g * p.C + c0;  // this tile's first channel in the pixel
         const int Nt = p.Nt;
         const int c_mid = ((Nt >> 1) + 31) & ~31;
         const int c_lo = warp < 4 ? 0 : c_mid, c_hi = warp < 4 ? min(c_mid, Nt) : Nt;
@@ -249,7 +277,8 @@ __global__ void __launch_bounds__(kDgThreads, 1)
             if (!valid) continue;
 #pragma unroll
             for (int j = 0; j < 32; j += 8)
-                if (cb + j < c_hi && c0 + cb + j < p.C) store8(p.out, obase + cb + j, v + j, p.out_dtype);
+                if (cb + j < c_hi && c0 + cb + j < p.C && cblk + cb + j < p.ch_lim)
+                    store8(p.out, obase + cb + j, v + j, p.out_dtype);
         }
     }
     tc_fence_before();

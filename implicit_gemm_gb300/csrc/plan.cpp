@@ -657,13 +657,27 @@ int make_dgrad_plan(const wg_problem* p, const DeviceCaps& caps, DgPlan* pl, std
     if (st) return st;
     const Problem& pb = pl->pb;
     (void)caps;
-    if (pb.C % 8) return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: C must be a multiple of 8 (16-byte W rows)");
-    if (pb.G > 1 && pb.K % 8)
-        return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: K must be a multiple of 8 when G > 1");
-    if (((long long)pb.G * pb.K) % 8)
-        return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: G*K must be a multiple of 8 (16-byte dY rows)");
-    if (pb.G > 65535) return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: too many groups");
     DgPlan& d = *pl;
+    if (((long long)pb.G * pb.K) % 8 || ((long long)pb.G * pb.C) % 8)
+        return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: G*C and G*K must be multiples of 8 (16-byte pixel rows)");
+    // Group fold for small C and K: the widest Gm with Gm*C and Gm*K at most 64
+    // and multiples of 8 (16-byte rows of the folded W and aligned dY windows).
+    d.Gm = 1;
+    for (int g = std::min(pb.G, 64); g >= 2; --g)
+        if (g * pb.C <= 64 && g * pb.K <= 64 && (g * pb.C) % 8 == 0 && (g * pb.K) % 8 == 0) {
+            d.Gm = g;
+            break;
+        }
+    if (d.Gm == 1) {
+        if (pb.C % 8) return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: C must be a multiple of 8 (16-byte W rows)");
+        if (pb.G > 1 && pb.K % 8)
+            return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: K must be a multiple of 8 when G > 1");
+    }
+    d.Gb = (int)cdiv(pb.G, d.Gm);
+    d.Cm = d.Gm * pb.C;
+    d.Km = d.Gm * pb.K;
+    d.ws_bytes = d.Gm > 1 ? (size_t)d.Gb * d.Km * (size_t)pb.T * d.Cm * 2 : 0;
+    if (d.Gb > 65535) return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: too many groups");
     if (pb.ndim == 1) {
         d.bw = 128, d.bh = 1;
     } else {
@@ -688,12 +702,12 @@ int make_dgrad_plan(const wg_problem* p, const DeviceCaps& caps, DgPlan* pl, std
         }
     d.max_yx = std::max(1, mx[0] * mx[1]);
     d.patch_bytes = round_up(d.PW * d.PH * 128, 1024);
-    d.n_kc = (int)cdiv(pb.K, 64);
+    d.n_kc = (int)cdiv(d.Km, 64);
     // N-tile and taps per stage: the widest N-tile (up to 256 channels) with
     // every (y, x) tap of a phase's plane in one stage and two stages in shared
     // memory; else 64 channels and the taps in groups.
     const int avail = kMaxSmemPerCta - 2048;
-    const int cmax = round_up(pb.C, 16);
+    const int cmax = round_up(d.Cm, 16);
     d.Nt = 0;
     for (int nt = 256; nt >= 16; nt /= 2) {
         if (nt > cmax && nt > 16) continue;
@@ -710,9 +724,15 @@ int make_dgrad_plan(const wg_problem* p, const DeviceCaps& caps, DgPlan* pl, std
         if (d.TG < 1) return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: the dY patch does not fit shared memory");
     }
     d.n_catoms = (int)cdiv(d.Nt, 64);
-    d.n_ctiles = (int)cdiv(pb.C, d.Nt);
+    d.n_ctiles = (int)cdiv(d.Cm, d.Nt);
     d.stage_bytes = d.patch_bytes + d.TG * d.n_catoms * 8192;
-    d.stages = std::min(4, avail / d.stage_bytes);
+    // Ring depth: up to 4, but no deeper than the stages a tile has -- with a
+    // single stage per tile (K <= 64, one plane, every tap in one group) a
+    // one-deep ring lets two CTAs share an SM and overlap their tiles.
+    int max_nz = 0;
+    for (int r = 0; r < d.dim[2].nph; ++r) max_nz = std::max(max_nz, d.dim[2].ntap[r]);
+    const long long iters = (long long)d.n_kc * std::max(1, max_nz) * cdiv(d.max_yx, d.TG);
+    d.stages = (int)std::min<long long>(std::min(4, avail / d.stage_bytes), std::max(1LL, iters));
     d.smem_bytes = d.stages * d.stage_bytes + 2048;
     d.tmem_cols = std::max(32, pow2_at_least(d.Nt));
     d.n_tw = (int)cdiv(std::max(1, mJ[0]), d.bw);
@@ -723,7 +743,7 @@ int make_dgrad_plan(const wg_problem* p, const DeviceCaps& caps, DgPlan* pl, std
     if (d.n_tiles > (1ll << 31) - 1) return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: too many pixel tiles");
     d.grid[0] = (unsigned)d.n_tiles;
     d.grid[1] = (unsigned)d.n_ctiles;
-    d.grid[2] = (unsigned)pb.G;
+    d.grid[2] = (unsigned)d.Gb;
     d.block = 256;
     return WG_OK;
 }
@@ -732,11 +752,12 @@ std::string dgrad_plan_string(const DgPlan& d)
 {
     char buf[512];
     snprintf(buf, sizeof buf,
-             "kernel=dgrad_tcgen05 phases=%d box=(w%d,h%d) patch=(w%d,h%d) Nt=%d catoms=%d ctiles=%d kchunks=%d "
-             "max_yx_taps=%d taps/stage=%d patch_bytes=%d stage_bytes=%d ring=%d smem=%d tmem_cols=%d "
-             "grid=(%u,%u,%u) block=%u",
-             d.n_phases, d.bw, d.bh, d.PW, d.PH, d.Nt, d.n_catoms, d.n_ctiles, d.n_kc, d.max_yx, d.TG, d.patch_bytes,
-             d.stage_bytes, d.stages, d.smem_bytes, d.tmem_cols, d.grid[0], d.grid[1], d.grid[2], d.block);
+             "kernel=dgrad_tcgen05 Gm=%d phases=%d box=(w%d,h%d) patch=(w%d,h%d) Nt=%d catoms=%d ctiles=%d "
+             "kchunks=%d max_yx_taps=%d taps/stage=%d patch_bytes=%d stage_bytes=%d ring=%d smem=%d tmem_cols=%d "
+             "grid=(%u,%u,%u) block=%u ws=%zu",
+             d.Gm, d.n_phases, d.bw, d.bh, d.PW, d.PH, d.Nt, d.n_catoms, d.n_ctiles, d.n_kc, d.max_yx, d.TG, d.patch_bytes,
+             d.stage_bytes, d.stages, d.smem_bytes, d.tmem_cols, d.grid[0], d.grid[1], d.grid[2], d.block,
+             d.ws_bytes);
     return buf;
 }
 

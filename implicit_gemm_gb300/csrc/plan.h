@@ -152,6 +152,12 @@ struct DgDim {
 
 struct DgPlan {
     Problem pb;
+    // Group fold: Gm groups with small C and K share one tile; the kernel sees
+    // Gb = ceil(G / Gm) "groups" of Cm = Gm*C and Km = Gm*K channels and reads
+    // a block-diagonal copy of W (zero between different groups), written into
+    // the workspace by an expansion kernel.  Gm = 1: W is read as it is.
+    int Gm, Gb, Cm, Km;
+    size_t ws_bytes;      // the block-diagonal W (0 when Gm = 1)
     int bw, bh;           // pixel box along (w, h), in phase positions
     int PW, PH;           // dY patch extent along (w, h)
     int Nt, n_catoms, n_ctiles;

@@ -704,7 +704,7 @@ int dgrad_plan_for(const wg_problem* p, wg::DgPlan* pl, std::string* key_out)
     return WG_OK;
 }
 
-int prepare_dgrad(const wg::DgPlan& d, const void* dy, const void* w, void* dx, DgPrepared* out)
+int prepare_dgrad(const wg::DgPlan& d, const void* dy, const void* w, void* dx, void* wexp, DgPrepared* out)
 {
     const wg::Problem& pb = d.pb;
     {
@@ -717,17 +717,19 @@ int prepare_dgrad(const wg::DgPlan& d, const void* dy, const void* w, void* dx, 
         if (st) return st;
     }
     {
-        // W viewed as (C, taps, K, G): k beyond the group's K is out of bounds and reads zero.
-        const cuuint64_t dims[5] = {(cuuint64_t)pb.C, (cuuint64_t)pb.T, (cuuint64_t)pb.K, (cuuint64_t)pb.G, 1};
+        // W (or its block-diagonal fold) viewed as (C, taps, K, G): k beyond the
+        // group's K is out of bounds and reads zero.
+        const cuuint64_t dims[5] = {(cuuint64_t)d.Cm, (cuuint64_t)pb.T, (cuuint64_t)d.Km, (cuuint64_t)d.Gb, 1};
         const cuuint32_t box[5] = {64, 1, 64, 1, 1};
         const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-        const int st = encode(&out->tmw, pb.in_dtype, const_cast<void*>(w), dims, box, estr, CU_TENSOR_MAP_SWIZZLE_128B,
-                              "W");
+        const int st = encode(&out->tmw, pb.in_dtype, d.Gm > 1 ? wexp : const_cast<void*>(w), dims, box, estr,
+                              CU_TENSOR_MAP_SWIZZLE_128B, "W");
         if (st) return st;
     }
     wg::DgParams& q = out->prm;
     memset(&q, 0, sizeof q);
-    q.G = pb.G, q.C = pb.C, q.K = pb.K;
+    q.G = d.Gb, q.C = d.Cm, q.K = d.Km;
+    q.ch_pix = pb.G * pb.C, q.ch_lim = pb.G * pb.C;
     q.X = pb.filt[2], q.Y = pb.filt[1];
     q.Wi = pb.in[2], q.Hi = pb.in[1], q.Di = pb.in[0];
     q.bw = d.bw, q.bh = d.bh, q.PW = d.PW, q.PH = d.PH;
@@ -763,7 +765,19 @@ int wg_bwd_data_plan_string(const wg_problem* p, char* buf, size_t n)
     return WG_OK;
 }
 
-int wg_conv_bwd_data(const wg_problem* p, const void* dy, const void* w, void* dx, void* stream)
+int wg_bwd_data_workspace_size(const wg_problem* p, size_t* bytes)
+{
+    if (!bytes) return set_err(WG_ERR_INVALID_ARGUMENT, "bytes is NULL");
+    wg::DgPlan d;
+    std::string key;
+    const int st = dgrad_plan_for(p, &d, &key);
+    if (st) return st;
+    *bytes = d.ws_bytes;
+    return WG_OK;
+}
+
+int wg_conv_bwd_data(const wg_problem* p, const void* dy, const void* w, void* dx, void* workspace, size_t ws_bytes,
+                     void* stream)
 {
     wg::DgPlan d;
     std::string pkey;
@@ -772,7 +786,17 @@ int wg_conv_bwd_data(const wg_problem* p, const void* dy, const void* w, void* d
     if (!dy || !w || !dx) return set_err(WG_ERR_INVALID_ARGUMENT, "dy, w and dx must be non-NULL device pointers");
     if (!aligned16(dy) || !aligned16(w) || !aligned16(dx))
         return set_err(WG_ERR_MISALIGNED, "dy, w and dx must be 16-byte aligned");
-    const std::string key = prep_key(pkey, dy, w, dx, nullptr);
+    if (d.ws_bytes > 0) {
+        if (!workspace || ws_bytes < d.ws_bytes) {
+            char buf[160];
+            snprintf(buf, sizeof buf, "workspace of %zu bytes needed (got %zu%s)", d.ws_bytes, ws_bytes,
+                     workspace ? "" : ", NULL");
+            return set_err(WG_ERR_WORKSPACE, buf);
+        }
+        if (!aligned16(workspace)) return set_err(WG_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    }
+    void* wexp = d.ws_bytes > 0 ? workspace : nullptr;
+    const std::string key = prep_key(pkey, dy, w, dx, wexp);
     DgPrepared pr;
     bool hit = false;
     {
@@ -781,7 +805,7 @@ int wg_conv_bwd_data(const wg_problem* p, const void* dy, const void* w, void* d
         if (it != dg_cache().end()) pr = it->second, hit = true;
     }
     if (!hit) {
-        st = prepare_dgrad(d, dy, w, dx, &pr);
+        st = prepare_dgrad(d, dy, w, dx, wexp, &pr);
         if (st) return st;
         std::lock_guard<std::mutex> lk(g_dg_mu);
         if (dg_cache().size() > 4096) dg_cache().clear();
@@ -790,8 +814,18 @@ int wg_conv_bwd_data(const wg_problem* p, const void* dy, const void* w, void* d
     st = ensure_smem(wg::dgrad_kernel, d.smem_bytes);
     if (st) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (d.Gm > 1) {
+        const wg::Problem& pb = d.pb;
+        const long long n = (long long)d.Gb * d.Km * pb.T * d.Cm;
+        const unsigned blocks = (unsigned)std::min<long long>((n + 255) / 256, 4096);
+        wg::dgrad_fold_w_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(w), static_cast<uint16_t*>(wexp),
+                                                       pb.G, pb.K, pb.C, (int)pb.T, d.Gm, n);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail("dgrad_fold_w_kernel launch", e);
+    }
     wg::dgrad_kernel<<<dim3(d.grid[0], d.grid[1], d.grid[2]), d.block, d.smem_bytes, s>>>(pr.tmy, pr.tmw, pr.prm);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail("dgrad_kernel launch", e);
     if (g_mark && (e = cudaEventRecord(g_mark, s)) != cudaSuccess) return cuda_fail("cudaEventRecord(mark)", e);
     return WG_OK;

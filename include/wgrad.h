@@ -214,14 +214,23 @@ WG_API int wg_set_mark_event(void* event);
  *      WG_BF16 or WG_FP16).
  *  dy: N(Do)(Ho)WoGK, w: GK(Z)(Y)XC (in_dtype), dx: N(D)(H)WGC (out_dtype),
  *      device pointers, 16-byte aligned, owned by the caller.  dX is
- *      overwritten (every element is written once; no workspace).
+ *      overwritten (every element is written once).
+ *  workspace / ws_bytes: at least wg_bwd_data_workspace_size bytes (may be NULL
+ *      when that is 0).  For small C and K several groups share one tile and the
+ *      kernel reads a block-diagonal copy of W that a first kernel writes here;
+ *      its contents need not be preserved between calls.
  * Supported: strides up to 8, any dilation and pads, up to 32 taps per
- * dimension, C a multiple of 8, K a multiple of 8 when G > 1; otherwise
- * WG_ERR_NOT_SUPPORTED.  Input positions that no (output position, tap) pair
- * reaches (a stride larger than the dilated filter) get 0.
+ * dimension, G*C and G*K multiples of 8, and without a group fold C a multiple
+ * of 8 and K a multiple of 8 when G > 1; otherwise WG_ERR_NOT_SUPPORTED.  Input
+ * positions that no (output position, tap) pair reaches (a stride larger than
+ * the dilated filter) get 0.
  * Returns WG_OK or an error status; nothing is launched on an error.  The
- * kernel runs on `stream` (a cudaStream_t). */
-WG_API int wg_conv_bwd_data(const wg_problem* p, const void* dy, const void* w, void* dx, void* stream);
+ * kernels run on `stream` (a cudaStream_t). */
+WG_API int wg_conv_bwd_data(const wg_problem* p, const void* dy, const void* w, void* dx, void* workspace,
+                            size_t ws_bytes, void* stream);
+
+/* Bytes of workspace wg_conv_bwd_data needs for p (0 when no group fold). */
+WG_API int wg_bwd_data_workspace_size(const wg_problem* p, size_t* bytes);
 
 /* Human-readable plan of wg_conv_bwd_data for p.  Host only. */
 WG_API int wg_bwd_data_plan_string(const wg_problem* p, char* buf, size_t n);

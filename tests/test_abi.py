@@ -188,11 +188,22 @@ def test_dgrad_plans_and_limits():
     assert "box=(w128,h1)" in binding.wg_bwd_data_plan_string(one_d)
     assert "phases=4 " in binding.wg_bwd_data_plan_string(spec(2, 1, 1, 16, 16, [9, 9], [3, 3], [2, 2]))
     for bad, status in ((spec(2, 1, 1, 16, 16, [40, 9], [3, 3], [9, 1]), 2),     # stride above 8
-                        (spec(2, 2, 1, 4, 8, [9, 9], [3, 3]), 2),                # C not a multiple of 8
+                        (spec(2, 1, 1, 4, 8, [9, 9], [3, 3]), 2),                # G*C not a multiple of 8
                         (spec(2, 1, 1, 0, 8, [9, 9], [3, 3]), 1)):               # C = 0
         with pytest.raises(binding.WgradError) as e:
             binding.wg_bwd_data_plan_string(bad)
         assert e.value.status == status
+
+
+def test_dgrad_group_fold():
+    # Small C and K: Gm groups share a tile through a block-diagonal copy of W in the workspace.
+    sp = WORKLOADS["2d_grouped_g32_c8_k8_n32_h28"][0]
+    ps = binding.wg_bwd_data_plan_string(sp)
+    assert " Gm=8 " in ps and "grid=(" in ps
+    assert binding.wg_bwd_data_workspace_size(sp) == 4 * 64 * 9 * 64 * 2
+    assert binding.wg_bwd_data_workspace_size(WORKLOADS["2d_dense_n32_h56_c64_k64"][0]) == 0
+    folded = spec(2, 2, 1, 4, 8, [9, 9], [3, 3])  # C = 4: supported only through the fold
+    assert " Gm=2 " in binding.wg_bwd_data_plan_string(folded)
 
 
 def test_dgrad_launch_checks_before_device(lib):

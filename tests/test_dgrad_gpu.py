@@ -79,6 +79,11 @@ SMALL = [
     spec(2, 1, 2, 24, 8, [12, 12], [3, 3], [2, 2], [2, 2], [2, 1], [1, 2], in_dtype="fp16", out_dtype="fp16"),
     spec(1, 1, 2, 16, 24, [100], [5], [3], [2], [4], [1]),
     spec(3, 1, 2, 16, 16, [7, 8, 9], [3, 3, 3], [2, 2, 2], [1, 1, 1], [1, 1, 1], [1, 1, 1]),
+    # group folds (block-diagonal W): full blocks, a partial last block, C = 4, strided
+    spec(2, 32, 2, 8, 8, [9, 10], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
+    spec(2, 12, 2, 8, 8, [7, 9], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], out_dtype="bf16"),
+    spec(2, 4, 2, 4, 12, [8, 7], [3, 2], [1, 1], [1, 1], [1, 0], [1, 1]),
+    spec(2, 16, 1, 8, 16, [11, 12], [3, 3], [2, 2], [1, 1], [1, 1], [1, 1]),
 ]
 
 
@@ -96,7 +101,8 @@ def test_dgrad_small(sp):
     assert_close(got, dx, A, sp["out_dtype"], _ids(sp))
 
 
-@pytest.mark.parametrize("sp", [SMALL[i] for i in (0, 3, 4, 5, 7, 10, 12, 14, 16, 17, 19, 20)], ids=_ids)
+@pytest.mark.parametrize("sp", [SMALL[i] for i in (0, 3, 4, 5, 7, 10, 12, 14, 16, 17, 19, 20, 21, 22, 23, 24)],
+                         ids=_ids)
 def test_dgrad_integer_bitwise(sp):
     sp = dict(sp, out_dtype="fp32")
     _, dy = make_inputs(sp, ("int", -2, 2), 311, 312)
@@ -132,3 +138,13 @@ def test_dgrad_3d_stride2_full():
     dx, A = ref(sp, dy, w)
     got = run_gpu(sp, dy, w)
     assert_close(got, dx, A, sp["out_dtype"], "dgrad 3-D stride 2")
+
+
+def test_dgrad_grouped_full():
+    # The geometry of the grouped weight-gradient workload (G 32, C = K = 8, 28x28).
+    sp = spec(2, 32, 32, 8, 8, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])
+    _, dy = make_inputs(sp, ("normal", 0.0, 1.0), 351, 352)
+    w = _w_bits(sp, ("normal", 0.0, 1.0), 353)
+    dx, A = ref(sp, dy, w)
+    got = run_gpu(sp, dy, w)
+    assert_close(got, dx, A, sp["out_dtype"], "dgrad grouped")

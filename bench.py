@@ -226,7 +226,12 @@ L2_BYTES = 129 * 1000 * 1000
 # DRAM bytes (read + write) of one launch of the workload's main kernel from an
 # ncu capture of the kernel as it now stands (summaries under profiles/); a
 # workload without such a capture reports null.
-TRAFFIC = {}
+TRAFFIC = {
+    # igemm_wgrad_kernel, plan S = 75, 3 M-tiles per CTA: 25,789,184 B read + 0 B written.
+    "2d_dense_n32_h56_c64_k64": 25_789_184,
+    # depthwise_wgrad_kernel<bf16, 2, sliding>: 103,019,520 B read + 3,580,928 B written.
+    "2d_depthwise_g512_n64_h28": 106_600_448,
+}
 MAX_COPIES = 512
 
 
@@ -454,6 +459,8 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=list(WORKLOADS))
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads and the CPU baseline")
     ap.add_argument("--graph", action="store_true", help="replay a CUDA graph of the call instead of calling it")
+    ap.add_argument("--dgrad", action="store_true",
+                    help="time backward-data on the workload's geometry instead of the weight gradient (no extras)")
     ap.add_argument("--sweep", action="store_true",
                     help="time the automatic plan against fixed merge widths on a depthwise shape sweep")
     args = ap.parse_args()
@@ -481,6 +488,13 @@ def main():
     if args.sweep:
         if rank == 0:
             run_sweep(torch, stream, flush, min(args.steps, 200), args.warmup)
+        return
+    if args.dgrad:
+        w3 = DgradWorkload(torch, args.workload)
+        ms = float(np.mean(time_steps(torch, w3, args.steps, args.warmup, flush, stream)))
+        if rank == 0:
+            print(json.dumps({"metric": "dgrad TFLOP/s", "value": w3.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                              "ms_per_step": ms, "config": {"workload": args.workload, "plan": w3.plan}}), flush=True)
         return
 
     wl = Workload(torch, args.workload)

@@ -175,6 +175,23 @@ def dist_setup():
     return ws, rank, local
 
 
+def max_over_ranks(dist, ms, device):
+    """The slowest rank's time (ms): every rank gets the same value.  `dist` is
+    torch.distributed with an initialised process group (NCCL on the GPUs; the
+    tests use gloo on the CPU), or None for a single process."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world_size, units_per_rank, ms):
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return world_size * units_per_rank / (ms * 1e-3)
+
+
 def run_reference(args, ws, rank):
     """Reference arm: the fp64 CPU oracle, as it stands, on this host's cores."""
     import oracle  # the one other place the bench runs the oracle
@@ -511,23 +528,16 @@ def main():
     t_wall = time.perf_counter() - t_wall
     clocks = sampler.stop()
     torch.cuda.synchronize()
-    step_ms = float(np.mean(times))
+    step_ms = max_over_ranks(pg, float(np.mean(times)), "cuda")
     if pg:
-        t = torch.tensor([step_ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        step_ms = float(t.item())
         pg.barrier()
     s = wl.s
-    value = ws * s["flops"] / (step_ms * 1e-3) / 1e12
+    value = job_value(ws, s["flops"], step_ms) / 1e12
 
     # End to end through the same C ABI call, host buffers: H2D of X and dY from
     # pinned memory, the call, D2H of dW, all inside the timed events.
     e2e_times = time_steps(torch, wl, max(20, args.steps // 10), args.warmup, flush, stream, e2e=True)
-    e2e_ms = float(np.mean(e2e_times))
-    if pg:
-        t = torch.tensor([e2e_ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(pg, float(np.mean(e2e_times)), "cuda")
 
     # Roofline of the dominant kernel (the call's main kernel: every FLOP of the
     # step and every algorithmic byte read or written goes through it): its
@@ -599,7 +609,7 @@ def main():
                            "l2": wl.l2_note() if not args.graph else "flushed before every timed step (graph mode)",
                            "parallelism": f"replicas x{ws}"},
                 "roofline": roof, "clocks": clocks, "gpu_launches": wl.launches_per_step * args.steps,
-                "e2e": {"value": ws * s["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "e2e": {"value": job_value(ws, s["flops"], e2e_ms) / 1e12, "unit": "TFLOP/s",
                         "h2d_bytes_per_step": 2 * (s["nx"] + s["ndy"]), "d2h_bytes_per_step": s["wsz"] * s["ndw"],
                         "ms_per_step": e2e_ms},
                 "wall_s_timed": t_wall, "workloads": extra}

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libwgrad.so")
 SOURCES = [os.path.join(CSRC, "wgrad.cu"), os.path.join(CSRC, "plan.cpp")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "k_igemm.cuh", "k_depthwise.cuh", "plan.h")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "k_igemm.cuh", "k_depthwise.cuh", "k_dgrad.cuh", "plan.h")] + [
     os.path.join(ROOT, "include", "wgrad.h")]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 _lock = threading.Lock()

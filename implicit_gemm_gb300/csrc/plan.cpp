@@ -656,7 +656,6 @@ int make_dgrad_plan(const wg_problem* p, const DeviceCaps& caps, DgPlan* pl, std
     int st = normalize(p, &pl->pb, err);
     if (st) return st;
     const Problem& pb = pl->pb;
-    (void)caps;
     DgPlan& d = *pl;
     if (((long long)pb.G * pb.K) % 8 || ((long long)pb.G * pb.C) % 8)
         return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: G*C and G*K must be multiples of 8 (16-byte pixel rows)");
@@ -703,13 +702,15 @@ int make_dgrad_plan(const wg_problem* p, const DeviceCaps& caps, DgPlan* pl, std
     d.max_yx = std::max(1, mx[0] * mx[1]);
     d.patch_bytes = round_up(d.PW * d.PH * 128, 1024);
     d.n_kc = (int)cdiv(d.Km, 64);
-    // N-tile and taps per stage: the widest N-tile (up to 256 channels) with
+    // N-tile and taps per stage: the widest N-tile (up to 128 channels) with
     // every (y, x) tap of a phase's plane in one stage and two stages in shared
     // memory; else 64 channels and the taps in groups.
-    const int avail = kMaxSmemPerCta - 2048;
+    const int avail = kMaxSmemPerCta - 2048 - kDgStaging;
     const int cmax = round_up(d.Cm, 16);
     d.Nt = 0;
-    for (int nt = 256; nt >= 16; nt /= 2) {
+    // At most 128: two accumulator buffers of 2 Nt columns then leave TMEM room
+    // for two CTAs per SM (1x1 stride 2, C 256: 40.8 us against 53.4 us at 256).
+    for (int nt = 128; nt >= 16; nt /= 2) {
         if (nt > cmax && nt > 16) continue;
         const int na = (int)cdiv(nt, 64);
         if (2 * (d.patch_bytes + d.max_yx * na * 8192) <= avail) {
@@ -725,26 +726,47 @@ int make_dgrad_plan(const wg_problem* p, const DeviceCaps& caps, DgPlan* pl, std
     }
     d.n_catoms = (int)cdiv(d.Nt, 64);
     d.n_ctiles = (int)cdiv(d.Cm, d.Nt);
-    d.stage_bytes = d.patch_bytes + d.TG * d.n_catoms * 8192;
-    // Ring depth: up to 4, but no deeper than the stages a tile has -- with a
-    // single stage per tile (K <= 64, one plane, every tap in one group) a
-    // one-deep ring lets two CTAs share an SM and overlap their tiles.
-    int max_nz = 0;
-    for (int r = 0; r < d.dim[2].nph; ++r) max_nz = std::max(max_nz, d.dim[2].ntap[r]);
-    const long long iters = (long long)d.n_kc * std::max(1, max_nz) * cdiv(d.max_yx, d.TG);
-    d.stages = (int)std::min<long long>(std::min(4, avail / d.stage_bytes), std::max(1LL, iters));
-    d.smem_bytes = d.stages * d.stage_bytes + 2048;
-    d.tmem_cols = std::max(32, pow2_at_least(d.Nt));
+    // Shared memory: resident W tiles (with a single (channel tile, group) every
+    // persistent CTA needs the same W tiles, loaded once) or W streamed with each
+    // patch, and a ring that runs on across a CTA's tiles, as deep as fits (<= 4).
+    // Two CTAs per SM come first (measured on GB300: two MMA issuers keep the
+    // tensor pipe busier than one at N <= 128, e.g. 56x56 C = K = 64: 20.8 us
+    // against 27.7 us with one CTA, W resident and a four-deep ring); then one
+    // CTA per SM, W resident only beside at least three patch stages.
+    const long long w_all = (long long)d.n_kc * pb.T * d.n_catoms * 8192;
+    const int streamed = d.patch_bytes + d.TG * d.n_catoms * 8192;
+    const int half = kMaxSmemPerCta / 2 - 1024 - 2048 - kDgStaging;  // ring + W of one of two CTAs
+    const bool tmem_half = pow2_at_least(2 * d.Nt) <= kMaxTmemCols / 2;
+    const bool can_res = d.n_ctiles * d.Gb == 1;
+    if (tmem_half && can_res && w_all + d.patch_bytes <= half) {
+        d.w_resident = 1, d.w_bytes = (int)w_all, d.stage_bytes = d.patch_bytes;
+        d.stages = std::min(4, (half - d.w_bytes) / d.stage_bytes);
+    } else if (tmem_half && streamed <= half) {
+        d.w_resident = 0, d.w_bytes = 0, d.stage_bytes = streamed;
+        d.stages = std::min(4, half / d.stage_bytes);
+    } else {
+        d.w_resident = (can_res && w_all + 3LL * d.patch_bytes <= avail) ? 1 : 0;
+        d.w_bytes = d.w_resident ? (int)w_all : 0;
+        d.stage_bytes = d.w_resident ? d.patch_bytes : streamed;
+        d.stages = std::min(4, (avail - d.w_bytes) / d.stage_bytes);
+    }
+    d.smem_bytes = d.w_bytes + d.stages * d.stage_bytes + kDgStaging + 2048;
+    d.tmem_cols = std::max(32, pow2_at_least(2 * d.Nt));  // two accumulator buffers
     d.n_tw = (int)cdiv(std::max(1, mJ[0]), d.bw);
     d.n_th = (int)cdiv(std::max(1, mJ[1]), d.bh);
     d.n_td = std::max(1, mJ[2]);
     d.n_phases = d.dim[0].nph * d.dim[1].nph * d.dim[2].nph;
     d.n_tiles = (long long)d.n_phases * d.n_tw * d.n_th * d.n_td * pb.N;
     if (d.n_tiles > (1ll << 31) - 1) return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: too many pixel tiles");
-    d.grid[0] = (unsigned)d.n_tiles;
-    d.grid[1] = (unsigned)d.n_ctiles;
-    d.grid[2] = (unsigned)d.Gb;
-    d.block = 256;
+    d.n_all = d.n_tiles * d.n_ctiles * d.Gb;
+    if (d.n_all > (1ll << 31) - 1) return fail(err, WG_ERR_NOT_SUPPORTED, "backward-data: too many tiles");
+    // Persistent grid: one CTA per SM (two when shared memory and TMEM allow),
+    // never more CTAs than tiles.
+    const int per_sm = (d.smem_bytes <= kMaxSmemPerCta / 2 - 1024 && d.tmem_cols <= 256) ? 2 : 1;
+    d.grid[0] = (unsigned)std::min<long long>(d.n_all, (long long)caps.num_sms * per_sm);
+    d.grid[1] = 1;
+    d.grid[2] = 1;
+    d.block = 192;
     return WG_OK;
 }
 
@@ -752,10 +774,11 @@ std::string dgrad_plan_string(const DgPlan& d)
 {
     char buf[512];
     snprintf(buf, sizeof buf,
-             "kernel=dgrad_tcgen05 Gm=%d phases=%d box=(w%d,h%d) patch=(w%d,h%d) Nt=%d catoms=%d ctiles=%d "
+             "kernel=dgrad_tcgen05 Gm=%d w_resident=%d phases=%d box=(w%d,h%d) patch=(w%d,h%d) Nt=%d catoms=%d "
+             "ctiles=%d "
              "kchunks=%d max_yx_taps=%d taps/stage=%d patch_bytes=%d stage_bytes=%d ring=%d smem=%d tmem_cols=%d "
              "grid=(%u,%u,%u) block=%u ws=%zu",
-             d.Gm, d.n_phases, d.bw, d.bh, d.PW, d.PH, d.Nt, d.n_catoms, d.n_ctiles, d.n_kc, d.max_yx, d.TG, d.patch_bytes,
+             d.Gm, d.w_resident, d.n_phases, d.bw, d.bh, d.PW, d.PH, d.Nt, d.n_catoms, d.n_ctiles, d.n_kc, d.max_yx, d.TG, d.patch_bytes,
              d.stage_bytes, d.stages, d.smem_bytes, d.tmem_cols, d.grid[0], d.grid[1], d.grid[2], d.block,
              d.ws_bytes);
     return buf;

@@ -140,6 +140,7 @@ std::string plan_string(const Plan& pl);
 // q_t = (r + pad_l - t*dil) / stride; per phase the taps are listed with their
 // row shift q_t - min q.  Stride 1 is the single phase r = 0 with every tap.
 constexpr int kDgMaxPhases = 8;
+constexpr int kDgStaging = 8192;  // epilogue staging of the backward-data kernel (4 warps x 32 x 64 B)
 constexpr int kDgMaxTaps = 32;
 struct DgDim {
     int nph;                                          // phases (= stride)
@@ -165,10 +166,13 @@ struct DgPlan {
     int TG;               // taps per stage (of one plane's (y, x) taps)
     int max_yx;           // most (y, x) taps of any phase
     int patch_bytes;      // dY patch bytes (1024-aligned)
+    int w_resident;       // 1: one (channel tile, group) and all its W tiles fit: loaded once per CTA
+    int w_bytes;          // resident W bytes (0 when streamed with the patches)
     int stage_bytes, stages, smem_bytes, tmem_cols;
     int n_tw, n_th, n_td; // boxes along w and h, depth positions, per phase (the largest phase)
     int n_phases;         // nph_w * nph_h * nph_d
     long long n_tiles;    // n_phases * n_tw * n_th * n_td * N
+    long long n_all;      // n_tiles * n_ctiles * Gb: the persistent CTAs' tile list
     DgDim dim[3];         // (w, h, d)
     unsigned grid[3];
     unsigned block;

@@ -16,6 +16,8 @@
 #include "k_igemm.cuh"
 #include "plan.h"
 
+static_assert(wg::kDgStaging == wg::kDgStagingBytes, "planner and kernel disagree on the dgrad staging size");
+
 namespace {
 
 thread_local std::string g_err;
@@ -734,7 +736,9 @@ int prepare_dgrad(const wg::DgPlan& d, const void* dy, const void* w, void* dx, 
     q.Wi = pb.in[2], q.Hi = pb.in[1], q.Di = pb.in[0];
     q.bw = d.bw, q.bh = d.bh, q.PW = d.PW, q.PH = d.PH;
     q.Nt = d.Nt, q.n_catoms = d.n_catoms, q.n_kc = d.n_kc, q.TG = d.TG;
-    q.n_tw = d.n_tw, q.n_th = d.n_th, q.n_td = d.n_td;
+    q.n_tw = d.n_tw, q.n_th = d.n_th, q.n_td = d.n_td, q.N = pb.N, q.n_ctiles = d.n_ctiles;
+    q.n_all = (int)d.n_all;
+    q.T = (int)pb.T, q.w_resident = d.w_resident, q.w_bytes = d.w_bytes;
     q.patch_bytes = d.patch_bytes, q.stage_bytes = d.stage_bytes, q.stages = d.stages, q.tmem_cols = d.tmem_cols;
     for (int j = 0; j < 3; ++j) q.dim[j] = d.dim[j];
     q.idesc = wg::make_idesc_f16(pb.in_dtype == WG_BF16, false, true, 128, d.Nt);

@@ -206,6 +206,28 @@ def test_dgrad_group_fold():
     assert " Gm=2 " in binding.wg_bwd_data_plan_string(folded)
 
 
+def _dg_fields(ps):
+    return {k: v for k, v in re.findall(r"(\w+)=(\S+)", ps)}
+
+
+def test_dgrad_persistent_plans():
+    # Two CTAs per SM (shared memory and TMEM of both fit) come first; W stays
+    # resident when one (channel tile, group) covers the problem.
+    nsm = 152
+    dense = _dg_fields(binding.wg_bwd_data_plan_string(WORKLOADS["2d_dense_n32_h56_c64_k64"][0]))
+    assert dense["w_resident"] == "1" and int(dense["smem"]) <= 232448 // 2 - 1024
+    assert dense["grid"] == f"({2 * nsm},1,1)" and int(dense["tmem_cols"]) <= 256
+    grouped = _dg_fields(binding.wg_bwd_data_plan_string(WORKLOADS["2d_grouped_g32_c8_k8_n32_h28"][0]))
+    assert grouped["w_resident"] == "0"  # four group blocks: W streamed with each patch
+    # C = 256 takes two 128-channel tiles (TMEM for two accumulators of two CTAs).
+    wide = _dg_fields(binding.wg_bwd_data_plan_string(WORKLOADS["2d_1x1s2_n32_h56_c256_k128"][0]))
+    assert wide["Nt"] == "128" and wide["ctiles"] == "2" and wide["w_resident"] == "0"
+    # Never more CTAs than tiles.
+    tiny = _dg_fields(binding.wg_bwd_data_plan_string(spec(2, 1, 1, 16, 16, [8, 8], [3, 3], [1, 1], [1, 1],
+                                                           [1, 1], [1, 1])))
+    assert tiny["grid"] == "(1,1,1)"
+
+
 def test_dgrad_launch_checks_before_device(lib):
     sp = spec(2, 1, 1, 16, 16, [8, 8], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])
     with pytest.raises(binding.WgradError) as e:

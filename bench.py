@@ -7,8 +7,9 @@ A step is one call of wg_conv_bwd_weight -- the whole path: every launch it make
 (split-K stage 1, the stage-2 reduce or the atomic-mode memset) -- over one batch
 of synthetic, seeded inputs already resident in HBM.  The device-side value
 times each call between CUDA events on its stream (--graph replays a captured
-CUDA graph of the call instead).  The e2e value times the same call with host
-buffers.  The headline workload is the 2-D dense 56x56, C = K = 64, N = 32, 3x3
+CUDA graph of the call instead).  The e2e value times wg_conv_bwd_weight_host,
+the same computation from pinned host buffers: X and dY copied in, the call,
+dW copied back, all enqueued by the library.  The headline workload is the 2-D dense 56x56, C = K = 64, N = 32, 3x3
 problem with bf16 inputs and bf16 dW; the other workloads, and the other plans
 the measurement table lists for each (split degrees, modes, merge widths, the
 tensor-core depthwise variant), are reported under "workloads".  No step finds
@@ -301,6 +302,10 @@ class Workload:
                                                    self.ws_bytes, **kw))
         self.next = 0
         self.rotating = self.copies > 1
+        # End to end: the host-buffer entry point, staging into self.x / self.dy / self.dw.
+        self.host_call = binding.PreparedHostCall(sp, self.x_host, self.dy_host, self.dw_host, self.x, self.dy,
+                                                  self.dw, self.split_k, self.mode, self.gm, self.ws, self.ws_bytes,
+                                                  **kw)
 
     def l2_note(self):
         if self.rotating:
@@ -327,11 +332,8 @@ class Workload:
             self.next = (self.next + 1) % self.copies
 
     def e2e_step(self, stream):
-        # The public call itself (no graph), with host<->device copies.
-        self.x.copy_(self.x_host, non_blocking=True)
-        self.dy.copy_(self.dy_host, non_blocking=True)
-        self.call(stream.cuda_stream)
-        self.dw_host.copy_(self.dw, non_blocking=True)
+        # One public call from host buffers: X and dY in, the computation, dW out.
+        self.host_call(stream.cuda_stream)
 
 
 class DgradWorkload:
@@ -611,7 +613,8 @@ def main():
                 "roofline": roof, "clocks": clocks, "gpu_launches": wl.launches_per_step * args.steps,
                 "e2e": {"value": job_value(ws, s["flops"], e2e_ms) / 1e12, "unit": "TFLOP/s",
                         "h2d_bytes_per_step": 2 * (s["nx"] + s["ndy"]), "d2h_bytes_per_step": s["wsz"] * s["ndw"],
-                        "ms_per_step": e2e_ms},
+                        "ms_per_step": e2e_ms,
+                        "call": "wg_conv_bwd_weight_host: pinned host X, dY in; dW out to pinned host memory"},
                 "wall_s_timed": t_wall, "workloads": extra}
         if ws == 1 and not args.no_extra:
             line["cpu_baseline"] = cpu_baseline(args.workload)

@@ -44,7 +44,7 @@ class WgradError(RuntimeError):
 
 EXPORTS = ("wg_problem_normalize", "wg_workspace_size", "wg_conv_bwd_weight", "wg_check_status",
            "wg_plan_string", "wg_status_string", "wg_last_error", "wg_conv_bwd_weight_noalloc",
-           "wg_set_mark_event", "wg_conv_bwd_data", "wg_bwd_data_plan_string", "wg_bwd_data_workspace_size")
+           "wg_set_mark_event", "wg_conv_bwd_data", "wg_bwd_data_plan_string", "wg_bwd_data_workspace_size", "wg_conv_bwd_weight_host")
 
 _lib = None
 _lock = threading.Lock()
@@ -70,6 +70,8 @@ def load():
                                                ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
             lib.wg_conv_bwd_weight_noalloc.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, O,
                                                        ctypes.c_void_p]
+            lib.wg_conv_bwd_weight_host.argtypes = [P] + [ctypes.c_void_p] * 6 + [O, ctypes.c_void_p, ctypes.c_size_t,
+                                                                                  ctypes.c_void_p]
             lib.wg_check_status.argtypes = [ctypes.c_void_p]
             lib.wg_set_mark_event.argtypes = [ctypes.c_void_p]
             lib.wg_conv_bwd_data.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -172,6 +174,40 @@ class PreparedCall:
         self.args = (ctypes.byref(self.p), ctypes.c_void_p(_addr(x)), ctypes.c_void_p(_addr(dy)),
                      ctypes.c_void_p(_addr(dw)), ctypes.byref(self.o), ctypes.c_void_p(_addr(workspace)),
                      ctypes.c_size_t(int(ws_bytes)))
+
+    def __call__(self, stream_handle: int | None = None) -> None:
+        st = self.fn(*self.args, stream_handle)
+        if st:
+            _check(st)
+
+
+def wg_conv_bwd_weight_host(spec: dict, x_host, dy_host, dw_host, x_dev, dy_dev, dw_dev, split_k: int = 0,
+                            mode: str = "auto", group_merge: int = 0, workspace=None, ws_bytes: int | None = None,
+                            stream=None, *, cluster: int = 0, kernel: str = "auto") -> None:
+    """The weight gradient from host buffers (x_host, dy_host; ideally pinned) into dw_host,
+    staged through the device buffers x_dev, dy_dev, dw_dev; copies overlap the compute."""
+    p, o = make_problem(spec), make_options(split_k, mode, group_merge, cluster, kernel)
+    if ws_bytes is None:
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().wg_conv_bwd_weight_host(ctypes.byref(p), _addr(x_host), _addr(dy_host), _addr(dw_host),
+                                          _addr(x_dev), _addr(dy_dev), _addr(dw_dev), ctypes.byref(o),
+                                          _addr(workspace), int(ws_bytes), _stream_handle(stream)))
+
+
+class PreparedHostCall:
+    """wg_conv_bwd_weight_host with its arguments marshalled once (one ctypes call per use)."""
+
+    def __init__(self, spec: dict, x_host, dy_host, dw_host, x_dev, dy_dev, dw_dev, split_k: int = 0,
+                 mode: str = "auto", group_merge: int = 0, workspace=None, ws_bytes: int | None = None, *,
+                 cluster: int = 0, kernel: str = "auto"):
+        self._keep = (x_host, dy_host, dw_host, x_dev, dy_dev, dw_dev, workspace)
+        self.p, self.o = make_problem(spec), make_options(split_k, mode, group_merge, cluster, kernel)
+        if ws_bytes is None:
+            ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        self.fn = load().wg_conv_bwd_weight_host
+        self.args = (ctypes.byref(self.p), *(ctypes.c_void_p(_addr(t)) for t in (x_host, dy_host, dw_host, x_dev,
+                                                                                 dy_dev, dw_dev)),
+                     ctypes.byref(self.o), ctypes.c_void_p(_addr(workspace)), ctypes.c_size_t(int(ws_bytes)))
 
     def __call__(self, stream_handle: int | None = None) -> None:
         st = self.fn(*self.args, stream_handle)

@@ -6,6 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <string>
@@ -339,16 +340,23 @@ int launch_reduce(const wg::Plan& pl, void* ws, void* dw, cudaStream_t stream)
     return WG_OK;
 }
 
-int launch_igemm(const wg::Plan& pl, const Prepared& pr, void* dw, void* ws, cudaStream_t stream)
+// A call runs as launch_pre (zero dW for atomic accumulation), the main kernel
+// (launch_main), then launch_post (the mark event, then the split reduction).
+int launch_pre(const wg::Plan& pl, void* dw, cudaStream_t stream)
 {
-    const wg::Problem& pb = pl.pb;
-    const wg::IgemmPlan& ig = pl.ig;
-    int st = ensure_smem(wg::igemm_wgrad_kernel, ig.smem_bytes);
-    if (st) return st;
     if (pl.mode == wg::MODE_ATOMIC) {
-        const cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)pb.dw_elems * 4, stream);
+        const cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)pl.pb.dw_elems * 4, stream);
         if (e != cudaSuccess) return cuda_fail("cudaMemsetAsync(dW)", e);
     }
+    return WG_OK;
+}
+
+int launch_igemm_main(const wg::Plan& pl, const Prepared& pr, cudaStream_t stream)
+{
+    const wg::IgemmPlan& ig = pl.ig;
+    const int st = ensure_smem(wg::igemm_wgrad_kernel, ig.smem_bytes);
+    if (st) return st;
+    const dim3 grid(pl.grid[0], pl.grid[1], pl.grid[2]);
     cudaError_t e;
     if (ig.cluster > 1) {
         // Consecutive splits form a cluster (grid z is a multiple of the cluster size).
@@ -360,53 +368,59 @@ int launch_igemm(const wg::Plan& pl, const Prepared& pr, void* dw, void* ws, cud
         attr[0].val.clusterDim.z = (unsigned)ig.cluster;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cfg.gridDim = dim3(pl.grid[0], pl.grid[1], pl.grid[2]);
+        cfg.gridDim = grid;
         cfg.blockDim = dim3(pl.block);
         cfg.dynamicSmemBytes = (size_t)ig.smem_bytes;
         cfg.stream = stream;
         e = cudaLaunchKernelEx(&cfg, wg::igemm_wgrad_kernel, pr.tmx, pr.tmy, pr.ig);
     } else {
-        wg::igemm_wgrad_kernel<<<dim3(pl.grid[0], pl.grid[1], pl.grid[2]), pl.block, ig.smem_bytes, stream>>>(
-            pr.tmx, pr.tmy, pr.ig);
+        wg::igemm_wgrad_kernel<<<grid, pl.block, ig.smem_bytes, stream>>>(pr.tmx, pr.tmy, pr.ig);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return cuda_fail("igemm_wgrad_kernel launch", e);
-    if (g_mark && (e = cudaEventRecord(g_mark, stream)) != cudaSuccess) return cuda_fail("cudaEventRecord(mark)", e);
-    if (pl.mode == wg::MODE_DETERMINISTIC) {
-        st = launch_reduce(pl, ws, dw, stream);
-        if (st) return st;
+    return WG_OK;
+}
+
+int launch_post(const wg::Plan& pl, void* ws, void* dw, cudaStream_t stream)
+{
+    if (g_mark) {
+        const cudaError_t e = cudaEventRecord(g_mark, stream);
+        if (e != cudaSuccess) return cuda_fail("cudaEventRecord(mark)", e);
     }
+    if (pl.mode == wg::MODE_DETERMINISTIC) return launch_reduce(pl, ws, dw, stream);
     return WG_OK;
 }
 
 template <bool BF16, int GM, bool SLIDE>
-int launch_dw_t(const wg::Plan& pl, const CUtensorMap& tmx, const CUtensorMap& tmy, const wg::DwParams& prm,
+int launch_dw_t(const wg::Plan& pl, dim3 grid, const CUtensorMap& tmx, const CUtensorMap& tmy, const wg::DwParams& prm,
                 cudaStream_t stream)
 {
     auto k = wg::depthwise_wgrad_kernel<BF16, GM, SLIDE>;
     const int st = ensure_smem(k, pl.dw.smem_bytes);
     if (st) return st;
-    k<<<dim3(pl.grid[0], pl.grid[1], pl.grid[2]), pl.block, pl.dw.smem_bytes, stream>>>(tmx, tmy, prm);
+    k<<<grid, pl.block, pl.dw.smem_bytes, stream>>>(tmx, tmy, prm);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail("depthwise_wgrad_kernel launch", e);
     return WG_OK;
 }
 
 template <bool BF16, int GM>
-int launch_dw_g(const wg::Plan& pl, const CUtensorMap& a, const CUtensorMap& b, const wg::DwParams& prm, cudaStream_t s)
+int launch_dw_g(const wg::Plan& pl, dim3 g, const CUtensorMap& a, const CUtensorMap& b, const wg::DwParams& prm,
+                cudaStream_t s)
 {
     const bool slide = pl.dw.sliding && pl.pb.filt[1] == 3 && pl.pb.filt[2] == 3;
-    return slide ? launch_dw_t<BF16, GM, true>(pl, a, b, prm, s) : launch_dw_t<BF16, GM, false>(pl, a, b, prm, s);
+    return slide ? launch_dw_t<BF16, GM, true>(pl, g, a, b, prm, s) : launch_dw_t<BF16, GM, false>(pl, g, a, b, prm, s);
 }
 
 template <bool BF16>
-int launch_dw_b(const wg::Plan& pl, const CUtensorMap& a, const CUtensorMap& b, const wg::DwParams& prm, cudaStream_t s)
+int launch_dw_b(const wg::Plan& pl, dim3 g, const CUtensorMap& a, const CUtensorMap& b, const wg::DwParams& prm,
+                cudaStream_t s)
 {
     switch (pl.dw.Gm) {
-        case 1: return launch_dw_g<BF16, 1>(pl, a, b, prm, s);
-        case 2: return launch_dw_g<BF16, 2>(pl, a, b, prm, s);
-        case 4: return launch_dw_g<BF16, 4>(pl, a, b, prm, s);
-        default: return launch_dw_g<BF16, 8>(pl, a, b, prm, s);
+        case 1: return launch_dw_g<BF16, 1>(pl, g, a, b, prm, s);
+        case 2: return launch_dw_g<BF16, 2>(pl, g, a, b, prm, s);
+        case 4: return launch_dw_g<BF16, 4>(pl, g, a, b, prm, s);
+        default: return launch_dw_g<BF16, 8>(pl, g, a, b, prm, s);
     }
 }
 
@@ -449,23 +463,61 @@ int prepare_depthwise(const wg::Plan& pl, const void* x, const void* dy, void* d
     return WG_OK;
 }
 
-int launch_depthwise(const wg::Plan& pl, const Prepared& pr, void* dw, void* ws, cudaStream_t stream)
+int launch_depthwise_main(const wg::Plan& pl, const Prepared& pr, cudaStream_t stream)
 {
-    const wg::Problem& pb = pl.pb;
-    if (pl.mode == wg::MODE_ATOMIC) {
-        const cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)pb.dw_elems * 4, stream);
-        if (e != cudaSuccess) return cuda_fail("cudaMemsetAsync(dW)", e);
+    const dim3 grid(pl.grid[0], pl.grid[1], pl.grid[2]);
+    return pl.pb.in_dtype == WG_BF16 ? launch_dw_b<true>(pl, grid, pr.tmx, pr.tmy, pr.dw, stream)
+                                     : launch_dw_b<false>(pl, grid, pr.tmx, pr.tmy, pr.dw, stream);
+}
+
+int launch_call(const wg::Plan& pl, const Prepared& pr, void* dw, void* ws, cudaStream_t stream)
+{
+    int st = launch_pre(pl, dw, stream);
+    if (!st)
+        st = pl.kind == wg::KIND_IGEMM ? launch_igemm_main(pl, pr, stream) : launch_depthwise_main(pl, pr, stream);
+    if (!st) st = launch_post(pl, ws, dw, stream);
+    return st;
+}
+
+// The prepared launch (tensor maps and kernel parameters) of a plan on these
+// buffers, from the cache or built and cached.
+int prepared_for(const wg::Plan& pl, const std::string& pkey, const void* x, const void* dy, void* dw, void* workspace,
+                 Prepared* pr)
+{
+    const void* ws_used = pl.ws_bytes > 0 ? workspace : nullptr;
+    const std::string key = prep_key(pkey, x, dy, dw, ws_used);
+    {
+        std::lock_guard<std::mutex> lk(g_prep_mu);
+        auto it = prep_cache().find(key);
+        if (it != prep_cache().end()) {
+            *pr = it->second;
+            return WG_OK;
+        }
     }
-    int st = pb.in_dtype == WG_BF16 ? launch_dw_b<true>(pl, pr.tmx, pr.tmy, pr.dw, stream)
-                                    : launch_dw_b<false>(pl, pr.tmx, pr.tmy, pr.dw, stream);
+    const int st = pl.kind == wg::KIND_IGEMM ? prepare_igemm(pl, x, dy, dw, workspace, pr)
+                                             : prepare_depthwise(pl, x, dy, dw, workspace, pr);
     if (st) return st;
-    if (g_mark) {
-        const cudaError_t e = cudaEventRecord(g_mark, stream);
-        if (e != cudaSuccess) return cuda_fail("cudaEventRecord(mark)", e);
-    }
-    if (pl.mode == wg::MODE_DETERMINISTIC) {
-        st = launch_reduce(pl, ws, dw, stream);
-        if (st) return st;
+    std::lock_guard<std::mutex> lk(g_prep_mu);
+    if (prep_cache().size() > 4096) prep_cache().clear();
+    prep_cache().emplace(key, *pr);
+    return WG_OK;
+}
+
+// Device buffers and workspace of a call: present, aligned, large enough.
+int check_buffers(const wg::Plan& pl, const void* x, const void* dy, const void* dw, const void* workspace,
+                  size_t ws_bytes)
+{
+    if (!x || !dy || !dw) return set_err(WG_ERR_INVALID_ARGUMENT, "x, dy and dw must be non-NULL device pointers");
+    if (!aligned16(x) || !aligned16(dy) || !aligned16(dw))
+        return set_err(WG_ERR_MISALIGNED, "x, dy and dw must be 16-byte aligned");
+    if (pl.ws_bytes > 0) {
+        if (!workspace || ws_bytes < pl.ws_bytes) {
+            char buf[160];
+            snprintf(buf, sizeof buf, "workspace of %zu bytes needed (got %zu%s)", pl.ws_bytes, ws_bytes,
+                     workspace ? "" : ", NULL");
+            return set_err(WG_ERR_WORKSPACE, buf);
+        }
+        if (!aligned16(workspace)) return set_err(WG_ERR_MISALIGNED, "workspace must be 16-byte aligned");
     }
     return WG_OK;
 }
@@ -533,38 +585,37 @@ int wg_conv_bwd_weight(const wg_problem* p, const void* x, const void* dy, void*
     std::string pkey;
     int st = plan_for(p, opt, &pl, &pkey);
     if (st) return st;
-    if (!x || !dy || !dw) return set_err(WG_ERR_INVALID_ARGUMENT, "x, dy and dw must be non-NULL device pointers");
-    if (!aligned16(x) || !aligned16(dy) || !aligned16(dw))
-        return set_err(WG_ERR_MISALIGNED, "x, dy and dw must be 16-byte aligned");
-    if (pl.ws_bytes > 0) {
-        if (!workspace || ws_bytes < pl.ws_bytes) {
-            char buf[160];
-            snprintf(buf, sizeof buf, "workspace of %zu bytes needed (got %zu%s)", pl.ws_bytes, ws_bytes,
-                     workspace ? "" : ", NULL");
-            return set_err(WG_ERR_WORKSPACE, buf);
-        }
-        if (!aligned16(workspace)) return set_err(WG_ERR_MISALIGNED, "workspace must be 16-byte aligned");
-    }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const void* ws_used = pl.ws_bytes > 0 ? workspace : nullptr;
-    const std::string key = prep_key(pkey, x, dy, dw, ws_used);
+    if ((st = check_buffers(pl, x, dy, dw, workspace, ws_bytes))) return st;
     Prepared pr;
-    bool hit = false;
-    {
-        std::lock_guard<std::mutex> lk(g_prep_mu);
-        auto it = prep_cache().find(key);
-        if (it != prep_cache().end()) pr = it->second, hit = true;
-    }
-    if (!hit) {
-        st = pl.kind == wg::KIND_IGEMM ? prepare_igemm(pl, x, dy, dw, workspace, &pr)
-                                       : prepare_depthwise(pl, x, dy, dw, workspace, &pr);
-        if (st) return st;
-        std::lock_guard<std::mutex> lk(g_prep_mu);
-        if (prep_cache().size() > 4096) prep_cache().clear();
-        prep_cache().emplace(key, pr);
-    }
-    st = pl.kind == wg::KIND_IGEMM ? launch_igemm(pl, pr, dw, workspace, s) : launch_depthwise(pl, pr, dw, workspace, s);
-    return st;
+    if ((st = prepared_for(pl, pkey, x, dy, dw, workspace, &pr))) return st;
+    return launch_call(pl, pr, dw, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int wg_conv_bwd_weight_host(const wg_problem* p, const void* x_host, const void* dy_host, void* dw_host,
+                            void* x_dev, void* dy_dev, void* dw_dev, const wg_options* opt, void* workspace,
+                            size_t ws_bytes, void* stream)
+{
+    wg::Plan pl;
+    std::string pkey;
+    int st = plan_for(p, opt, &pl, &pkey);
+    if (st) return st;
+    if (!x_host || !dy_host || !dw_host)
+        return set_err(WG_ERR_INVALID_ARGUMENT, "x_host, dy_host and dw_host must be non-NULL");
+    if ((st = check_buffers(pl, x_dev, dy_dev, dw_dev, workspace, ws_bytes))) return st;
+    Prepared pr;
+    if ((st = prepared_for(pl, pkey, x_dev, dy_dev, dw_dev, workspace, &pr))) return st;
+    const wg::Problem& pb = pl.pb;
+    const size_t dw_bytes = (size_t)pb.dw_elems * (pb.out_dtype == WG_FP32 ? 4 : 2);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(x_dev, x_host, (size_t)pb.x_elems * 2, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail("cudaMemcpyAsync(X)", e);
+    if ((e = cudaMemcpyAsync(dy_dev, dy_host, (size_t)pb.dy_elems * 2, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail("cudaMemcpyAsync(dY)", e);
+    if ((st = launch_call(pl, pr, dw_dev, workspace, s))) return st;
+    if ((e = cudaMemcpyAsync(dw_host, dw_dev, dw_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail("cudaMemcpyAsync(dW)", e);
+    return WG_OK;
 }
 
 int wg_check_status(void* stream)

@@ -20,7 +20,9 @@
  *
  * Conventions for every entry point below:
  *  - Pointers x, dy, dw and workspace are DEVICE pointers on the current CUDA
- *    device, owned by the caller.  The library allocates no device memory.
+ *    device, owned by the caller (wg_conv_bwd_weight_host also takes the
+ *    host buffers x_host, dy_host and dw_host).  The library allocates no
+ *    device memory.
  *  - x, dy, dw and workspace must be 16-byte aligned (WG_ERR_MISALIGNED).
  *  - dW is overwritten (beta = 0) in every mode.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
@@ -189,6 +191,29 @@ WG_API const char* wg_last_error(void);
  * threads) race on it and must be serialised by the caller. */
 WG_API int wg_conv_bwd_weight_noalloc(const wg_problem* p, const void* x, const void* dy, void* dw,
                                       const wg_options* opt, void* stream);
+
+/* wg_conv_bwd_weight with the inputs and the result in host memory (no
+ * counterpart in the CK page: it is a property of this library's API).
+ *
+ *  x_host, dy_host: X and dY in host memory, layouts as for wg_conv_bwd_weight.
+ *    Page-locked memory (cudaHostAlloc, cudaHostRegister) is copied
+ *    asynchronously; pageable memory goes through the driver's staging (the
+ *    call then returns only after it has been read).
+ *  dw_host: host memory that receives dW (out_dtype).
+ *  x_dev, dy_dev, dw_dev: device buffers of the sizes of X, dY and dW that the
+ *    call copies into and computes from (caller-owned, 16-byte aligned).
+ *  opt, workspace, ws_bytes, stream: as for wg_conv_bwd_weight.
+ *
+ * Enqueues on `stream`: the copies of X and dY to the device buffers, the
+ * computation exactly as wg_conv_bwd_weight on those buffers, and the copy of
+ * dW to dw_host, which holds dW once `stream` has completed the call.
+ * (Copying in image chunks overlapped with the main kernel's split ranges was
+ * measured slower on GB300 than copying first: 181 us against 162 us per call
+ * for the 56x56 C = K = 64 problem, so the copies run first.)  Returns WG_OK
+ * or an error status; nothing is enqueued on an error. */
+WG_API int wg_conv_bwd_weight_host(const wg_problem* p, const void* x_host, const void* dy_host, void* dw_host,
+                                   void* x_dev, void* dy_dev, void* dw_dev, const wg_options* opt, void* workspace,
+                                   size_t ws_bytes, void* stream);
 
 /* Measurement hook (no counterpart in the CK page: it exists so that the
  * kernels of one call can be timed separately with CUDA events).  While

@@ -138,6 +138,23 @@ def test_launch_argument_checks_before_device(lib):
     assert "workspace" in binding.wg_last_error()
 
 
+def test_host_entry_argument_checks_before_device(lib):
+    # The host-buffer entry point validates before it enqueues anything: NULL host
+    # buffers (1), unaligned device buffers (3), a missing workspace (4).
+    sp = spec(2, 1, 1, 16, 16, [8, 8], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])
+    for args, status in (((0, 64, 128, 4096, 8192, 12288), 1),
+                         ((64, 0, 128, 4096, 8192, 12288), 1),
+                         ((64, 128, 0, 4096, 8192, 12288), 1),
+                         ((64, 128, 192, 4096 + 8, 8192, 12288), 3),
+                         ((64, 128, 192, 4096, 8192, 0), 1)):
+        with pytest.raises(binding.WgradError) as e:
+            binding.wg_conv_bwd_weight_host(sp, *args)
+        assert e.value.status == status, args
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_conv_bwd_weight_host(sp, 64, 128, 192, 4096, 8192, 12288, split_k=3, mode="deterministic")
+    assert e.value.status == 4
+
+
 @pytest.mark.parametrize("name", list(WORKLOADS))
 def test_plans_for_workloads(name):
     sp = WORKLOADS[name][0]

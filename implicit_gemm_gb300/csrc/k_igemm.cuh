@@ -572,7 +572,7 @@ __global__ void __launch_bounds__(kRedThreads)
                 : "memory");
         }
     }
-    if (!mbar_wait(&bar, 0)) return;
+    if (!__syncthreads_and(mbar_wait(&bar, 0))) return;  // one decision for the whole CTA
     const int G = red_groups(S);
     float* part = sm + (size_t)S * W;  // [G][W]
     // Each thread adds one split range for 4 consecutive elements (W is a

@@ -517,13 +517,6 @@ __global__ void __launch_bounds__(kIgThreads, 1)
 // contiguous ranges, each summed in index order, and the four range sums are
 // added in range order; for S < 8 one range.  The result is bitwise
 // reproducible.
-//
-// Bulk path: CTA b owns workspace slice b (W consecutive elements of one dW
-// row), whose S partials are one contiguous block; one warp pulls it into
-// shared memory with a few large cp.async.bulk copies, then four threads per
-// element add the four split ranges.  Launched with programmatic dependent
-// launch: its set-up overlaps the split-K kernel's tail, and it waits for that
-// kernel's writes with griddepcontrol.wait.
 __device__ __forceinline__ void store_cast(void* dw, long long i, float a, int out_dtype)
 {
     if (out_dtype == 2)
@@ -540,48 +533,23 @@ constexpr uint32_t kRedPiece = 16384;  // bytes per bulk copy
 
 __host__ __device__ __forceinline__ int red_groups(int S) { return S >= 8 ? kRedGroups : 1; }
 
-__global__ void __launch_bounds__(kRedThreads)
-    reduce_splits_bulk_kernel(const float* __restrict__ ws, void* __restrict__ dw, const WsLayout w, int out_dtype)
+// Sum nsl consecutive slices staged in shared memory -- slice sl0 + k at
+// sm + k * S * W, with kRedGroups * W floats of scratch at part + k * kRedGroups * W
+// -- in the fixed order and store their elements of dW.  Every thread of the CTA
+// calls it (it synchronises them once); the work of all the slices is shared.
+__device__ __forceinline__ void slices_reduce_store(const float* sm, float* part, const WsLayout& w, long long sl0,
+                                                    int nsl, void* dw, int out_dtype)
 {
-    extern __shared__ uint8_t red_raw[];
-    float* sm = align_shared<float>(red_raw, 128);
-    __shared__ uint64_t bar;
     const int S = w.S, W = w.W;
-    const long long r = blockIdx.x / w.nj;
-    const int j = (int)(blockIdx.x - r * w.nj);
-    const long long x0 = (long long)j * W;
-    const int n = (int)min((long long)W, w.L - x0);
-    const long long e0 = r * w.L + x0;
-    const uint32_t total = (uint32_t)S * (uint32_t)W * 4u;  // the whole slice, tail elements included
-    if (threadIdx.x == 0) {
-        mbar_init(&bar, 1);
-        fence_mbar_init();
-        mbar_arrive_expect_tx(&bar, total);
-    }
-    __syncthreads();
-    // Everything above may run while the split-K kernel is still finishing.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (threadIdx.x < 32) {
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(ws + (long long)blockIdx.x * S * W);
-        for (uint32_t off = threadIdx.x * kRedPiece; off < total; off += 32 * kRedPiece) {
-            const uint32_t size = min(kRedPiece, total - off);
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    smem_u32(sm) + off),
-                "l"(src + off), "r"(size), "r"(smem_u32(&bar))
-                : "memory");
-        }
-    }
-    if (!__syncthreads_and(mbar_wait(&bar, 0))) return;  // one decision for the whole CTA
     const int G = red_groups(S);
-    float* part = sm + (size_t)S * W;  // [G][W]
-    // Each thread adds one split range for 4 consecutive elements (W is a
-    // multiple of 4): 16-byte shared-memory loads, four independent chains.
-    const int W4 = W >> 2;
-    for (int idx = threadIdx.x; idx < W4 * G; idx += kRedThreads) {
-        const int g = idx / W4, i4 = idx - g * W4;
+    // Each item adds one split range for 4 consecutive elements of one slice (W
+    // is a multiple of 4): 16-byte shared-memory loads, four independent chains.
+    const int W4 = W >> 2, per_slice = W4 * G;
+    for (int idx = threadIdx.x; idx < nsl * per_slice; idx += blockDim.x) {
+        const int k = idx / per_slice, rem = idx - k * per_slice;
+        const int g = rem / W4, i4 = rem - g * W4;
         const int s0 = S * g / G, s1 = S * (g + 1) / G;
-        const float4* q = reinterpret_cast<const float4*>(sm + (size_t)s0 * W) + i4;
+        const float4* q = reinterpret_cast<const float4*>(sm + ((size_t)k * S + s0) * W) + i4;
         float4 a = q[0];
         q += W4;
         int s = s0 + 1;
@@ -593,14 +561,59 @@ __global__ void __launch_bounds__(kRedThreads)
             for (int jj = 0; jj < 4; ++jj) a.x += v[jj].x, a.y += v[jj].y, a.z += v[jj].z, a.w += v[jj].w;
         }
         for (; s < s1; ++s, q += W4) a.x += q[0].x, a.y += q[0].y, a.z += q[0].z, a.w += q[0].w;
-        reinterpret_cast<float4*>(part + (size_t)g * W)[i4] = a;
+        reinterpret_cast<float4*>(part + ((size_t)k * kRedGroups + g) * W)[i4] = a;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += kRedThreads) {
-        float a = part[i];
-        for (int g = 1; g < G; ++g) a += part[g * W + i];
-        store_cast(dw, e0 + i, a, out_dtype);
+    for (int idx = threadIdx.x; idx < nsl * W; idx += blockDim.x) {
+        const int k = idx / W, i = idx - k * W;
+        const long long sl = sl0 + k;
+        const long long r = sl / w.nj;
+        const long long x0 = (sl - r * w.nj) * W;
+        if (x0 + i >= w.L) continue;  // past the end of the row (its last slice)
+        const float* pk = part + (size_t)k * kRedGroups * W;
+        float a = pk[i];
+        for (int g = 1; g < G; ++g) a += pk[g * W + i];
+        store_cast(dw, r * w.L + x0 + i, a, out_dtype);
     }
+}
+
+// Bulk path: CTA b owns workspace slices [b * spc, (b + 1) * spc) (spc > 1 when
+// slices are small: W elements of one dW row each), whose S partials are one
+// contiguous block; one warp pulls it into shared memory with a few large
+// cp.async.bulk copies, then the threads add the split ranges.  Launched with
+// programmatic dependent launch: its set-up overlaps the split-K kernel's
+// tail, and it waits for that kernel's writes with griddepcontrol.wait.
+__global__ void __launch_bounds__(kRedThreads)
+    reduce_splits_bulk_kernel(const float* __restrict__ ws, void* __restrict__ dw, const WsLayout w, int out_dtype,
+                              int spc, long long n_slices)
+{
+    extern __shared__ uint8_t red_raw[];
+    float* sm = align_shared<float>(red_raw, 128);
+    __shared__ uint64_t bar;
+    const long long sl0 = (long long)blockIdx.x * spc;
+    const int nsl = (int)min((long long)spc, n_slices - sl0);
+    const uint32_t total = (uint32_t)nsl * (uint32_t)w.S * (uint32_t)w.W * 4u;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&bar, total);
+    }
+    __syncthreads();
+    // Everything above may run while the split-K kernel is still finishing.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x < 32) {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(ws + sl0 * w.S * w.W);
+        for (uint32_t off = threadIdx.x * kRedPiece; off < total; off += 32 * kRedPiece) {
+            const uint32_t size = min(kRedPiece, total - off);
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_u32(sm) + off),
+                "l"(src + off), "r"(size), "r"(smem_u32(&bar))
+                : "memory");
+        }
+    }
+    if (!__syncthreads_and(mbar_wait(&bar, 0))) return;  // one decision for the whole CTA
+    slices_reduce_store(sm, sm + (size_t)spc * w.S * w.W, w, sl0, nsl, dw, out_dtype);
 }
 
 // Fallback for split counts whose slice block does not fit shared memory: one

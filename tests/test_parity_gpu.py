@@ -195,6 +195,20 @@ def test_deterministic_mode_repeats_bitwise(name):
     assert np.array_equal(a.view(np.int64), b.view(np.int64))
 
 
+@pytest.mark.parametrize("split_k,mode", [(8, "atomic"), (8, "deterministic"), (0, "auto")])
+def test_3d_ragged_gemmk(split_k, mode):
+    # The 3-D stride-2 geometry (C 128, K 96, 3x3x3, pad 1) on 3 images of 13^3:
+    # output 7^3, GemmK = 3 * 343 = 1029, not a multiple of any K-tile, in the
+    # 3-D workload's modes.
+    sp = spec(3, 1, 3, 128, 96, [13, 13, 13], [3, 3, 3], [2, 2, 2], [1, 1, 1], [1, 1, 1], [1, 1, 1],
+              in_dtype="fp16", out_dtype="fp32")
+    assert binding.wg_problem_normalize(sp) == [7, 7, 7]
+    x, dy = make_inputs(sp, ("normal", 0.0, 0.5), 47, 48)
+    dw, A = ref(sp, x, dy)
+    got = run_gpu(sp, x, dy, split_k, mode)
+    assert_close(got, dw, A, sp["out_dtype"], f"3-D ragged S={split_k} {mode}")
+
+
 def test_more_splits_than_tiles():
     sp = spec(2, 1, 1, 16, 32, [8, 8], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])
     x, dy = make_inputs(sp, ("int", -2, 2), 37, 38)

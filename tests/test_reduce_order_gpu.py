@@ -6,7 +6,8 @@ documents -- for S >= 8 four contiguous ranges of splits, each summed in index
 order in fp32, then the four range sums in range order; for S < 8 index order --
 rounds to the output type (round to nearest even) and requires dW to match bit
 for bit, for split degrees below and above 8, 16-bit and fp32 dW, 2-D and 3-D
-problems and a grouped one.  The workspace layout is the documented one: dW as
+problems, a grouped one, and depthwise problems (whose workspace holds all of
+dW as one row).  The workspace layout is the documented one: dW as
 rows of L = T*C elements per (g, k), rows cut into slices of W elements, the S
 partials of a slice stored together.
 """
@@ -41,9 +42,10 @@ def _rne_bf16(a32):
     return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
 
 
-def _expected(ws, sp, S, out_dtype):
+def _expected(ws, sp, S, out_dtype, depthwise_kernel):
     T = int(np.prod(sp["filt"]))
-    rows, L = sp["G"] * sp["K"], T * sp["C"]
+    # Tensor-core kernel: one row per (g, k); depthwise kernel: all of dW as one row.
+    rows, L = (1, sp["G"] * T) if depthwise_kernel else (sp["G"] * sp["K"], T * sp["C"])
     W = _slice_width(L)
     nj = -(-L // W)
     part = ws[: rows * nj * S * W].reshape(rows, nj, S, W)
@@ -74,13 +76,18 @@ CASES = [
     (spec(2, 1, 8, 64, 64, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16", "bf16"), 392),
     (spec(2, 4, 4, 16, 24, [20, 20], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "fp16", "fp16"), 12),
     (spec(3, 1, 2, 32, 32, [8, 8, 8], [3, 3, 3], [2, 2, 2], [1, 1, 1], [1, 1, 1], [1, 1, 1], "fp16", "fp32"), 16),
+    # depthwise kernel
+    (spec(2, 512, 8, 1, 1, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16", "fp32"), 19),
+    (spec(2, 64, 4, 1, 1, [20, 20], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16", "bf16"), 6),
 ]
 
 
 @pytest.mark.parametrize("case", range(len(CASES)))
 def test_reduction_order_bitwise(case):
     sp, S = CASES[case]
-    assert f" S={S} " in binding.wg_plan_string(sp, S, "deterministic", 0)
+    plan = binding.wg_plan_string(sp, S, "deterministic", 0)
+    assert f" S={S} " in plan
+    depthwise_kernel = plan.startswith("kernel=depthwise")
     x, dy = make_inputs(sp, ("uniform", -1.0, 1.0), 500 + case, 600 + case)
     idt = torch.bfloat16 if sp["in_dtype"] == "bf16" else torch.float16
     xd = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(idt).cuda()
@@ -93,5 +100,5 @@ def test_reduction_order_bitwise(case):
     binding.wg_conv_bwd_weight(sp, xd, dyd, dw, S, "deterministic", 0, ws, nb)
     binding.wg_check_status()
     got = dw.cpu().view(torch.int32 if odt == torch.float32 else torch.int16).numpy()
-    want = _expected(ws.cpu().numpy(), sp, S, sp["out_dtype"])
-    np.testing.assert_array_equal(got.view(want.dtype), want, err_msg=f"S={S}")
+    want = _expected(ws.cpu().numpy(), sp, S, sp["out_dtype"], depthwise_kernel)
+    np.testing.assert_array_equal(got.view(want.dtype), want, err_msg=plan)

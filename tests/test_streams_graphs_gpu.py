@@ -98,8 +98,10 @@ def test_graph_replay_matches_eager(split_k, mode):
         torch.cuda.synchronize()
         got = _bits(c.dw)
         if mode == "atomic":
-            # Atomic adds land in another order on every run: a few fp32 ulps.
-            np.testing.assert_allclose(got.view(np.float32), eager[seed].view(np.float32), rtol=1e-5, atol=1e-6)
+            # Atomic adds land in another order on every run: a few fp32 ulps of
+            # the partial sums, which can be far larger than a cancelled result.
+            e32 = eager[seed].view(np.float32)
+            np.testing.assert_allclose(got.view(np.float32), e32, rtol=0, atol=1e-5 * float(np.max(np.abs(e32))))
         else:
             np.testing.assert_array_equal(got, eager[seed])
     binding.wg_check_status()

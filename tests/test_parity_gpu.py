@@ -209,6 +209,31 @@ def test_3d_ragged_gemmk(split_k, mode):
     assert_close(got, dw, A, sp["out_dtype"], f"3-D ragged S={split_k} {mode}")
 
 
+LARGE = [
+    # wide channels: 8 channel chunks per tap, two N-tiles of K
+    spec(2, 1, 2, 512, 512, [7, 7], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], out_dtype="bf16"),
+    # large filter, large stride (11x11, stride 4), narrow input channels
+    spec(2, 1, 2, 8, 64, [35, 39], [11, 11], [4, 4], [1, 1], [2, 3], [2, 1]),
+    # long 1-D signal, 31 dilated taps
+    spec(1, 2, 2, 16, 16, [1500], [31], [1], [3], [45], [45], in_dtype="fp16"),
+    # anisotropic 3-D filter with groups
+    spec(3, 4, 2, 32, 32, [6, 9, 12], [3, 5, 7], [1, 1, 1], [1, 1, 1], [1, 2, 3], [1, 2, 3]),
+    # many images of 2x2
+    spec(2, 1, 512, 32, 48, [2, 2], [2, 2], [1, 1], [1, 1], [0, 0], [0, 0]),
+]
+
+
+@pytest.mark.parametrize("sp", LARGE, ids=_ids)
+def test_large_and_unusual_shapes(sp):
+    x, dy = make_inputs(sp, ("uniform", -1.0, 1.0), 57, 58)
+    dw, A = ref(sp, x, dy)
+    for split_k, mode in ((0, "auto"), (0, "atomic")):
+        if mode == "atomic" and sp["out_dtype"] != "fp32":
+            continue
+        got = run_gpu(sp, x, dy, split_k, mode)
+        assert_close(got, dw, A, sp["out_dtype"], f"{_ids(sp)} {mode}")
+
+
 def test_more_splits_than_tiles():
     sp = spec(2, 1, 1, 16, 32, [8, 8], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])
     x, dy = make_inputs(sp, ("int", -2, 2), 37, 38)

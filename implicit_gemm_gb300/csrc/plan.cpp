@@ -95,7 +95,7 @@ bool dim_phases(int F, int s, int d, DimPhases* o)
 
 struct IgCand {
     int halo, box[4], nt[4], KT, mt, stages, stage_bytes, patch[3], patch_bytes, n_patches, dy_off;
-    long long cost, tile_clk;
+    long long cost, tile_clk, S;
 };
 
 // Cost terms of the split-K epilogue, in SM cycles (GB300 at ~2 GHz): L2
@@ -105,6 +105,9 @@ struct IgCand {
 // shared memory at ~12 B/cycle (measured), plus two cluster barriers.
 constexpr long long kL2BytesPerClk = 2900;
 constexpr long long kReduceLaunchClk = 3000;
+// Cold reads from HBM, device-wide (~6 TB/s at ~2 GHz): no split degree reads
+// the inputs faster than this.
+constexpr long long kDramBytesPerClk = 3000;
 
 long long epilogue_clk(long long dw_bytes, int n_out, int Q, long long red_bytes, bool atomic)
 {
@@ -119,6 +122,20 @@ long long epilogue_clk(long long dw_bytes, int n_out, int Q, long long red_bytes
 }
 
 int cap_index(int q) { return q == 1 ? 0 : q == 2 ? 1 : q == 4 ? 2 : 3; }
+
+// Cycles the device needs to read the inputs once from HBM: all of dY, and the
+// part of X that some tap reaches (along each dim a fraction of about
+// min(1, dilated filter extent / stride) of the input positions: a quarter of
+// X for a 1x1 filter with stride 2).
+long long dram_read_clk(const Problem& pb)
+{
+    double frac = 1.0;
+    for (int i = 0; i < 3; ++i) {
+        const double extent = (double)(pb.filt[i] - 1) * pb.dil[i] + 1;
+        frac *= std::min(1.0, extent / pb.stride[i]);
+    }
+    return (long long)(2.0 * ((double)pb.x_elems * frac + (double)pb.dy_elems) / kDramBytesPerClk);
+}
 
 // Split degree without clusters: the caller's, 1 for mode DIRECT, else enough
 // splits of the K-tiles to fill the device once, evened out so that no split
@@ -227,24 +244,40 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
                 const long long load_clk = stage / 40;
                 long long tile_clk = std::max(mma_clk, load_clk) + 64;
                 if (stages < 3) tile_clk = tile_clk * 13 / 10;
-                // Whole-call estimate: the split degree this tiling gets (the
-                // caller's, or enough to fill the device once), the K-tiles of
-                // one split in waves of resident CTAs, and the partial sums that
-                // the splits write and the reduction reads back.
+                // Whole-call estimate for the split degrees this tiling may get
+                // (the caller's; else enough splits to fill the device once, or
+                // 3/4, 2/3 or 1/2 of that): the K-tiles of one split in waves of
+                // resident CTAs -- but no faster than the device reads the inputs
+                // from HBM -- plus the partial sums that the splits write and the
+                // reduction reads back.  Fewer splits pay when the cold read, not
+                // the per-SM loads, bounds the main loop (1x1 C 64 -> K 256:
+                // 23.3-23.8 us with S = 75-100 against 24.8 us with S = 150).
                 const long long base = mranges * ig.n_ntiles * ig.n_gblocks;
-                const long long S = split_for(o, base, ktiles, caps);
-                const long long waves = cdiv(base * S, caps.cluster_ctas[0]);
+                const long long s_fill = split_for(o, base, ktiles, caps);
+                const bool auto_s = o.split_k == 0 && o.mode != WG_MODE_DIRECT && o.cluster <= 1;
+                const long long dram_clk = dram_read_clk(pb);
                 const long long red_bytes = (long long)mt * ig.Nt * 512;
-                const long long cost = waves * cdiv(ktiles, S) * tile_clk +
-                                       epilogue_clk(pb.dw_elems * 4, (int)S, 1, red_bytes, o.mode == WG_MODE_ATOMIC);
-                if (best.cost < 0 || cost < best.cost) {
-                    c.mt = mt;
-                    c.stages = stages;
-                    c.stage_bytes = (int)stage;
-                    c.dy_off = n_x * c.patch_bytes;
-                    c.cost = cost;
-                    c.tile_clk = tile_clk;
-                    best = c;
+                for (int f = 0; f < (auto_s ? 4 : 1); ++f) {
+                    static const int num[4] = {1, 3, 2, 1}, den[4] = {1, 4, 3, 2};
+                    long long S = std::max(1LL, s_fill * num[f] / den[f]);
+                    if (f > 0) S = cdiv(ktiles, cdiv(ktiles, S));  // splits of whole, even K-tile counts
+                    // The per-CTA estimate also breaks ties between tilings whose
+                    // main loops all sit under the HBM bound (with weight 1/8).
+                    const long long waves = cdiv(base * S, caps.cluster_ctas[0]);
+                    const long long main_clk = waves * cdiv(ktiles, S) * tile_clk;
+                    const long long cost = std::max(main_clk, dram_clk) + main_clk / 8 +
+                                           epilogue_clk(pb.dw_elems * 4, (int)S, 1, red_bytes,
+                                                        o.mode == WG_MODE_ATOMIC);
+                    if (best.cost < 0 || cost < best.cost) {
+                        c.mt = mt;
+                        c.stages = stages;
+                        c.stage_bytes = (int)stage;
+                        c.dy_off = n_x * c.patch_bytes;
+                        c.cost = cost;
+                        c.tile_clk = tile_clk;
+                        c.S = S;
+                        best = c;
+                    }
                 }
             }
         }
@@ -341,7 +374,7 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
             if (o.cluster > 0 ? q != o.cluster : q != 1) continue;
             if (q > 1 && !cl_ok) continue;
             const long long fit = caps.cluster_ctas[cap_index(q)] / (base * q);
-            long long s = q * std::max(1LL, fit);
+            long long s = q == 1 && o.cluster <= 1 ? best.S : q * std::max(1LL, fit);
             s = std::min<long long>(s, round_up((int)std::min<long long>(ig.total_kt, 1 << 20), q));
             const long long per = cdiv(ig.total_kt, s);
             s = std::min<long long>(65535 / q * q, round_up((int)cdiv(ig.total_kt, per), q));

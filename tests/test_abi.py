@@ -223,6 +223,25 @@ def test_dgrad_group_fold():
     assert " Gm=2 " in binding.wg_bwd_data_plan_string(folded)
 
 
+def _plan_fields(ps):
+    return {k: v for k, v in re.findall(r"(\w+)=(\S+)", ps)}
+
+
+def test_planner_choices_on_default_caps():
+    # With the GB300 defaults (no device): the headline plan, split degrees below
+    # the device-filling one where the cold HBM read bounds the main loop, and
+    # explicit split degrees that keep well-shaped pixel tiles (a cost floor
+    # must not make every tiling tie).
+    dense = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_dense_n32_h56_c64_k64"][0]))
+    assert (dense["S"], dense["mt_per_cta"], dense["box"]) == ("75", "3", "(w8,h7,d1,n4)")
+    one = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_1x1_n32_h56_c64_k256"][0]))
+    assert int(one["S"]) < 150
+    for S in (75, 100, 150):
+        p = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_1x1_n32_h56_c64_k256"][0], S, "deterministic", 0))
+        h = int(p["box"].split(",")[1][1:])
+        assert p["S"] == str(S) and h >= 4, p["box"]
+
+
 def _dg_fields(ps):
     return {k: v for k, v in re.findall(r"(\w+)=(\S+)", ps)}
 

@@ -44,7 +44,8 @@ class WgradError(RuntimeError):
 
 EXPORTS = ("wg_problem_normalize", "wg_workspace_size", "wg_conv_bwd_weight", "wg_check_status",
            "wg_plan_string", "wg_status_string", "wg_last_error", "wg_conv_bwd_weight_noalloc",
-           "wg_set_mark_event", "wg_conv_bwd_data", "wg_bwd_data_plan_string", "wg_bwd_data_workspace_size", "wg_conv_bwd_weight_host")
+           "wg_set_mark_event", "wg_conv_bwd_data", "wg_bwd_data_plan_string", "wg_bwd_data_workspace_size",
+           "wg_conv_bwd_weight_host", "wg_selftest_timeout")
 
 _lib = None
 _lock = threading.Lock()
@@ -73,6 +74,7 @@ def load():
             lib.wg_conv_bwd_weight_host.argtypes = [P] + [ctypes.c_void_p] * 6 + [O, ctypes.c_void_p, ctypes.c_size_t,
                                                                                   ctypes.c_void_p]
             lib.wg_check_status.argtypes = [ctypes.c_void_p]
+            lib.wg_selftest_timeout.argtypes = [ctypes.c_void_p]
             lib.wg_set_mark_event.argtypes = [ctypes.c_void_p]
             lib.wg_conv_bwd_data.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                              ctypes.c_size_t, ctypes.c_void_p]
@@ -281,6 +283,11 @@ def wg_set_mark_event(event) -> None:
     A torch event must have been recorded once, so that it exists."""
     h = None if event is None else (event if isinstance(event, int) else int(event.cuda_event))
     _check(load().wg_set_mark_event(h))
+
+
+def wg_selftest_timeout(stream=None) -> None:
+    """Launch the library's bounded-wait self-test (see include/wgrad.h)."""
+    _check(load().wg_selftest_timeout(_stream_handle(stream)))
 
 
 def wg_check_status(stream=None) -> None:

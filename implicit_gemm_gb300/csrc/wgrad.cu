@@ -19,6 +19,22 @@
 
 static_assert(wg::kDgStaging == wg::kDgStagingBytes, "planner and kernel disagree on the dgrad staging size");
 
+namespace wg {
+
+// One thread waits on an mbarrier that nothing completes: the bounded wait
+// runs out, sets the status word and returns (wg_selftest_timeout).
+__global__ void selftest_timeout_kernel()
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        (void)mbar_wait(&bar, 0);
+    }
+}
+
+}  // namespace wg
+
 namespace {
 
 thread_local std::string g_err;
@@ -624,6 +640,14 @@ int wg_conv_bwd_weight_host(const wg_problem* p, const void* x_host, const void*
     if ((st = launch_call(pl, pr, dw_dev, workspace, s))) return st;
     if ((e = cudaMemcpyAsync(dw_host, dw_dev, dw_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
         return cuda_fail("cudaMemcpyAsync(dW)", e);
+    return WG_OK;
+}
+
+int wg_selftest_timeout(void* stream)
+{
+    wg::selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail("selftest_timeout_kernel launch", e);
     return WG_OK;
 }
 

@@ -215,6 +215,14 @@ WG_API int wg_conv_bwd_weight_host(const wg_problem* p, const void* x_host, cons
                                    void* x_dev, void* dy_dev, void* dw_dev, const wg_options* opt, void* workspace,
                                    size_t ws_bytes, void* stream);
 
+/* Self-test of failure detection (no counterpart in the CK page).  Launches
+ * one thread on `stream` that waits on an mbarrier which nothing completes:
+ * the wait is bounded like every wait in the library's kernels, runs out
+ * after the library's limit (2 s), sets the device status word and returns.
+ * The next wg_check_status then returns WG_ERR_DEVICE_TIMEOUT (and clears
+ * the word); the context stays usable.  Returns WG_OK or WG_ERR_CUDA (launch). */
+WG_API int wg_selftest_timeout(void* stream);
+
 /* Measurement hook (no counterpart in the CK page: it exists so that the
  * kernels of one call can be timed separately with CUDA events).  While
  * `event` (a cudaEvent_t owned by the caller, valid while set) is non-NULL,

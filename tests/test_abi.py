@@ -78,6 +78,20 @@ def test_not_supported_paths():
     assert e.value.status == 1
 
 
+def test_size_limits():
+    # Tensors of 2^31 elements or more and split degrees above 65535 are refused
+    # before anything is planned on a device.
+    big = spec(2, 1, 70000, 128, 128, [128, 128], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_workspace_size(big)
+    assert e.value.status == 2 and "2^31" in binding.wg_last_error()
+    small = spec(2, 1, 2, 16, 16, [8, 8], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_workspace_size(small, split_k=70000, mode="deterministic")
+    assert e.value.status == 2
+    assert binding.wg_workspace_size(small, split_k=65535, mode="deterministic") > 0
+
+
 def test_workspace_sizes():
     sp = WORKLOADS["2d_dense_n32_h56_c64_k64"][0]
     E = 1 * 64 * 9 * 64  # rows of 576 = 6 slices of 96: no padding

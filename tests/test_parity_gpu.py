@@ -209,6 +209,26 @@ def test_3d_ragged_gemmk(split_k, mode):
     assert_close(got, dw, A, sp["out_dtype"], f"3-D ragged S={split_k} {mode}")
 
 
+DEGENERATE = [
+    # the filter covers the whole image: one output position per image
+    spec(2, 2, 3, 16, 24, [7, 9], [7, 9]),
+    # a 1x1 image with a 1x1 filter; a 1x1 image with a 3x3 filter and pad 1
+    spec(2, 1, 5, 16, 16, [1, 1], [1, 1]),
+    spec(2, 1, 4, 32, 16, [1, 1], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
+    # stride larger than the filter: input positions no tap reaches
+    spec(2, 1, 2, 16, 16, [13, 13], [2, 2], [5, 5]),
+]
+
+
+@pytest.mark.parametrize("sp", DEGENERATE, ids=_ids)
+def test_degenerate_shapes_bitwise(sp):
+    x, dy = make_inputs(sp, ("int", -2, 2), 67, 68)
+    dw, _ = ref(sp, x, dy)
+    for split_k, mode in ((0, "auto"), (1, "direct"), (0, "atomic")):
+        got = run_gpu(sp, x, dy, split_k, mode)
+        np.testing.assert_array_equal(got, dw, err_msg=f"{_ids(sp)} {mode}")
+
+
 LARGE = [
     # wide channels: 8 channel chunks per tap, two N-tiles of K
     spec(2, 1, 2, 512, 512, [7, 7], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], out_dtype="bf16"),

@@ -55,6 +55,10 @@ struct IgParams {
     int per_split, total_kt;
     int Gm, Nt, n_ntiles, n_katoms, n_atoms, n_mtiles, mtpc;
     int halo;
+    // Tap form: xs = 0, every tap on the MMA rows; xs = X, the x taps on the
+    // columns (atoms are (z, y, chunk); B atom j = tap x = xs-1-j of one dY
+    // patch per K-tile, dy_xoff = (X-1)*dil_w columns of it left of the tile).
+    int xs, Nmma, dy_tx, dy_xoff;
     int patch[3];
     int patch_bytes, patch_tx;
     int n_patches, dy_off, slot_bytes, stage_bytes, stages;
@@ -73,6 +77,8 @@ struct IgParams {
     // the step's first 8-pixel group (start-address field) and the byte offset
     // of its second group (SBO field).  Filled on the host.
     unsigned long long kd_table[16];
+    // The same for the B operand when xs > 0 (rows of the dY patch).
+    unsigned long long kd_table_b[16];
 };
 
 // Up to kEpiCols consecutive TMEM columns (n a multiple of 16) with one wait:
@@ -227,7 +233,7 @@ __device__ __forceinline__ void cluster_reduce_store(const IgParams& p, uint32_t
 
 struct MmaArgs {
     uint64_t b0;        // dY descriptor of stage 0, K-step 0
-    uint32_t idesc, Nt, stage16;
+    uint32_t idesc, Nt, stage16;  // Nt: TMEM columns per M-tile (the MMA N)
     int ksteps, stages;
 };
 
@@ -238,10 +244,11 @@ struct MmaArgs {
 // the stage offset.  The K-step loop is unrolled against the parameter table:
 // descriptor operands built from runtime geometry inside the loop halved the
 // MMA issue rate.
-template <int MT>
+template <int MT, bool XS>
 __device__ __forceinline__ void mma_mainloop(const MmaArgs a, const uint64_t (&ab)[kMaxMt], uint64_t* full,
                                              uint64_t* empty, uint64_t* accb, uint32_t tbase, int nk,
-                                             const unsigned long long* __restrict__ kdt)
+                                             const unsigned long long* __restrict__ kdt,
+                                             const unsigned long long* __restrict__ kdtb)
 {
     const uint64_t b0 = a.b0;
     const uint32_t idesc = a.idesc, Nt = a.Nt, stage16 = a.stage16;
@@ -256,7 +263,7 @@ __device__ __forceinline__ void mma_mainloop(const MmaArgs a, const uint64_t (&a
         for (int ks = 0; ks < 16; ++ks) {
             if (ks >= ksteps) break;
             const uint64_t kd = kdt[ks] + soff;
-            const uint64_t bdesc = b0 + soff + (uint64_t)(ks * 128);
+            const uint64_t bdesc = XS ? b0 + soff + kdtb[ks] : b0 + soff + (uint64_t)(ks * 128);
             const uint32_t acc = (i | ks) != 0 ? 1u : 0u;
             if (elect_one()) {
 #pragma unroll
@@ -325,14 +332,14 @@ __global__ void __launch_bounds__(kIgThreads, 1)
         tc_fence_after();
         tbase = *tslot;
     }
-#define MMA_ARGS ma, ab, full, empty, accb, tbase, nk, p.kd_table
+#define MMA_ARGS ma, ab, full, empty, accb, tbase, nk, p.kd_table, p.kd_table_b
 
     if (warp == 0) {
         if (lane == 0 && nk > 0) {
             // ------------------------------------------------ TMA producer
             tma_prefetch_desc(&tmx);
             tma_prefetch_desc(&tmy);
-            const uint32_t tx = (uint32_t)(p.n_patches * p.patch_tx + p.n_katoms * p.slot_bytes);
+            const uint32_t tx = (uint32_t)(p.n_patches * p.patch_tx + p.dy_tx);
             for (int i = 0; i < nk; ++i) {
                 const int st = i % p.stages;
                 const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
@@ -367,7 +374,8 @@ __global__ void __launch_bounds__(kIgThreads, 1)
                     }
                 }
                 for (int j = 0; j < p.n_katoms; ++j)
-                    tma_load_5d(sb + p.dy_off + j * p.slot_bytes, &tmy, &full[st], k_base + 64 * j, wo0, ho0, do0, n0);
+                    tma_load_5d(sb + p.dy_off + j * p.slot_bytes, &tmy, &full[st], k_base + 64 * j, wo0 - p.dy_xoff,
+                                ho0, do0, n0);
             }
         }
     } else if (warp == 1) {
@@ -392,26 +400,38 @@ __global__ void __launch_bounds__(kIgThreads, 1)
                 }
             }
             MmaArgs ma;
-            ma.b0 = make_sdesc(sbase + (uint32_t)p.dy_off, (uint32_t)p.slot_bytes, 1024u, 2u, 0u);
-            ma.idesc = p.idesc, ma.Nt = (uint32_t)Nt, ma.stage16 = (uint32_t)stage_bytes >> 4;
+            ma.idesc = p.idesc, ma.Nt = (uint32_t)p.Nmma, ma.stage16 = (uint32_t)stage_bytes >> 4;
             ma.ksteps = ksteps, ma.stages = stages;
-            switch (mtn) {
-                case 1: mma_mainloop<1>(MMA_ARGS); break;
-                case 2: mma_mainloop<2>(MMA_ARGS); break;
-                case 3: mma_mainloop<3>(MMA_ARGS); break;
-                case 4: mma_mainloop<4>(MMA_ARGS); break;
-                case 5: mma_mainloop<5>(MMA_ARGS); break;
-                case 6: mma_mainloop<6>(MMA_ARGS); break;
-                case 7: mma_mainloop<7>(MMA_ARGS); break;
-                case 8: mma_mainloop<8>(MMA_ARGS); break;
-                case 9: mma_mainloop<9>(MMA_ARGS); break;
-                case 10: mma_mainloop<10>(MMA_ARGS); break;
-                case 11: mma_mainloop<11>(MMA_ARGS); break;
-                case 12: mma_mainloop<12>(MMA_ARGS); break;
-                case 13: mma_mainloop<13>(MMA_ARGS); break;
-                case 14: mma_mainloop<14>(MMA_ARGS); break;
-                case 15: mma_mainloop<15>(MMA_ARGS); break;
-                default: mma_mainloop<16>(MMA_ARGS); break;
+            if (p.xs) {
+                // One dY patch: B atom j starts j*dil_w rows in (LBO); the K-step
+                // part (start row, SBO) comes from kd_table_b.
+                ma.b0 = make_sdesc(sbase + (uint32_t)p.dy_off, (uint32_t)(p.d[0] * 128), 0u, 2u, 0u);
+                switch (mtn) {
+                    case 1: mma_mainloop<1, true>(MMA_ARGS); break;
+                    case 2: mma_mainloop<2, true>(MMA_ARGS); break;
+                    case 3: mma_mainloop<3, true>(MMA_ARGS); break;
+                    default: mma_mainloop<4, true>(MMA_ARGS); break;
+                }
+            } else {
+                ma.b0 = make_sdesc(sbase + (uint32_t)p.dy_off, (uint32_t)p.slot_bytes, 1024u, 2u, 0u);
+                switch (mtn) {
+                    case 1: mma_mainloop<1, false>(MMA_ARGS); break;
+                    case 2: mma_mainloop<2, false>(MMA_ARGS); break;
+                    case 3: mma_mainloop<3, false>(MMA_ARGS); break;
+                    case 4: mma_mainloop<4, false>(MMA_ARGS); break;
+                    case 5: mma_mainloop<5, false>(MMA_ARGS); break;
+                    case 6: mma_mainloop<6, false>(MMA_ARGS); break;
+                    case 7: mma_mainloop<7, false>(MMA_ARGS); break;
+                    case 8: mma_mainloop<8, false>(MMA_ARGS); break;
+                    case 9: mma_mainloop<9, false>(MMA_ARGS); break;
+                    case 10: mma_mainloop<10, false>(MMA_ARGS); break;
+                    case 11: mma_mainloop<11, false>(MMA_ARGS); break;
+                    case 12: mma_mainloop<12, false>(MMA_ARGS); break;
+                    case 13: mma_mainloop<13, false>(MMA_ARGS); break;
+                    case 14: mma_mainloop<14, false>(MMA_ARGS); break;
+                    case 15: mma_mainloop<15, false>(MMA_ARGS); break;
+                    default: mma_mainloop<16, false>(MMA_ARGS); break;
+                }
             }
         }
     }
@@ -427,9 +447,10 @@ __global__ void __launch_bounds__(kIgThreads, 1)
         }
         const int q = warp & 3;
         const int row = q * 32 + lane;
-        // Column half of this warp: [c_lo, c_hi), split at a multiple of 16.
-        const int c_mid = ((Nt >> 1) + 15) & ~15;
-        const int c_lo = warp < 4 ? 0 : c_mid, c_hi = warp < 4 ? c_mid : Nt;
+        // Column half of this warp: [c_lo, c_hi) of the MMA N, split at a multiple of 16.
+        const int Nmma = p.Nmma;
+        const int c_mid = ((Nmma >> 1) + 15) & ~15;
+        const int c_lo = warp < 4 ? 0 : c_mid, c_hi = warp < 4 ? c_mid : Nmma;
         const int K = p.K, C = p.C, T = p.T, GC = p.GC, Gm = p.Gm, n_atoms = p.n_atoms, ncc = p.ncc, mode = p.mode;
         const int out_dtype = p.out_dtype;
         void* const out = p.out;
@@ -474,27 +495,40 @@ __global__ void __launch_bounds__(kIgThreads, 1)
             const int c = cg - gr * C;
             vrow = vrow && cg < GC && gr >= g0 && gr < g0 + Gm;
             const int n_lo = gr * K - k_base;
-            const long long rowbase = ((long long)gr * K * T + tap) * C + c;
             const long long kstride = (long long)T * C;
-            const uint32_t ta = trow + (uint32_t)(m * Nt + c_lo);
-            const int nc = c_hi - c_lo, nl = n_lo - c_lo;
-            if (mode == 3) {
-                // Workspace: the row's first element (k = 0) and the step per k.
-                const long long x = (long long)tap * C + c;
-                const long long j = x / p.ws.W;
-                const long long wbase = (((long long)gr * K * p.ws.nj + j) * p.ws.S + ws_s) * p.ws.W + (x - j * p.ws.W);
-                epilogue_mtile<3, float>(ta, nc, have_acc, vrow, nl, K, static_cast<float*>(out), wbase,
-                                         (long long)p.ws.nj * p.ws.S * p.ws.W);
-            } else if (mode == 2) {
-                if (have_acc)
-                    epilogue_mtile<2, float>(ta, nc, true, vrow, nl, K, static_cast<float*>(out), rowbase, kstride);
-            } else if (out_dtype == 2) {
-                epilogue_mtile<1, float>(ta, nc, have_acc, vrow, nl, K, static_cast<float*>(out), rowbase, kstride);
-            } else if (out_dtype == 0) {
-                epilogue_mtile<1, __nv_bfloat16>(ta, nc, have_acc, vrow, nl, K, static_cast<__nv_bfloat16*>(out),
-                                                 rowbase, kstride);
-            } else {
-                epilogue_mtile<1, __half>(ta, nc, have_acc, vrow, nl, K, static_cast<__half*>(out), rowbase, kstride);
+            // Column blocks: the whole N-tile, or with the x taps on the
+            // columns one 64-column block per tap x = xs-1-jb (the atom's tap
+            // entry is that of x = 0).
+            const int nblk = p.xs ? p.xs : 1, bw = p.xs ? 64 : Nmma;
+            for (int jb = 0; jb < nblk; ++jb) {
+                const int lo = max(c_lo, jb * bw), hi = min(c_hi, jb * bw + bw);
+                if (lo >= hi) continue;
+                const int tapj = p.xs ? tap + (p.xs - 1 - jb) : tap;
+                const long long rowbase = ((long long)gr * K * T + tapj) * C + c;
+                const uint32_t ta = trow + (uint32_t)(m * Nmma + lo);
+                const int nc = hi - lo, nl = n_lo - (lo - jb * bw);
+                if (mode == 3) {
+                    // Workspace: the row's first element (k = 0) and the step per k.
+                    const long long x = (long long)tapj * C + c;
+                    const long long j = x / p.ws.W;
+                    const long long wbase =
+                        (((long long)gr * K * p.ws.nj + j) * p.ws.S + ws_s) * p.ws.W + (x - j * p.ws.W);
+                    epilogue_mtile<3, float>(ta, nc, have_acc, vrow, nl, K, static_cast<float*>(out), wbase,
+                                             (long long)p.ws.nj * p.ws.S * p.ws.W);
+                } else if (mode == 2) {
+                    if (have_acc)
+                        epilogue_mtile<2, float>(ta, nc, true, vrow, nl, K, static_cast<float*>(out), rowbase,
+                                                 kstride);
+                } else if (out_dtype == 2) {
+                    epilogue_mtile<1, float>(ta, nc, have_acc, vrow, nl, K, static_cast<float*>(out), rowbase,
+                                             kstride);
+                } else if (out_dtype == 0) {
+                    epilogue_mtile<1, __nv_bfloat16>(ta, nc, have_acc, vrow, nl, K,
+                                                     static_cast<__nv_bfloat16*>(out), rowbase, kstride);
+                } else {
+                    epilogue_mtile<1, __half>(ta, nc, have_acc, vrow, nl, K, static_cast<__half*>(out), rowbase,
+                                              kstride);
+                }
             }
         }
     }

@@ -50,11 +50,13 @@ int fail(std::string* err, int status, const char* fmt, ...)
 
 // Candidate pixel tiles (w, h, d, n) for the tensor-core path: KT = product, a
 // multiple of 16 (the MMA K of kind::f16) and at most 256; each extent at most
-// the (rounded-up) output extent.  With w8 the w extent is a multiple of 8, so
-// that every 8-pixel K group is one contiguous run of a halo patch row.
-void enumerate_tiles(const Problem& pb, bool w8, std::vector<std::array<int, 4>>* out)
+// the (rounded-up) extent of the pixel index space (Wo along w, or the wider
+// shifted range of the x-taps-on-columns form).  With w8 the w extent is a
+// multiple of 8, so that every 8-pixel K group is one contiguous run of a
+// halo patch row.
+void enumerate_tiles(const Problem& pb, int Wo, bool w8, std::vector<std::array<int, 4>>* out)
 {
-    const int Wo = pb.out[2], Ho = pb.out[1], Do = pb.out[0], N = pb.N;
+    const int Ho = pb.out[1], Do = pb.out[0], N = pb.N;
     const int lim_w = std::min(256 / pb.stride[2], round_up(Wo, w8 ? 8 : 16));
     const int lim_h = std::min(256 / pb.stride[1], pow2_at_least(Ho));
     const int lim_d = std::min(256 / pb.stride[0], pow2_at_least(Do));
@@ -95,6 +97,7 @@ bool dim_phases(int F, int s, int d, DimPhases* o)
 
 struct IgCand {
     int halo, box[4], nt[4], KT, mt, stages, stage_bytes, patch[3], patch_bytes, n_patches, dy_off;
+    int xs, Nt, n_ntiles, n_katoms, n_atoms, n_mtiles, Nmma, dy_w, dy_bytes;
     long long cost, tile_clk, S;
 };
 
@@ -187,23 +190,60 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
 
     // Stride phases per dim, in (w, h, d) order.
     DimPhases ph[3];
-    bool halo_ok = ig.n_atoms <= kMaxHaloAtoms;
-    for (int i = 0; i < 3; ++i) halo_ok = dim_phases(pb.filt[2 - i], pb.stride[2 - i], pb.dil[2 - i], &ph[i]) && halo_ok;
+    bool ph_ok = true;
+    for (int i = 0; i < 3; ++i) ph_ok = dim_phases(pb.filt[2 - i], pb.stride[2 - i], pb.dil[2 - i], &ph[i]) && ph_ok;
+    bool halo_ok = ph_ok && ig.n_atoms <= kMaxHaloAtoms;
     const int n_combos = halo_ok ? ph[0].nph * ph[1].nph * ph[2].nph : 0;
     if (halo_ok && n_combos * ig.n_cchunks > kMaxPatches) halo_ok = false;
 
+    // The x taps on the MMA columns (IgemmPlan::xs) need stride 1 (then a shift
+    // of the pixel index along w is a shift of dY), whole 64-wide k atoms of one
+    // group, and at most 256 columns.
+    const int X = pb.filt[2], Y = pb.filt[1], Z = pb.filt[0];
+    const char* mn_no = nullptr;
+    if (pb.stride[0] != 1 || pb.stride[1] != 1 || pb.stride[2] != 1)
+        mn_no = "stride 1 in every dim";
+    else if (Gm != 1)
+        mn_no = "one group per tile (no group fold)";
+    else if (pb.K % 64)
+        mn_no = "K a multiple of 64";
+    else if (X < 2 || X > 4)
+        mn_no = "2 to 4 filter taps along w";
+    else if (o.cluster > 1)
+        mn_no = "no cluster reduction";
+    else if (!ph_ok || ig.n_cchunks > kMaxPatches || (long long)Z * Y * ig.n_cchunks > kMaxHaloAtoms)
+        mn_no = "one halo patch per channel chunk";
+    if (o.kernel == WG_KERNEL_IGEMM_TAPS_MN && mn_no)
+        return fail(err, WG_ERR_NOT_SUPPORTED, "the x-taps-on-columns tile needs %s", mn_no);
+    const bool try_m = o.kernel != WG_KERNEL_IGEMM_TAPS_MN;
+    const bool try_mn = !mn_no && o.kernel != WG_KERNEL_IGEMM_TAPS_M;
+
     const int avail = kMaxSmemPerCta - 3072;
-    const int mt_max = std::min({ig.n_mtiles, kMaxTmemCols / ig.Nt, kMaxMtPerCta});
     IgCand best{};
     best.cost = -1;
     std::vector<std::array<int, 4>> tiles;
-    for (int halo = halo_ok ? 1 : 0; halo >= 0; --halo) {
-        enumerate_tiles(pb, halo != 0, &tiles);
+    // Forms: 2 = x taps on the columns (halo patches), 1 = every tap on the
+    // rows with halo patches, 0 = every tap on the rows with per-tap boxes.
+    for (int form = 2; form >= 0; --form) {
+        if (form == 2 ? !try_mn : (!try_m || (form == 1 && !halo_ok))) continue;
+        const bool mn = form == 2;
+        const int halo = form >= 1 ? 1 : 0;
+        IgCand f{};
+        f.xs = mn ? X : 0;
+        f.Nt = mn ? 64 : ig.Nt;
+        f.n_ntiles = mn ? pb.K / 64 : ig.n_ntiles;
+        f.n_katoms = mn ? 1 : ig.n_katoms;
+        f.n_atoms = mn ? Z * Y * ig.n_cchunks : ig.n_atoms;
+        f.n_mtiles = (int)cdiv(f.n_atoms, 2);
+        f.Nmma = mn ? 64 * X : ig.Nt;
+        const int wq = mn ? pb.out[2] + (X - 1) * pb.dil[2] : pb.out[2];
+        const int mt_max = std::min({f.n_mtiles, kMaxTmemCols / f.Nmma, kMaxMtPerCta});
+        enumerate_tiles(pb, wq, halo != 0, &tiles);
         for (const auto& t : tiles) {
-            IgCand c{};
+            IgCand c = f;
             c.halo = halo;
             for (int i = 0; i < 4; ++i) c.box[i] = t[i];
-            c.nt[0] = (int)cdiv(pb.out[2], c.box[0]);
+            c.nt[0] = (int)cdiv(wq, c.box[0]);
             c.nt[1] = (int)cdiv(pb.out[1], c.box[1]);
             c.nt[2] = (int)cdiv(pb.out[0], c.box[2]);
             c.nt[3] = (int)cdiv(pb.N, c.box[3]);
@@ -212,22 +252,30 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
             if (halo) {
                 bool fits = true;
                 for (int i = 0; i < 3; ++i) {
-                    c.patch[i] = c.box[i] + ph[i].qmax;
+                    c.patch[i] = c.box[i] + (mn && i == 0 ? 0 : ph[i].qmax);
                     if (c.patch[i] * pb.stride[2 - i] > 256) fits = false;
                 }
                 if (!fits) continue;
                 const long long rows = (long long)c.patch[0] * c.patch[1] * c.patch[2] * c.box[3];
                 if (rows * 128 > avail) continue;
                 c.patch_bytes = round_up((int)(rows * 128), 1024);
-                c.n_patches = n_combos * ig.n_cchunks;
+                c.n_patches = (mn ? 1 : n_combos) * ig.n_cchunks;
             } else {
                 for (int i = 0; i < 3; ++i) c.patch[i] = c.box[i];
                 c.patch_bytes = slot;
             }
+            // dY staging: the K-tile's 64-channel boxes, or one patch widened
+            // by the x taps' shifts.
+            c.dy_w = mn ? c.box[0] + (X - 1) * pb.dil[2] : c.box[0];
+            if (c.dy_w > 256) continue;
+            const long long dy_bytes = mn ? (long long)c.dy_w * c.box[1] * c.box[2] * c.box[3] * 128
+                                          : (long long)c.n_katoms * slot;
+            if (dy_bytes > avail) continue;
+            c.dy_bytes = (int)dy_bytes;
             const long long ktiles = (long long)c.nt[0] * c.nt[1] * c.nt[2] * c.nt[3];
             for (int mt = mt_max; mt >= 1; --mt) {
                 const int n_x = halo ? c.n_patches : 2 * mt;
-                const long long stage = (long long)n_x * c.patch_bytes + (long long)ig.n_katoms * slot;
+                const long long stage = ((long long)n_x * c.patch_bytes + c.dy_bytes + 1023) / 1024 * 1024;
                 if (stage > avail) continue;
                 const int stages = std::min(8, (int)(avail / stage));
                 if (stages < 2) continue;
@@ -238,8 +286,8 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
                 // workload, where 2, 3 and 5 M-tiles per CTA measured 27.6,
                 // 24.7 and 26.5 us), plus a fixed overhead; fewer than 3 stages
                 // exposes latency.
-                const long long mranges = cdiv(ig.n_mtiles, mt);
-                const long long mma_one = std::max<long long>(ig.Nt / 2, 32 + ig.Nt / 4);
+                const long long mranges = cdiv(c.n_mtiles, mt);
+                const long long mma_one = std::max<long long>(c.Nmma / 2, 32 + c.Nmma / 4);
                 const long long mma_clk = (long long)mt * (c.KT / 16) * mma_one;
                 const long long load_clk = stage / 40;
                 long long tile_clk = std::max(mma_clk, load_clk) + 64;
@@ -252,15 +300,15 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
                 // reduction reads back.  Fewer splits pay when the cold read, not
                 // the per-SM loads, bounds the main loop (1x1 C 64 -> K 256:
                 // 23.3-23.8 us with S = 75-100 against 24.8 us with S = 150).
-                const long long base = mranges * ig.n_ntiles * ig.n_gblocks;
+                const long long base = mranges * c.n_ntiles * ig.n_gblocks;
                 const long long s_fill = split_for(o, base, ktiles, caps);
                 const bool auto_s = o.split_k == 0 && o.mode != WG_MODE_DIRECT && o.cluster <= 1;
                 const long long dram_clk = dram_read_clk(pb);
-                const long long red_bytes = (long long)mt * ig.Nt * 512;
-                for (int f = 0; f < (auto_s ? 4 : 1); ++f) {
+                const long long red_bytes = (long long)mt * c.Nmma * 512;
+                for (int fi = 0; fi < (auto_s ? 4 : 1); ++fi) {
                     static const int num[4] = {1, 3, 2, 1}, den[4] = {1, 4, 3, 2};
-                    long long S = std::max(1LL, s_fill * num[f] / den[f]);
-                    if (f > 0) S = cdiv(ktiles, cdiv(ktiles, S));  // splits of whole, even K-tile counts
+                    long long S = std::max(1LL, s_fill * num[fi] / den[fi]);
+                    if (fi > 0) S = cdiv(ktiles, cdiv(ktiles, S));  // splits of whole, even K-tile counts
                     // The per-CTA estimate also breaks ties between tilings whose
                     // main loops all sit under the HBM bound (with weight 1/8).
                     const long long waves = cdiv(base * S, caps.cluster_ctas[0]);
@@ -284,6 +332,15 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
     }
     if (best.cost < 0) return fail(err, WG_ERR_NOT_SUPPORTED, "no tile configuration fits shared memory");
     ig.halo = best.halo;
+    ig.xs = best.xs;
+    ig.Nt = best.Nt;
+    ig.n_ntiles = best.n_ntiles;
+    ig.n_katoms = best.n_katoms;
+    ig.n_atoms = best.n_atoms;
+    ig.n_mtiles = best.n_mtiles;
+    ig.Nmma = best.Nmma;
+    ig.dy_w = best.dy_w;
+    ig.dy_bytes = best.dy_bytes;
     std::memcpy(ig.box, best.box, sizeof best.box);
     std::memcpy(ig.ntile, best.nt, sizeof best.nt);
     std::memcpy(ig.patch, best.patch, sizeof best.patch);
@@ -294,12 +351,12 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
     ig.mt_per_cta = (int)cdiv(ig.n_mtiles, ig.n_mranges);
     ig.n_patches = ig.halo ? best.n_patches : 2 * ig.mt_per_cta;
     ig.dy_off = ig.n_patches * ig.patch_bytes;
-    ig.stage_bytes = ig.dy_off + ig.n_katoms * ig.slot_bytes;
+    ig.stage_bytes = round_up(ig.dy_off + ig.dy_bytes, 1024);
     ig.stages = std::min(8, avail / ig.stage_bytes);
     // Stage buffers, then 1 KB of slack that a padding atom's reads may reach,
     // then 1 KB of barriers and tables; plus 1 KB to align the base.
     ig.smem_bytes = ig.stages * ig.stage_bytes + 3072;
-    ig.tmem_cols = std::max(32, pow2_at_least(ig.mt_per_cta * ig.Nt));
+    ig.tmem_cols = std::max(32, pow2_at_least(ig.mt_per_cta * ig.Nmma));
     ig.total_kt = (long long)ig.ntile[0] * ig.ntile[1] * ig.ntile[2] * ig.ntile[3];
     ig.est_cycles = best.cost / std::max(1, num_sms);
     ig.tile_clk = best.tile_clk;
@@ -322,10 +379,12 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
         struct At { unsigned off; int tap, cc; };
         At at[kMaxHaloAtoms];
         int na = 0;
-        const int X = pb.filt[2], Y = pb.filt[1], Z = pb.filt[0];
+        // With the x taps on the columns an atom is (z, y, chunk) and its tap
+        // entry is that of x = 0; the epilogue adds each column block's x.
+        const int XA = ig.xs ? 1 : X;
         for (int z = 0; z < Z; ++z)
             for (int y = 0; y < Y; ++y)
-                for (int x = 0; x < X; ++x)
+                for (int x = 0; x < XA; ++x)
                     for (int cc = 0; cc < ig.n_cchunks; ++cc) {
                         const int combo = (ph[2].phidx[z] * ph[1].nph + ph[1].phidx[y]) * ph[0].nph + ph[0].phidx[x];
                         const int patch = combo * ig.n_cchunks + cc;
@@ -348,7 +407,7 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
     if (base > 65535LL * 65535LL) return fail(err, WG_ERR_NOT_SUPPORTED, "grid too large");
     // Cluster reduction: the CTA's partial sums (mt_per_cta * Nt columns of 128
     // fp32 rows) are staged in its pipeline buffers.
-    const long long red_bytes = (long long)ig.mt_per_cta * ig.Nt * 128 * 4;
+    const long long red_bytes = (long long)ig.mt_per_cta * ig.Nmma * 128 * 4;
     const bool cl_ok = red_bytes <= (long long)ig.stages * ig.stage_bytes;
     if (o.cluster > 1 && !cl_ok)
         return fail(err, WG_ERR_NOT_SUPPORTED,
@@ -561,7 +620,7 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
         return fail(err, WG_ERR_INVALID_ARGUMENT, "group_merge must be 0, 1, 2, 4 or 8");
     if (o.cluster != 0 && o.cluster != 1 && o.cluster != 2 && o.cluster != 4 && o.cluster != 8)
         return fail(err, WG_ERR_INVALID_ARGUMENT, "cluster must be 0, 1, 2, 4 or 8");
-    if (o.kernel < WG_KERNEL_AUTO || o.kernel > WG_KERNEL_DEPTHWISE)
+    if (o.kernel < WG_KERNEL_AUTO || o.kernel > WG_KERNEL_IGEMM_TAPS_MN)
         return fail(err, WG_ERR_INVALID_ARGUMENT, "bad kernel selector");
     if (o.mode == WG_MODE_DIRECT && o.split_k > 1 && o.split_k != o.cluster)
         return fail(err, WG_ERR_INVALID_ARGUMENT,
@@ -574,7 +633,8 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
     const bool depthwise = pb.C == 1 && pb.K == 1;
     if (o.group_merge > 1 && !depthwise)
         return fail(err, WG_ERR_NOT_SUPPORTED, "group_merge > 1 is for depthwise problems (C = K = 1) only");
-    const bool use_dw = depthwise && dw_eligible(pb) && o.kernel != WG_KERNEL_IGEMM;
+    const bool use_dw =
+        depthwise && dw_eligible(pb) && (o.kernel == WG_KERNEL_AUTO || o.kernel == WG_KERNEL_DEPTHWISE);
     if (o.kernel == WG_KERNEL_DEPTHWISE && !use_dw)
         return fail(err, WG_ERR_NOT_SUPPORTED,
                     "the depthwise kernel needs C = K = 1, 1-D or 2-D, <= 9 taps and G %% 8 == 0");
@@ -630,12 +690,13 @@ std::string plan_string(const Plan& pl)
     if (pl.kind == KIND_IGEMM) {
         const IgemmPlan& ig = pl.ig;
         snprintf(buf, sizeof buf,
-                 "kernel=igemm_tcgen05 %s mode=%s S=%d cluster=%d Gm=%d gblocks=%d cchunks=%d Nt=%d ntiles=%d "
+                 "kernel=igemm_tcgen05 %s taps=%s Nmma=%d mode=%s S=%d cluster=%d Gm=%d gblocks=%d cchunks=%d "
+                 "Nt=%d ntiles=%d "
                  "katoms=%d "
                  "box=(w%d,h%d,d%d,n%d) KT=%d ktiles=%lld per_split=%lld atoms=%d mtiles=%d mt_per_cta=%d "
                  "mranges=%d tmem_cols=%d stages=%d stage_bytes=%d smem=%d grid=(%u,%u,%u) block=%u ws=%zu "
                  "reduce=%s",
-                 ig.halo ? "halo" : "pertap", mode, pl.S, ig.cluster, ig.Gm, ig.n_gblocks, ig.n_cchunks, ig.Nt, ig.n_ntiles, ig.n_katoms, ig.box[0], ig.box[1],
+                 ig.halo ? "halo" : "pertap", ig.xs ? "mn" : "m", ig.Nmma, mode, pl.S, ig.cluster, ig.Gm, ig.n_gblocks, ig.n_cchunks, ig.Nt, ig.n_ntiles, ig.n_katoms, ig.box[0], ig.box[1],
                  ig.box[2], ig.box[3], ig.KT, ig.total_kt, pl.per_split, ig.n_atoms, ig.n_mtiles, ig.mt_per_cta,
                  ig.n_mranges, ig.tmem_cols, ig.stages, ig.stage_bytes, ig.smem_bytes, pl.grid[0], pl.grid[1],
                  pl.grid[2], pl.block, pl.ws_bytes, pl.mode == MODE_DETERMINISTIC ? "kernel" : "none");

@@ -69,6 +69,17 @@ struct IgemmPlan {
     unsigned int atom_off[kMaxHaloAtoms];    // byte offset of atom (patch + tap row shift) in a stage
     unsigned short atom_tap[kMaxHaloAtoms];
     unsigned char atom_cc[kMaxHaloAtoms];
+    // Tap form.  xs = 0: every tap on the MMA rows, atoms are (tap, chunk).
+    // xs = X (2..4): the filter's x taps on the MMA columns.  Atoms are
+    // (z, y, chunk) rows of an X patch with no halo along w; the B operand is
+    // one dY patch per K-tile, dy_w = box w + (X-1)*dil_w columns wide, read
+    // as xs 64-column atoms (atom j = tap x = X-1-j, a row shift of j*dil_w),
+    // so the MMA N is Nmma = 64*xs.  Pixel tiles run over q = wo + x*dil_w in
+    // [0, Wo + (X-1)*dil_w) along w; dY is zero outside [0, Wo) (TMA fill).
+    int xs;
+    int Nmma;         // MMA N (Nt when xs = 0)
+    int dy_w;         // dY staging extent along w (box w when xs = 0)
+    int dy_bytes;     // dY bytes per stage (the TMA transaction count of its boxes)
     long long est_cycles;  // planner's cost estimate (for the plan string)
     long long tile_clk;    // planner's estimate of one K-tile on one CTA, in SM cycles
     int cluster;           // CTAs per thread-block cluster along the split (1: none)

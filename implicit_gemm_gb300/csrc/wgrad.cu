@@ -263,7 +263,7 @@ int prepare_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, v
     {
         const cuuint64_t dims[5] = {GK, (cuuint64_t)pb.out[2], (cuuint64_t)pb.out[1], (cuuint64_t)pb.out[0],
                                     (cuuint64_t)pb.N};
-        const cuuint32_t box[5] = {64, (cuuint32_t)ig.box[0], (cuuint32_t)ig.box[1], (cuuint32_t)ig.box[2],
+        const cuuint32_t box[5] = {64, (cuuint32_t)ig.dy_w, (cuuint32_t)ig.box[1], (cuuint32_t)ig.box[2],
                                    (cuuint32_t)ig.box[3]};
         const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
         const int st = encode(&tmy, pb.in_dtype, const_cast<void*>(dy), dims, box, estr, CU_TENSOR_MAP_SWIZZLE_128B, "dY");
@@ -286,11 +286,13 @@ int prepare_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, v
     prm.Gm = ig.Gm, prm.Nt = ig.Nt, prm.n_ntiles = ig.n_ntiles, prm.n_katoms = ig.n_katoms;
     prm.n_atoms = ig.n_atoms, prm.n_mtiles = ig.n_mtiles, prm.mtpc = ig.mt_per_cta;
     prm.halo = ig.halo;
+    prm.xs = ig.xs, prm.Nmma = ig.Nmma, prm.dy_tx = ig.dy_bytes;
+    prm.dy_xoff = ig.xs ? (pb.filt[2] - 1) * pb.dil[2] : 0;
     prm.patch_bytes = ig.patch_bytes;
     prm.patch_tx = ig.halo ? ig.patch[0] * ig.patch[1] * ig.patch[2] * ig.box[3] * 128 : ig.slot_bytes;
     prm.n_patches = ig.n_patches, prm.dy_off = ig.dy_off, prm.slot_bytes = ig.slot_bytes;
     prm.stage_bytes = ig.stage_bytes, prm.stages = ig.stages, prm.tmem_cols = ig.tmem_cols;
-    prm.idesc = wg::make_idesc_f16(pb.in_dtype == WG_BF16, true, true, 128, ig.Nt);
+    prm.idesc = wg::make_idesc_f16(pb.in_dtype == WG_BF16, true, true, 128, ig.Nmma);
     prm.mode = pl.mode, prm.out_dtype = pb.out_dtype;
     prm.clq = ig.cluster;
     prm.out = pl.mode == wg::MODE_DETERMINISTIC ? ws : dw;
@@ -311,6 +313,21 @@ int prepare_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, v
                            : (unsigned)(16 * ks + 8 * h);
         }
         prm.kd_table[ks] = ((unsigned long long)((r[1] - r[0]) * 8u) << 32) + (unsigned long long)(r[0] * 8u);
+        if (ig.xs) {
+            // B: the same pixels in the dY patch, dy_w rows per (n, d, h) row.
+            for (int h = 0; h < 2; ++h) {
+                int q = 16 * ks + 8 * h;
+                const int iw = q % ig.box[0];
+                q /= ig.box[0];
+                const int ih = q % ig.box[1];
+                q /= ig.box[1];
+                const int id = q % ig.box[2];
+                const int in = q / ig.box[2];
+                r[h] = (unsigned)(((in * ig.box[2] + id) * ig.box[1] + ih) * ig.dy_w + iw);
+            }
+            prm.kd_table_b[ks] =
+                ((unsigned long long)((r[1] - r[0]) * 8u) << 32) + (unsigned long long)(r[0] * 8u);
+        }
     }
     if (ig.halo) {
         memcpy(prm.patch_ph, ig.patch_ph, sizeof prm.patch_ph);

@@ -101,10 +101,25 @@ typedef struct {
  *  IGEMM:      the tensor-core implicit GEMM for every problem.  For small C
  *              and K it folds several groups into one tile and keeps only the
  *              diagonal blocks (the merged-tile design of the CK page's group
- *              merging), so depthwise problems run on it too.
+ *              merging), so depthwise problems run on it too.  The planner
+ *              picks the tile form (below) from its cost model.
  *  DEPTHWISE:  the CUDA-core depthwise kernel; WG_ERR_NOT_SUPPORTED where it
- *              does not apply. */
-typedef enum { WG_KERNEL_AUTO = 0, WG_KERNEL_IGEMM = 1, WG_KERNEL_DEPTHWISE = 2 } wg_kernel;
+ *              does not apply.
+ *  IGEMM_TAPS_M:  the tensor-core kernel with every filter tap on the MMA rows:
+ *              D[(tap, c), k] (the CK page's GemmN = C*YX, transposed).
+ *  IGEMM_TAPS_MN: the tensor-core kernel with the filter's x taps moved to the
+ *              MMA columns: D[(z, y, c), (x, k)], summed over pixels q shifted
+ *              by x along W (dY read at q - x*dil, X at q - pad), which turns
+ *              K = 64 into 64*X columns per MMA.  Needs stride 1, no group
+ *              fold (C + K > 64 or G = 1), K a multiple of 64, 2 <= X <= 4 and
+ *              no cluster; WG_ERR_NOT_SUPPORTED otherwise. */
+typedef enum {
+    WG_KERNEL_AUTO = 0,
+    WG_KERNEL_IGEMM = 1,
+    WG_KERNEL_DEPTHWISE = 2,
+    WG_KERNEL_IGEMM_TAPS_M = 3,
+    WG_KERNEL_IGEMM_TAPS_MN = 4
+} wg_kernel;
 
 /* Per-call options (the CK page's k_batch, plus the two ways of combining splits).
  *  split_k:     0 = choose automatically, 1 = no split, S > 1 = S splits of GemmK.

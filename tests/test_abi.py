@@ -203,12 +203,41 @@ def test_kernel_selector():
     assert e.value.status == 2
     with pytest.raises(binding.WgradError) as e:
         lib_opts = binding.make_options()
-        lib_opts.kernel = 3
+        lib_opts.kernel = 5
         p = binding.make_problem(dense)
         import ctypes
         buf = ctypes.create_string_buffer(256)
         binding._check(binding.load().wg_plan_string(ctypes.byref(p), ctypes.byref(lib_opts), buf, len(buf)))
     assert e.value.status == 1
+
+
+def test_tap_form_selector():
+    # x taps on the MMA columns: stride 1, no group fold, K a multiple of 64,
+    # 2 <= X <= 4 and no cluster; NOT_SUPPORTED (2) otherwise when forced.
+    ok = [spec(2, 1, 2, 64, 64, [13, 11], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
+          spec(2, 1, 2, 64, 128, [9, 14], [3, 4], [1, 1], [1, 1], [1, 2], [1, 1]),
+          spec(1, 1, 3, 40, 64, [50], [2], [1], [3], [3], [3]),
+          spec(3, 2, 2, 72, 64, [5, 6, 7], [3, 3, 3], [1, 1, 1], [1, 1, 1], [1, 1, 1], [1, 1, 1])]
+    for sp in ok:
+        f = _plan_fields(binding.wg_plan_string(sp, kernel="igemm_taps_mn"))
+        assert f["taps"] == "mn" and f["Nmma"] == str(64 * sp["filt"][-1]) and f["Nt"] == "64", f
+        assert int(f["tmem_cols"]) >= int(f["mt_per_cta"]) * int(f["Nmma"])
+        assert _plan_fields(binding.wg_plan_string(sp, kernel="igemm_taps_m"))["taps"] == "m"
+    bad = [spec(2, 1, 2, 64, 64, [13, 11], [3, 3], [2, 2], [1, 1], [1, 1], [1, 1]),   # stride 2
+           spec(2, 1, 2, 64, 96, [13, 11], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),   # K = 96
+           spec(2, 1, 2, 64, 64, [13, 11], [3, 1], [1, 1], [1, 1], [1, 0], [1, 0]),   # X = 1
+           spec(2, 1, 2, 64, 64, [13, 11], [3, 5], [1, 1], [1, 1], [1, 2], [1, 2]),   # X = 5
+           spec(2, 4, 2, 16, 64, [13, 11], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])]   # groups folded
+    for sp in bad:
+        with pytest.raises(binding.WgradError) as e:
+            binding.wg_plan_string(sp, kernel="igemm_taps_mn")
+        assert e.value.status == 2, sp
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_plan_string(ok[0], 4, "deterministic", 0, cluster=2, kernel="igemm_taps_mn")
+    assert e.value.status == 2
+    # Depthwise problems run on the tensor cores under either tap form selector.
+    dw = WORKLOADS["2d_depthwise_g512_n64_h28"][0]
+    assert "kernel=igemm_tcgen05" in binding.wg_plan_string(dw, kernel="igemm_taps_m")
 
 
 def test_dgrad_plans_and_limits():
@@ -246,7 +275,7 @@ def test_planner_choices_on_default_caps():
     # the device-filling one where the cold HBM read bounds the main loop, and
     # explicit split degrees that keep well-shaped pixel tiles (a cost floor
     # must not make every tiling tie).
-    dense = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_dense_n32_h56_c64_k64"][0]))
+    dense = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_dense_n32_h56_c64_k64"][0], kernel="igemm_taps_m"))
     assert (dense["S"], dense["mt_per_cta"], dense["box"]) == ("75", "3", "(w8,h7,d1,n4)")
     one = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_1x1_n32_h56_c64_k256"][0]))
     assert int(one["S"]) < 150

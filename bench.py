@@ -73,6 +73,7 @@ VARIANTS = [
     ("2d_tiny_n1_h8_c16_k32", "2d_tiny_n1_h8_c16_k32", 0, "auto", 0, "auto"),
     ("2d_dense_n32_h56_c64_k64/S1_direct", "2d_dense_n32_h56_c64_k64", 1, "direct", 0, "auto"),
     ("2d_dense_n32_h56_c64_k64/S4_deterministic", "2d_dense_n32_h56_c64_k64", 4, "deterministic", 0, "auto"),
+    ("2d_dense_n32_h56_c64_k64/taps_m", "2d_dense_n32_h56_c64_k64", 0, "auto", 0, "igemm_taps_m"),
     ("2d_grouped_g32_c8_k8_n32_h28", "2d_grouped_g32_c8_k8_n32_h28", 0, "auto", 0, "auto"),
     ("2d_grouped_g32_c8_k8_n32_h28/atomic", "2d_grouped_g32_c8_k8_n32_h28", 0, "atomic", 0, "auto"),
     ("2d_depthwise_g512_n64_h28/gm8", "2d_depthwise_g512_n64_h28", 0, "auto", 8, "auto"),
@@ -245,8 +246,8 @@ L2_BYTES = 129 * 1000 * 1000
 # ncu capture of the kernel as it now stands (summaries under profiles/); a
 # workload without such a capture reports null.
 TRAFFIC = {
-    # igemm_wgrad_kernel, plan S = 75, 3 M-tiles per CTA: 25,789,184 B read + 0 B written.
-    "2d_dense_n32_h56_c64_k64": 25_789_184,
+    # igemm_wgrad_kernel, plan taps=mn S = 75, one M-tile per CTA: 25,785,344 B read + 0 B written.
+    "2d_dense_n32_h56_c64_k64": 25_785_344,
     # depthwise_wgrad_kernel<bf16, 2, sliding>: 103,019,520 B read + 3,580,928 B written.
     "2d_depthwise_g512_n64_h28": 106_600_448,
 }

@@ -275,6 +275,8 @@ def test_planner_choices_on_default_caps():
     # the device-filling one where the cold HBM read bounds the main loop, and
     # explicit split degrees that keep well-shaped pixel tiles (a cost floor
     # must not make every tiling tie).
+    dense = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_dense_n32_h56_c64_k64"][0]))
+    assert (dense["taps"], dense["S"], dense["mt_per_cta"], dense["box"]) == ("mn", "75", "1", "(w32,h8,d1,n1)")
     dense = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_dense_n32_h56_c64_k64"][0], kernel="igemm_taps_m"))
     assert (dense["S"], dense["mt_per_cta"], dense["box"]) == ("75", "3", "(w8,h7,d1,n4)")
     one = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_1x1_n32_h56_c64_k256"][0]))

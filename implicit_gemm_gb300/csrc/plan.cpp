@@ -197,16 +197,15 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
     if (halo_ok && n_combos * ig.n_cchunks > kMaxPatches) halo_ok = false;
 
     // The x taps on the MMA columns (IgemmPlan::xs) need stride 1 (then a shift
-    // of the pixel index along w is a shift of dY), whole 64-wide k atoms of one
-    // group, and at most 256 columns.
+    // of the pixel index along w is a shift of dY), whole 64-wide k atoms (a
+    // folded tile keeps its block-diagonal mask in the epilogue), and at most
+    // 256 columns.
     const int X = pb.filt[2], Y = pb.filt[1], Z = pb.filt[0];
     const char* mn_no = nullptr;
     if (pb.stride[0] != 1 || pb.stride[1] != 1 || pb.stride[2] != 1)
         mn_no = "stride 1 in every dim";
-    else if (Gm != 1)
-        mn_no = "one group per tile (no group fold)";
-    else if (pb.K % 64)
-        mn_no = "K a multiple of 64";
+    else if (kwin % 64)
+        mn_no = "a k window (K, or K times the groups folded into a tile) that is a multiple of 64";
     else if (X < 2 || X > 4)
         mn_no = "2 to 4 filter taps along w";
     else if (o.cluster > 1)
@@ -231,7 +230,7 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
         IgCand f{};
         f.xs = mn ? X : 0;
         f.Nt = mn ? 64 : ig.Nt;
-        f.n_ntiles = mn ? pb.K / 64 : ig.n_ntiles;
+        f.n_ntiles = mn ? kwin / 64 : ig.n_ntiles;
         f.n_katoms = mn ? 1 : ig.n_katoms;
         f.n_atoms = mn ? Z * Y * ig.n_cchunks : ig.n_atoms;
         f.n_mtiles = (int)cdiv(f.n_atoms, 2);

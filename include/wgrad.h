@@ -110,9 +110,10 @@ typedef struct {
  *  IGEMM_TAPS_MN: the tensor-core kernel with the filter's x taps moved to the
  *              MMA columns: D[(z, y, c), (x, k)], summed over pixels q shifted
  *              by x along W (dY read at q - x*dil, X at q - pad), which turns
- *              K = 64 into 64*X columns per MMA.  Needs stride 1, no group
- *              fold (C + K > 64 or G = 1), K a multiple of 64, 2 <= X <= 4 and
- *              no cluster; WG_ERR_NOT_SUPPORTED otherwise. */
+ *              K = 64 into 64*X columns per MMA.  Needs stride 1, a k window
+ *              that is a multiple of 64 (K, or K times the groups folded into
+ *              one tile when C and K are small), 2 <= X <= 4 and no cluster;
+ *              WG_ERR_NOT_SUPPORTED otherwise. */
 typedef enum {
     WG_KERNEL_AUTO = 0,
     WG_KERNEL_IGEMM = 1,

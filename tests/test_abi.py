@@ -217,7 +217,8 @@ def test_tap_form_selector():
     ok = [spec(2, 1, 2, 64, 64, [13, 11], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
           spec(2, 1, 2, 64, 128, [9, 14], [3, 4], [1, 1], [1, 1], [1, 2], [1, 1]),
           spec(1, 1, 3, 40, 64, [50], [2], [1], [3], [3], [3]),
-          spec(3, 2, 2, 72, 64, [5, 6, 7], [3, 3, 3], [1, 1, 1], [1, 1, 1], [1, 1, 1], [1, 1, 1])]
+          spec(3, 2, 2, 72, 64, [5, 6, 7], [3, 3, 3], [1, 1, 1], [1, 1, 1], [1, 1, 1], [1, 1, 1]),
+          spec(2, 32, 2, 8, 8, [9, 10], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])]  # 8 groups folded: k window 64
     for sp in ok:
         f = _plan_fields(binding.wg_plan_string(sp, kernel="igemm_taps_mn"))
         assert f["taps"] == "mn" and f["Nmma"] == str(64 * sp["filt"][-1]) and f["Nt"] == "64", f
@@ -227,7 +228,7 @@ def test_tap_form_selector():
            spec(2, 1, 2, 64, 96, [13, 11], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),   # K = 96
            spec(2, 1, 2, 64, 64, [13, 11], [3, 1], [1, 1], [1, 1], [1, 0], [1, 0]),   # X = 1
            spec(2, 1, 2, 64, 64, [13, 11], [3, 5], [1, 1], [1, 1], [1, 2], [1, 2]),   # X = 5
-           spec(2, 4, 2, 16, 64, [13, 11], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])]   # groups folded
+           spec(2, 2, 2, 24, 40, [13, 11], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])]   # folded k window 80
     for sp in bad:
         with pytest.raises(binding.WgradError) as e:
             binding.wg_plan_string(sp, kernel="igemm_taps_mn")

@@ -6,8 +6,9 @@ The form changes what the MMA rows and columns mean, the pixel range along W
 (Wo + (X-1)*dil_w positions, dY zero outside [0, Wo)), the dY staging (one
 patch per K-tile read as X row-shifted column blocks) and the epilogue's tap of
 each column block, so it is checked on its own: ragged images, dilation,
-asymmetric pads, X = 2, 3 and 4, 1-D and 3-D, K and C above 64, groups,
-channel counts that are not multiples of 64, every split mode, integer inputs
+asymmetric pads, X = 2, 3 and 4, 1-D and 3-D, K and C above 64, groups (and
+small groups folded into one tile), channel counts that are not multiples of
+64, every split mode, integer inputs
 bit for bit, and the 56x56 workload at full size in both tile forms.
 """
 import numpy as np
@@ -72,6 +73,13 @@ CASES = [
     spec(2, 3, 2, 72, 64, [6, 9], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
     # a 3x3 image, one image
     spec(2, 1, 1, 64, 64, [3, 3], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
+    # small groups folded into one tile (block-diagonal mask): 8 groups of 8 per
+    # 64-wide window; a 128-wide k window; 12 groups of 16; 10 groups (the last
+    # block half empty)
+    spec(2, 32, 2, 8, 8, [9, 10], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
+    spec(2, 8, 3, 8, 16, [14, 14], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], out_dtype="bf16"),
+    spec(2, 12, 2, 16, 16, [7, 9], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], in_dtype="fp16"),
+    spec(2, 10, 2, 8, 8, [8, 11], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
     # no padding, so the shifted range reaches past the image on both sides
     spec(2, 1, 4, 64, 64, [12, 30], [3, 3], [1, 1], [1, 1], [0, 0], [0, 0]),
 ]
@@ -96,7 +104,7 @@ def test_taps_mn_all_modes(sp):
         assert_close(got, dw, A, sp["out_dtype"], f"{_ids(sp)} S={split_k} {mode}: {plan}")
 
 
-@pytest.mark.parametrize("sp", [CASES[i] for i in (0, 2, 3, 4, 5, 7, 10, 12)], ids=_ids)
+@pytest.mark.parametrize("sp", [CASES[i] for i in (0, 2, 3, 4, 5, 7, 10, 12, 14, 15, 16)], ids=_ids)
 def test_taps_mn_integer_inputs_bitwise(sp):
     x, dy = make_inputs(sp, ("int", -2, 2), 73, 74)
     dw, _ = ref(sp, x, dy)

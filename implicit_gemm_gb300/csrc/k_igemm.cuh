@@ -566,48 +566,60 @@ constexpr int kRedGroups = 4;
 constexpr uint32_t kRedPiece = 16384;  // bytes per bulk copy
 
 __host__ __device__ __forceinline__ int red_groups(int S) { return S >= 8 ? kRedGroups : 1; }
+static_assert(kRedGroups == 4, "slices_reduce_store maps (slice, range) pairs with shifts by 2");
 
 // Sum nsl consecutive slices staged in shared memory -- slice sl0 + k at
 // sm + k * S * W, with kRedGroups * W floats of scratch at part + k * kRedGroups * W
 // -- in the fixed order and store their elements of dW.  Every thread of the CTA
-// calls it (it synchronises them once); the work of all the slices is shared.
+// calls it (it synchronises them once).  W <= 128 (the planner's slice width),
+// so a slice row is at most 32 float4 columns: pass 1 gives each warp one
+// (slice, split range) and each lane one float4 column; pass 2 gives each
+// thread one element.  The index arithmetic is shifts and one 32-bit division
+// per element: with general divisions per item (and a 64-bit one per element)
+// the two passes took ~2,300 cycles on the 56x56 workload's slices, against
+// the few hundred their loads and adds need.
 __device__ __forceinline__ void slices_reduce_store(const float* sm, float* part, const WsLayout& w, long long sl0,
                                                     int nsl, void* dw, int out_dtype)
 {
     const int S = w.S, W = w.W;
-    const int G = red_groups(S);
-    // Each item adds one split range for 4 consecutive elements of one slice (W
-    // is a multiple of 4): 16-byte shared-memory loads, four independent chains.
-    const int W4 = W >> 2, per_slice = W4 * G;
-    for (int idx = threadIdx.x; idx < nsl * per_slice; idx += blockDim.x) {
-        const int k = idx / per_slice, rem = idx - k * per_slice;
-        const int g = rem / W4, i4 = rem - g * W4;
-        const int s0 = S * g / G, s1 = S * (g + 1) / G;
-        const float4* q = reinterpret_cast<const float4*>(sm + ((size_t)k * S + s0) * W) + i4;
-        float4 a = q[0];
-        q += W4;
-        int s = s0 + 1;
-        for (; s + 4 <= s1; s += 4, q += 4 * W4) {
-            float4 v[4];
+    const int G = red_groups(S);  // 1 or kRedGroups (= 4)
+    const int W4 = W >> 2;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    // Pass 1: range g of slice k is summed in index order, four independent
+    // float4 chains per lane (16-byte shared-memory loads).
+    for (int t = warp; t < nsl * G; t += nwarps) {
+        const int k = G == 1 ? t : t >> 2;
+        const int g = t - k * G;
+        const int s0 = G == 1 ? 0 : (S * g) >> 2, s1 = G == 1 ? S : (S * (g + 1)) >> 2;
+        if (lane < W4) {
+            const float4* q = reinterpret_cast<const float4*>(sm + ((size_t)k * S + s0) * W) + lane;
+            float4 a = q[0];
+            q += W4;
+            int s = s0 + 1;
+            for (; s + 4 <= s1; s += 4, q += 4 * W4) {
+                float4 v[4];
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) v[jj] = q[jj * W4];
+                for (int jj = 0; jj < 4; ++jj) v[jj] = q[jj * W4];
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) a.x += v[jj].x, a.y += v[jj].y, a.z += v[jj].z, a.w += v[jj].w;
+                for (int jj = 0; jj < 4; ++jj) a.x += v[jj].x, a.y += v[jj].y, a.z += v[jj].z, a.w += v[jj].w;
+            }
+            for (; s < s1; ++s, q += W4) a.x += q[0].x, a.y += q[0].y, a.z += q[0].z, a.w += q[0].w;
+            reinterpret_cast<float4*>(part + ((size_t)k * kRedGroups + g) * W)[lane] = a;
         }
-        for (; s < s1; ++s, q += W4) a.x += q[0].x, a.y += q[0].y, a.z += q[0].z, a.w += q[0].w;
-        reinterpret_cast<float4*>(part + ((size_t)k * kRedGroups + g) * W)[i4] = a;
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < nsl * W; idx += blockDim.x) {
-        const int k = idx / W, i = idx - k * W;
-        const long long sl = sl0 + k;
-        const long long r = sl / w.nj;
-        const long long x0 = (sl - r * w.nj) * W;
+    // Pass 2: the range sums of each element added in range order.
+    for (int t = threadIdx.x; t < nsl * 128; t += blockDim.x) {
+        const int k = t >> 7, i = t & 127;
+        if (i >= W) continue;
+        const int sl = (int)(sl0 + k);  // slice indices fit 31 bits (checked on the host)
+        const int r = sl / w.nj;
+        const int x0 = (sl - r * w.nj) * W;
         if (x0 + i >= w.L) continue;  // past the end of the row (its last slice)
         const float* pk = part + (size_t)k * kRedGroups * W;
         float a = pk[i];
         for (int g = 1; g < G; ++g) a += pk[g * W + i];
-        store_cast(dw, r * w.L + x0 + i, a, out_dtype);
+        store_cast(dw, (long long)r * w.L + x0 + i, a, out_dtype);
     }
 }
 

@@ -368,7 +368,7 @@ int launch_reduce(const wg::Plan& pl, void* ws, void* dw, cudaStream_t stream)
     cfg.blockDim = dim3(wg::kRedThreads);
     cudaError_t e;
     const float* wsf = static_cast<const float*>(ws);
-    if (smem <= wg::kMaxSmemPerCta && n_slices < (1LL << 31)) {
+    if (smem <= wg::kMaxSmemPerCta && n_slices < (1LL << 31) && w.W <= 128) {
         const int st = ensure_smem(wg::reduce_splits_bulk_kernel, (int)smem);
         if (st) return st;
         cfg.gridDim = dim3((unsigned)((n_slices + spc - 1) / spc));

@@ -23,6 +23,14 @@
 //    coordinates and the conv stride as the TMA element stride.
 // Implicit zero padding is the TMA out-of-bounds fill, for both operands.
 //
+// Tap forms.  With every tap on the rows, K = 64 output channels give N = 64,
+// and a 128x64x16 MMA is bound by its shared-memory operand reads.  For
+// stride 1 the pixel sum can run over q = wo + x*dil_w instead, with dY read
+// at q - x*dil_w (zero outside the image) and X at q - pad: the x taps then
+// sit on the columns, D[(z, y, c), (x, k)], B being one dY patch per K-tile
+// read as xs 64-column atoms one dil_w row apart -- 128x192x16 MMAs for 3x3
+// filters, at the tensor rate.
+//
 // Warp roles (192 threads): warp 0 lane 0 issues TMA; warp 1 owns TMEM and its
 // lane 0 issues tcgen05.mma; warps 2..5 read TMEM (lane quadrant = warp % 4)
 // and store dW / atomically add / write the split-K workspace.

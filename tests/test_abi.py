@@ -280,6 +280,9 @@ def test_planner_choices_on_default_caps():
     assert (dense["taps"], dense["S"], dense["mt_per_cta"], dense["box"]) == ("mn", "75", "1", "(w32,h8,d1,n1)")
     dense = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_dense_n32_h56_c64_k64"][0], kernel="igemm_taps_m"))
     assert (dense["S"], dense["mt_per_cta"], dense["box"]) == ("75", "3", "(w8,h7,d1,n4)")
+    # 8 groups of C = K = 8 folded into a 64-wide window: the column form too.
+    grouped = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_grouped_g32_c8_k8_n32_h28"][0]))
+    assert (grouped["taps"], grouped["Gm"], grouped["Nmma"], grouped["S"]) == ("mn", "8", "192", "38")
     one = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_1x1_n32_h56_c64_k256"][0]))
     assert int(one["S"]) < 150
     for S in (75, 100, 150):

@@ -302,21 +302,31 @@ __global__ void __launch_bounds__(kDgThreads, 1)
                 const int y0 = tg * TG, ntap = min(TG, d.nyx - y0);
                 const int z = DD.tap[d.pd][zi];
                 const uint32_t sst = sbase + (uint32_t)(st * stage_bytes);
+                // Descriptors are a base plus byte offsets added to the start-address
+                // field (shared-memory addresses stay below 2^18, so the 14-bit field
+                // never carries into the next one), and the tap's (y, x) index runs
+                // as a counter: rebuilding both from the tap geometry for every tap
+                // held back the MMA issue rate.
+                const uint64_t a_base = make_sdesc(sst, 16u, sbo, 2u, 0u);
+                const uint64_t b_base = wr ? make_sdesc(wbase, kDgWTile, 1024u, 2u, 0u)
+                                           : make_sdesc(sst + (uint32_t)patch_bytes, kDgWTile, 1024u, 2u, 0u);
+                const int ztap = z * p.Y;
+                const int kcT = kc * p.T;
+                int yi = y0 / d.nx, xi = y0 - yi * d.nx;
                 for (int j = 0; j < ntap; ++j) {
-                    const int yi = (y0 + j) / d.nx, xi = (y0 + j) - yi * d.nx;
                     const int shift = DH.shift[d.ph][yi] * p.PW + DW.shift[d.pw][xi];
-                    const uint64_t a0 = make_sdesc(sst + (uint32_t)shift * 128u, 16u, sbo, 2u, 0u);
+                    const uint64_t a0 = a_base + (uint64_t)(shift * 8);  // 128 bytes per row, in 16-byte units
                     // B: this tap's W tile -- resident (indexed by K chunk and tap) or in the stage.
-                    const int tap = (z * p.Y + DH.tap[d.ph][yi]) * X + DW.tap[d.pw][xi];
-                    const uint32_t baddr = wr ? wbase + (uint32_t)((kc * p.T + tap) * n_catoms) * kDgWTile
-                                              : sst + (uint32_t)patch_bytes + (uint32_t)(j * n_catoms) * kDgWTile;
-                    const uint64_t b0 = make_sdesc(baddr, kDgWTile, 1024u, 2u, 0u);
+                    const int tap = (ztap + DH.tap[d.ph][yi]) * X + DW.tap[d.pw][xi];
+                    const int wt = wr ? (kcT + tap) * n_catoms : j * n_catoms;
+                    const uint64_t b0 = b_base + (uint64_t)(wt * (kDgWTile >> 4));
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint32_t acc = (i | j | ks) != 0 ? 1u : 0u;
                         if (elect_one()) umma_f16(tacc, a0 + (uint64_t)(2 * ks), b0 + (uint64_t)(128 * ks), idesc, acc);
                         __syncwarp();
                     }
+                    if (++xi == d.nx) xi = 0, ++yi;
                 }
                 if (elect_one()) umma_commit(&empty[st]);
                 __syncwarp();

@@ -825,9 +825,10 @@ int make_dgrad_plan(const wg_problem* p, const DeviceCaps& caps, DgPlan* pl, std
     // persistent CTA needs the same W tiles, loaded once) or W streamed with each
     // patch, and a ring that runs on across a CTA's tiles, as deep as fits (<= 4).
     // Two CTAs per SM come first (measured on GB300: two MMA issuers keep the
-    // tensor pipe busier than one at N <= 128, e.g. 56x56 C = K = 64: 20.8 us
-    // against 27.7 us with one CTA, W resident and a four-deep ring); then one
-    // CTA per SM, W resident only beside at least three patch stages.
+    // tensor pipe busier than one at N <= 128, e.g. 56x56 C = K = 64: 18.7 us
+    // against 22.5 us with one CTA, W resident and a four-deep ring; 1x1
+    // stride 2, C 256: 36.9 against 53.5 us); then one CTA per SM, W resident
+    // only beside at least three patch stages.
     const long long w_all = (long long)d.n_kc * pb.T * d.n_catoms * 8192;
     const int streamed = d.patch_bytes + d.TG * d.n_catoms * 8192;
     const int half = kMaxSmemPerCta / 2 - 1024 - 2048 - kDgStaging;  // ring + W of one of two CTAs

@@ -317,26 +317,72 @@ __global__ void __launch_bounds__(kIgThreads, 1)
     // A split-reduction kernel launched after this one may take each SM as soon
     // as this grid's CTA there exits (it waits for the whole grid's results).
     pdl_launch_dependents();
+    // Stage i of the TMA ring: the K-tile's X patches (or per-tap boxes) and dY.
+    const uint32_t tx = (uint32_t)(p.n_patches * p.patch_tx + p.dy_tx);
+    auto issue_stage = [&](int i) {
+        const int st = i % p.stages;
+        uint8_t* sb = smem + st * p.stage_bytes;
+        mbar_arrive_expect_tx(&full[st], tx);
+        int kt = kt0 + i;
+        const int tw = kt % p.ntile[0];
+        kt /= p.ntile[0];
+        const int th = kt % p.ntile[1];
+        kt /= p.ntile[1];
+        const int td = kt % p.ntile[2];
+        const int tn = kt / p.ntile[2];
+        const int wo0 = tw * p.box[0], ho0 = th * p.box[1], do0 = td * p.box[2], n0 = tn * p.box[3];
+        const int bw = wo0 * p.s[0] - p.pl[0], bh = ho0 * p.s[1] - p.pl[1], bd = do0 * p.s[2] - p.pl[2];
+        if (p.halo) {
+            for (int q = 0; q < p.n_patches; ++q)
+                tma_load_5d(sb + q * p.patch_bytes, &tmx, &full[st], c_al + 64 * p.patch_ph[q][3],
+                            bw + p.patch_ph[q][0], bh + p.patch_ph[q][1], bd + p.patch_ph[q][2], n0);
+        } else {
+            for (int a = 0; a < p.n_patches; ++a) {
+                const int atom = atom0 + a;
+                if (a < 2 * mtn && atom < p.n_atoms) {
+                    const int tap = atom / p.ncc, cc = atom - tap * p.ncc;
+                    const int x = tap % p.X, y = (tap / p.X) % p.Y, z = tap / (p.X * p.Y);
+                    tma_load_5d(sb + a * p.patch_bytes, &tmx, &full[st], c_al + 64 * cc, bw + x * p.d[0],
+                                bh + y * p.d[1], bd + z * p.d[2], n0);
+                } else {
+                    // Padding atom: a box entirely past the channel extent reads zeros.
+                    tma_load_5d(sb + a * p.patch_bytes, &tmx, &full[st], p.GC, 0, 0, 0, 0);
+                }
+            }
+        }
+        for (int j = 0; j < p.n_katoms; ++j)
+            tma_load_5d(sb + p.dy_off + j * p.slot_bytes, &tmy, &full[st], k_base + 64 * j, wo0 - p.dy_xoff,
+                        ho0, do0, n0);
+    };
+    // Thread 0 (the TMA producer) initialises the barriers and issues the first
+    // stage before the block barrier, and warp 1 allocates TMEM meanwhile: the
+    // tensor maps' first fetch by the TMA unit (~1 us) then overlaps the
+    // prologue instead of following it.  (Issuing every ring stage here held
+    // the other warps at the barrier for longer than the data took to land.)
+    int pre = 0;
     if (threadIdx.x == 0) {
+        if (nk > 0) {
+            tma_prefetch_desc(&tmx);
+            tma_prefetch_desc(&tmy);
+        }
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
         mbar_init(accb, 1);
         fence_mbar_init();
+        pre = min(1, nk);
+        for (int i = 0; i < pre; ++i) issue_stage(i);
     }
-    __syncthreads();  // barriers initialised: the producer may start
     if (warp == 1) {
         tmem_alloc(tslot, (uint32_t)p.tmem_cols);
         tmem_relinquish();
         tc_fence_before();
     }
-    // The TMEM address is read after the allocation by the MMA warp (and the
-    // warps that only wait for the epilogue); the producer starts at once and
-    // reads it after the main loop.
+    __syncthreads();  // barriers initialised, TMEM allocated, the first stage on its way
+    // The producer reads the TMEM address after the main loop.
     uint32_t tbase = 0;
     if (warp != 0) {
-        named_bar_sync(1, kIgThreads - 32);  // warps 1..7
         tc_fence_after();
         tbase = *tslot;
     }
@@ -345,45 +391,11 @@ __global__ void __launch_bounds__(kIgThreads, 1)
     if (warp == 0) {
         if (lane == 0 && nk > 0) {
             // ------------------------------------------------ TMA producer
-            tma_prefetch_desc(&tmx);
-            tma_prefetch_desc(&tmy);
-            const uint32_t tx = (uint32_t)(p.n_patches * p.patch_tx + p.dy_tx);
-            for (int i = 0; i < nk; ++i) {
+            for (int i = pre; i < nk; ++i) {
                 const int st = i % p.stages;
                 const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
                 if (i >= p.stages && !mbar_wait(&empty[st], ph ^ 1u)) break;
-                uint8_t* sb = smem + st * p.stage_bytes;
-                mbar_arrive_expect_tx(&full[st], tx);
-                int kt = kt0 + i;
-                const int tw = kt % p.ntile[0];
-                kt /= p.ntile[0];
-                const int th = kt % p.ntile[1];
-                kt /= p.ntile[1];
-                const int td = kt % p.ntile[2];
-                const int tn = kt / p.ntile[2];
-                const int wo0 = tw * p.box[0], ho0 = th * p.box[1], do0 = td * p.box[2], n0 = tn * p.box[3];
-                const int bw = wo0 * p.s[0] - p.pl[0], bh = ho0 * p.s[1] - p.pl[1], bd = do0 * p.s[2] - p.pl[2];
-                if (p.halo) {
-                    for (int q = 0; q < p.n_patches; ++q)
-                        tma_load_5d(sb + q * p.patch_bytes, &tmx, &full[st], c_al + 64 * p.patch_ph[q][3],
-                                    bw + p.patch_ph[q][0], bh + p.patch_ph[q][1], bd + p.patch_ph[q][2], n0);
-                } else {
-                    for (int a = 0; a < p.n_patches; ++a) {
-                        const int atom = atom0 + a;
-                        if (a < 2 * mtn && atom < p.n_atoms) {
-                            const int tap = atom / p.ncc, cc = atom - tap * p.ncc;
-                            const int x = tap % p.X, y = (tap / p.X) % p.Y, z = tap / (p.X * p.Y);
-                            tma_load_5d(sb + a * p.patch_bytes, &tmx, &full[st], c_al + 64 * cc, bw + x * p.d[0],
-                                        bh + y * p.d[1], bd + z * p.d[2], n0);
-                        } else {
-                            // Padding atom: a box entirely past the channel extent reads zeros.
-                            tma_load_5d(sb + a * p.patch_bytes, &tmx, &full[st], p.GC, 0, 0, 0, 0);
-                        }
-                    }
-                }
-                for (int j = 0; j < p.n_katoms; ++j)
-                    tma_load_5d(sb + p.dy_off + j * p.slot_bytes, &tmy, &full[st], k_base + 64 * j, wo0 - p.dy_xoff,
-                                ho0, do0, n0);
+                issue_stage(i);
             }
         }
     } else if (warp == 1) {

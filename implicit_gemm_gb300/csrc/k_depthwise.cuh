@@ -157,12 +157,32 @@ __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
     // A split-reduction kernel launched after this one may take each SM as soon
     // as this grid's CTA there exits (it waits for the whole grid's results).
     pdl_launch_dependents();
+    // Row tile i of this split into ring stage i % stages: X rows with halo, dY rows.
+    auto issue_tile = [&](int i) {
+        const int st = i % p.stages;
+        const int tile = t0 + i;
+        const int n = tile / p.n_hstrips;
+        const int ho0 = (tile - n * p.n_hstrips) * p.R;
+        uint8_t* sb = smem + st * p.stage_bytes;
+        mbar_arrive_expect_tx(&full[st], (uint32_t)(p.x_tx + p.dy_tx));
+        tma_load_5d(sb, &tmx, &full[st], cb * p.CB, -p.plw, ho0 * p.sh - p.plh, 0, n);
+        tma_load_5d(sb + p.x_bytes_al, &tmy, &full[st], cb * p.CB, 0, ho0, 0, n);
+    };
+    // Thread 0 initialises the barriers and issues the first tile before the
+    // block barrier, so that the TMA unit's first fetch of the tensor maps
+    // overlaps the prologue; the producer warp continues from the second tile.
+    const int pre = ntl > 0 ? 1 : 0;
     if (tid == 0) {
+        if (pre) {
+            tma_prefetch_desc(&tmx);
+            tma_prefetch_desc(&tmy);
+        }
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], (uint32_t)n_cwarps);
         }
         fence_mbar_init();
+        for (int i = 0; i < pre; ++i) issue_tile(i);
     }
     __syncthreads();
 
@@ -177,19 +197,11 @@ __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
     if (warp == n_cwarps) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            tma_prefetch_desc(&tmx);
-            tma_prefetch_desc(&tmy);
-            for (int i = 0; i < ntl; ++i) {
+            for (int i = pre; i < ntl; ++i) {
                 const int st = i % p.stages;
                 const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
                 if (i >= p.stages && !mbar_wait(&empty[st], ph ^ 1u)) break;
-                const int tile = t0 + i;
-                const int n = tile / p.n_hstrips;
-                const int ho0 = (tile - n * p.n_hstrips) * p.R;
-                uint8_t* sb = smem + st * p.stage_bytes;
-                mbar_arrive_expect_tx(&full[st], (uint32_t)(p.x_tx + p.dy_tx));
-                tma_load_5d(sb, &tmx, &full[st], cb * p.CB, -p.plw, ho0 * p.sh - p.plh, 0, n);
-                tma_load_5d(sb + p.x_bytes_al, &tmy, &full[st], cb * p.CB, 0, ho0, 0, n);
+                issue_tile(i);
             }
         }
     } else {

@@ -203,7 +203,13 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     const int stages = p.stages, stage_bytes = p.stage_bytes, patch_bytes = p.patch_bytes;
     const int n_catoms = p.n_catoms, X = p.X, TG = p.TG, Nt = p.Nt;
 
+    // Thread 0 (the TMA producer) prefetches the tensor maps, initialises the
+    // barriers and issues the resident W tiles before the block barrier, and
+    // warp 1 allocates TMEM meanwhile: the TMA unit's first fetch of the
+    // tensor maps then overlaps the prologue.
     if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmy);
+        tma_prefetch_desc(&tmw);
         for (int i = 0; i < stages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
@@ -214,16 +220,24 @@ __global__ void __launch_bounds__(kDgThreads, 1)
         }
         mbar_init(wbar, 1);
         fence_mbar_init();
+        if (wr) {
+            // Every (K chunk, tap, channel atom) tile of the one (channel tile, group).
+            mbar_arrive_expect_tx(wbar, (uint32_t)p.w_bytes);
+            for (int kc = 0; kc < p.n_kc; ++kc)
+                for (int tap = 0; tap < p.T; ++tap)
+                    for (int a = 0; a < n_catoms; ++a)
+                        tma_load_5d(wres + (uint32_t)((kc * p.T + tap) * n_catoms + a) * kDgWTile, &tmw, wbar,
+                                    64 * a, tap, kc * 64, 0, 0);
+        }
     }
-    __syncthreads();
     if (warp == 1) {
         tmem_alloc(tslot, (uint32_t)p.tmem_cols);
         tmem_relinquish();
         tc_fence_before();
     }
+    __syncthreads();  // barriers initialised, TMEM allocated, W on its way
     uint32_t tbase = 0;
     if (warp != 0) {
-        named_bar_sync(1, kDgThreads - 32);  // warps 1..5: the allocation is done
         tc_fence_after();
         tbase = *tslot;
     }
@@ -231,18 +245,7 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            tma_prefetch_desc(&tmy);
-            tma_prefetch_desc(&tmw);
             const uint32_t patch_tx = (uint32_t)(p.PW * p.PH * 128);
-            if (wr) {
-                // Every (K chunk, tap, channel atom) tile of the one (channel tile, group).
-                mbar_arrive_expect_tx(wbar, (uint32_t)p.w_bytes);
-                for (int kc = 0; kc < p.n_kc; ++kc)
-                    for (int tap = 0; tap < p.T; ++tap)
-                        for (int a = 0; a < n_catoms; ++a)
-                            tma_load_5d(wres + (uint32_t)((kc * p.T + tap) * n_catoms + a) * kDgWTile, &tmw, wbar,
-                                        64 * a, tap, kc * 64, 0, 0);
-            }
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < n_all && ok; t += gridDim.x) {

@@ -457,7 +457,8 @@ def run_sweep(torch, stream, flush, steps, warmup):
             del wl
         best = min(res, key=res.get)
         row = {"shape": name, "auto_us": res["auto"], "best": best, "best_us": res[best],
-               "auto_vs_best": res[best] / res["auto"]}
+               "auto_vs_best": res[best] / res["auto"], "plans_us": res,
+               "auto_plan": binding.wg_plan_string(sp, 0, "auto", 0)}
         if "gm1" in res:
             row["gm1_us"] = res["gm1"]
             row["auto_speedup_vs_gm1"] = res["gm1"] / res["auto"]

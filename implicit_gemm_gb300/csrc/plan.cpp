@@ -640,6 +640,18 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
     if (use_dw) {
         pl->kind = KIND_DEPTHWISE;
         st = plan_depthwise(pl, o, num_sms, err);
+        // Automatic vector width: two channels, or four when the sliding 3x3
+        // window is used and every CTA walks many row tiles.  On a sweep of
+        // 16 depthwise shapes four-channel vectors won only there (G = 512,
+        // N = 64, 28x28: 27.9 against 29.6 us, 14 tiles per CTA); with 7 tiles
+        // per CTA or fewer two channels were as fast or faster.
+        if (st == WG_OK && o.group_merge == 0 && pl->dw.sliding && pl->per_split >= 10) {
+            wg_options o4 = o;
+            o4.group_merge = 4;
+            Plan p4;
+            std::memcpy(&p4, pl, sizeof p4);
+            if (plan_depthwise(&p4, o4, num_sms, nullptr) == WG_OK && p4.dw.sliding) std::memcpy(pl, &p4, sizeof p4);
+        }
     } else {
         if (o.group_merge > 1)
             return fail(err, WG_ERR_NOT_SUPPORTED,

@@ -280,6 +280,12 @@ def test_planner_choices_on_default_caps():
     assert (dense["taps"], dense["S"], dense["mt_per_cta"], dense["box"]) == ("mn", "75", "1", "(w32,h8,d1,n1)")
     dense = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_dense_n32_h56_c64_k64"][0], kernel="igemm_taps_m"))
     assert (dense["S"], dense["mt_per_cta"], dense["box"]) == ("75", "3", "(w8,h7,d1,n4)")
+    # Depthwise vector width: four channels for the G = 512, N = 64 workload (14
+    # row tiles per CTA), two for a small problem.
+    dwp = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_depthwise_g512_n64_h28"][0]))
+    assert (dwp["kernel"], dwp["Gm"]) == ("depthwise", "4")
+    small = _plan_fields(binding.wg_plan_string(spec(2, 64, 2, 1, 1, [9, 13], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])))
+    assert small["Gm"] == "2"
     # 8 groups of C = K = 8 folded into a 64-wide window: the column form too.
     grouped = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_grouped_g32_c8_k8_n32_h28"][0]))
     assert (grouped["taps"], grouped["Gm"], grouped["Nmma"], grouped["S"]) == ("mn", "8", "192", "38")

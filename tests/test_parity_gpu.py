@@ -77,6 +77,7 @@ WORKLOAD_MODES = [
     ("2d_grouped_g32_c8_k8_n32_h28", 0, "atomic", 0, 0),
     ("2d_grouped_g32_c8_k8_n32_h28", 32, "deterministic", 0, 4),
     ("2d_grouped_g32_c8_k8_n32_h28", 16, "atomic", 0, 8),
+    ("2d_depthwise_g512_n64_h28", 0, "auto", 0, 0),
     ("2d_depthwise_g512_n64_h28", 0, "auto", 1, 0),
     ("2d_depthwise_g512_n64_h28", 0, "auto", 2, 0),
     ("2d_depthwise_g512_n64_h28", 0, "auto", 4, 0),

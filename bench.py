@@ -248,8 +248,8 @@ L2_BYTES = 129 * 1000 * 1000
 TRAFFIC = {
     # igemm_wgrad_kernel, plan taps=mn S = 75, one M-tile per CTA: 25,778,688 B read + 0 B written.
     "2d_dense_n32_h56_c64_k64": 25_778_688,
-    # depthwise_wgrad_kernel<bf16, 2, sliding>: 103,075,584 B read + 3,901,440 B written.
-    "2d_depthwise_g512_n64_h28": 106_977_024,
+    # depthwise_wgrad_kernel<bf16, 4, sliding>: 103,047,168 B read + 3,496,960 B written.
+    "2d_depthwise_g512_n64_h28": 106_544_128,
 }
 MAX_COPIES = 512
 

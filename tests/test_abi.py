@@ -5,6 +5,7 @@ nothing is ever launched."""
 import os
 import re
 
+import numpy as np
 import pytest
 
 import oracle
@@ -327,3 +328,58 @@ def test_dgrad_launch_checks_before_device(lib):
     with pytest.raises(binding.WgradError) as e:
         binding.wg_conv_bwd_data(sp, 4096, 8192 + 4, 12288)
     assert e.value.status == 3
+
+
+def test_planner_invariants_on_random_problems():
+    # Seeded random problems (1-, 2- and 3-D, strides, dilations, groups, both
+    # tile forms and the depthwise kernel): every plan is either refused with
+    # NOT_SUPPORTED or satisfies the limits the kernels rely on.
+    rng = np.random.default_rng(20261202)
+    checked = {"m": 0, "mn": 0, "depthwise": 0}
+    for _ in range(400):
+        nd = int(rng.integers(1, 4))
+        G = int(rng.choice([1, 1, 2, 4, 8, 32]))
+        C = int(rng.choice([1, 8, 16, 24, 40, 64, 72, 128]))
+        K = int(rng.choice([1, 8, 16, 32, 64, 96, 128, 256]))
+        if C == 1 or K == 1:
+            C = K = 1
+            G = int(rng.choice([8, 16, 64, 512]))
+        if (G * C) % 8 or (G * K) % 8:
+            continue
+        filt = [int(rng.choice([1, 2, 3, 3, 4, 5])) for _ in range(nd)]
+        stride = [int(rng.choice([1, 1, 1, 2, 3])) for _ in range(nd)]
+        dil = [int(rng.choice([1, 1, 2])) for _ in range(nd)]
+        inn = [int(rng.integers(1, 40)) for _ in range(nd)]
+        pl = [int(rng.integers(0, f)) for f in filt]
+        pr = [int(rng.integers(0, f)) for f in filt]
+        sp = spec(nd, G, int(rng.integers(1, 9)), C, K, inn, filt, stride, dil, pl, pr)
+        try:
+            binding.wg_problem_normalize(sp)
+        except binding.WgradError:
+            continue  # no output position
+        for kernel in ("auto", "igemm_taps_m", "igemm_taps_mn"):
+            for split_k, mode in ((0, "auto"), (1, "direct"), (7, "deterministic")):
+                try:
+                    ps = binding.wg_plan_string(sp, split_k, mode, 0, kernel=kernel)
+                except binding.WgradError as e:
+                    assert e.status == 2, (sp, kernel, split_k, mode, e)
+                    continue
+                f = _plan_fields(ps)
+                assert int(f["smem"]) <= 232448, ps
+                if f["kernel"] == "depthwise":
+                    checked["depthwise"] += 1
+                    continue
+                w, h, d, n = (int(v[1:]) for v in f["box"].strip("()").split(","))
+                KT = w * h * d * n
+                assert KT == int(f["KT"]) and KT % 16 == 0 and KT <= 256, ps
+                assert int(f["stage_bytes"]) % 1024 == 0, ps
+                assert int(f["mt_per_cta"]) * int(f["Nmma"]) <= int(f["tmem_cols"]) <= 512, ps
+                if f["taps"] == "mn":
+                    checked["mn"] += 1
+                    assert sp["stride"] == [1] * nd and int(f["Nmma"]) == 64 * filt[-1] <= 256, ps
+                    assert " halo " in ps, ps
+                else:
+                    checked["m"] += 1
+                    if kernel == "igemm_taps_mn":
+                        raise AssertionError(f"forced column form planned as rows: {ps}")
+    assert min(checked.values()) > 20, checked

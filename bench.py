@@ -12,7 +12,8 @@ the same computation from pinned host buffers: X and dY copied in, the call,
 dW copied back, all enqueued by the library.  The headline workload is the 2-D dense 56x56, C = K = 64, N = 32, 3x3
 problem with bf16 inputs and bf16 dW; the other workloads, and the other plans
 the measurement table lists for each (split degrees, modes, merge widths, the
-tensor-core depthwise variant), are reported under "workloads".  No step finds
+tensor-core depthwise variant, the tensor-core kernel with every filter tap on
+the MMA rows), are reported under "workloads".  No step finds
 its inputs in L2: each step reads the next of several copies of X and dY whose
 total exceeds twice the L2; inputs too small for that (the 8x8 problem) are
 evicted instead by an L2 flush before every step (a 256 MiB write, then a

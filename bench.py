@@ -6,8 +6,10 @@
 A step is one call of wg_conv_bwd_weight -- the whole path: every launch it makes
 (split-K stage 1, the stage-2 reduce or the atomic-mode memset) -- over one batch
 of synthetic, seeded inputs already resident in HBM.  The device-side value
-times each call between CUDA events on its stream (--graph replays a captured
-CUDA graph of the call instead).  The e2e value times wg_conv_bwd_weight_host,
+times the K steps back to back between one pair of CUDA events on the calls'
+stream and divides by K (steps that need an L2 flush are timed one by one, the
+flush outside the events; --graph replays a captured CUDA graph of the call
+instead).  The e2e value times wg_conv_bwd_weight_host,
 the same computation from pinned host buffers: X and dY copied in, the call,
 dW copied back, all enqueued by the library.  The headline workload is the 2-D dense 56x56, C = K = 64, N = 32, 3x3
 problem with bf16 inputs and bf16 dW; the other workloads, and the other plans
@@ -19,7 +21,8 @@ total exceeds twice the L2; inputs too small for that (the 8x8 problem) are
 evicted instead by an L2 flush before every step (a 256 MiB write, then a
 256 MiB read of another buffer so the write's dirty lines are written back
 before the timed events).  The roofline's kernel time comes from a second pass
-over the same steps with an event recorded right after the main kernel.
+over the same steps with an event recorded at each step's start and one right
+after its main kernel.
 
 Prints one JSON line on rank 0.  Multi-GPU runs (torchrun) are independent
 replicas (weak scaling): the path has no exchange step on one node.
@@ -79,6 +82,7 @@ VARIANTS = [
     ("2d_grouped_g32_c8_k8_n32_h28/atomic", "2d_grouped_g32_c8_k8_n32_h28", 0, "atomic", 0, "auto"),
     ("2d_depthwise_g512_n64_h28/gm8", "2d_depthwise_g512_n64_h28", 0, "auto", 8, "auto"),
     ("2d_depthwise_g512_n64_h28/gm1", "2d_depthwise_g512_n64_h28", 0, "auto", 1, "auto"),
+    ("2d_depthwise_g512_n64_h28/gm2", "2d_depthwise_g512_n64_h28", 0, "auto", 2, "auto"),
     ("2d_depthwise_g512_n64_h28", "2d_depthwise_g512_n64_h28", 0, "auto", 0, "auto"),
     ("2d_depthwise_g512_n64_h28/gm4", "2d_depthwise_g512_n64_h28", 0, "auto", 4, "auto"),
     ("2d_depthwise_g512_n64_h28/gm4_atomic", "2d_depthwise_g512_n64_h28", 0, "atomic", 4, "auto"),
@@ -95,8 +99,11 @@ def out_dims(sp):
     return binding.wg_problem_normalize(sp)
 
 
-def sizes(sp):
-    o = out_dims(sp)
+def sizes(sp, dims=None):
+    """Element counts, FLOPs and algorithmic bytes of a problem.  `dims` computes the
+    output lengths (the library's normalisation by default; the reference arm passes
+    the oracle's, so that it never loads the library)."""
+    o = (dims or out_dims)(sp)
     T = int(np.prod(sp["filt"]))
     P = sp["N"] * int(np.prod(o))
     nx = sp["N"] * int(np.prod(sp["in"])) * sp["G"] * sp["C"]
@@ -106,6 +113,49 @@ def sizes(sp):
     wsz = 4 if sp["out_dtype"] == "fp32" else 2
     return {"out": o, "nx": nx, "ndy": ndy, "ndw": ndw, "flops": flops,
             "bytes": 2.0 * nx + 2.0 * ndy + float(wsz) * ndw, "wsz": wsz}
+
+
+# The five configurations and the modes each is quoted in, as VARIANTS labels
+# (the main line's label is its workload name), for the compact per-config
+# summary printed at the end of the JSON line.
+CONFIG_LABELS = [
+    ("c1_tiny", "2d_tiny_n1_h8_c16_k32"),
+    ("c2_dense_auto", "2d_dense_n32_h56_c64_k64"),
+    ("c2_dense_S1_direct", "2d_dense_n32_h56_c64_k64/S1_direct"),
+    ("c2_dense_S4_det", "2d_dense_n32_h56_c64_k64/S4_deterministic"),
+    ("c3_grouped_auto", "2d_grouped_g32_c8_k8_n32_h28"),
+    ("c3_grouped_atomic", "2d_grouped_g32_c8_k8_n32_h28/atomic"),
+    ("c4_dw_auto", "2d_depthwise_g512_n64_h28"),
+    ("c4_dw_gm1", "2d_depthwise_g512_n64_h28/gm1"),
+    ("c4_dw_gm2", "2d_depthwise_g512_n64_h28/gm2"),
+    ("c4_dw_gm4", "2d_depthwise_g512_n64_h28/gm4"),
+    ("c4_dw_gm8", "2d_depthwise_g512_n64_h28/gm8"),
+    ("c4_dw_gm4_atomic", "2d_depthwise_g512_n64_h28/gm4_atomic"),
+    ("c4_dw_tensor_core", "2d_depthwise_g512_n64_h28/tensor_core"),
+    ("c5_3d_S8_atomic", "3d_n4_d16_c128_k96_s2"),
+    ("c5_3d_S8_det", "3d_n4_d16_c128_k96_s2/S8_deterministic"),
+    ("c5_3d_auto", "3d_n4_d16_c128_k96_s2/auto"),
+]
+
+
+def plan_tag(plan):
+    """A few words of a plan string: kernel, tile form, mode, split degree, merge width."""
+    f = dict(kv.split("=", 1) for kv in plan.split() if "=" in kv)
+    if f.get("kernel") == "depthwise":
+        return f"dw Gm{f['Gm']} {f['mode'][:3]} S{f['S']}"
+    return f"tc {f.get('taps', '')} {f['mode'][:3]} S{f['S']} Gm{f.get('Gm', 1)}"
+
+
+def compact_configs(main_label, main, extra):
+    """Per configuration: [step us, main-kernel roofline fraction, step roofline fraction, plan tag]."""
+    out = {"fields": ["step_us", "kernel_frac", "step_frac", "plan"]}
+    for key, label in CONFIG_LABELS:
+        r = main if label == main_label else extra.get(label)
+        if r is None:
+            continue
+        out[key] = [round(r["ms_per_step"] * 1e3, 2), round(r["kernel_roofline_frac"], 3),
+                    round(r["roofline_frac"], 3), r["tag"]]
+    return out
 
 
 def peaks():
@@ -205,7 +255,7 @@ def run_reference(args, ws, rank):
     nsample = 1
     sps = dict(sp, N=nsample)
     dist, seed = WORKLOADS[args.workload][1], WORKLOADS[args.workload][2]
-    s = sizes(sps)
+    s = sizes(sps, oracle.out_dims)
     x = oracle.decode(synth.tensor_bits(1000 + seed, s["nx"], sp["in_dtype"], *dist), sp["in_dtype"])
     dy = oracle.decode(synth.tensor_bits(2000 + seed, s["ndy"], sp["in_dtype"], *dist), sp["in_dtype"])
     for _ in range(args.warmup):
@@ -230,7 +280,7 @@ def cpu_baseline(name):
     10 s of CPU work have been timed."""
     import oracle
     sp, dist, seed = WORKLOADS[name][0], WORKLOADS[name][1], WORKLOADS[name][2]
-    s = sizes(sp)
+    s = sizes(sp, oracle.out_dims)
     x = oracle.decode(synth.tensor_bits(1000 + seed, s["nx"], sp["in_dtype"], *dist), sp["in_dtype"])
     dy = oracle.decode(synth.tensor_bits(2000 + seed, s["ndy"], sp["in_dtype"], *dist), sp["in_dtype"])
     runs, t0 = 0, time.perf_counter()
@@ -390,10 +440,13 @@ class L2Flush:
 
 
 def time_steps(torch, wl, steps, warmup, flush, stream, e2e=False, mark=False):
-    """Per-step CUDA-event times (ms) on `stream`; inputs not in L2 at each step
-    (rotating copies, else an L2 flush before the step).  With `mark`, the times
-    run from the step's start to the end of the call's main kernel (an event the
-    library records between its main and its reduction kernel)."""
+    """CUDA-event times (ms) of `steps` steps on `stream`, one entry per step;
+    inputs not in L2 at each step (rotating copies, else an L2 flush before the
+    step).  Steps that need no flush run back to back between one pair of events
+    (every entry is then the average); flushed steps are timed one by one with
+    the flush outside the events.  With `mark`, each time runs from the step's
+    start to the end of the call's main kernel (an event the library records
+    between its main and its reduction kernel)."""
     fn = wl.e2e_step if e2e else wl.step
     do_flush = not e2e and (not wl.rotating or wl.graph is not None)
     with torch.cuda.stream(stream):
@@ -402,6 +455,15 @@ def time_steps(torch, wl, steps, warmup, flush, stream, e2e=False, mark=False):
                 flush()
             fn(stream)
         stream.synchronize()
+        if not do_flush and not mark:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(steps):
+                fn(stream)
+            b.record(stream)
+            stream.synchronize()
+            binding.wg_check_status(stream)
+            return [a.elapsed_time(b) / steps] * steps
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         if mark:
             for _, b in evs:
@@ -480,6 +542,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=HEADLINE, choices=list(WORKLOADS))
+    ap.add_argument("--variant", default=None, choices=[v[0] for v in VARIANTS],
+                    help="time this listed plan (a label of VARIANTS) as the main line; sets --workload")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads and the CPU baseline")
     ap.add_argument("--graph", action="store_true", help="replay a CUDA graph of the call instead of calling it")
     ap.add_argument("--dgrad", action="store_true",
@@ -520,7 +584,11 @@ def main():
                               "ms_per_step": ms, "config": {"workload": args.workload, "plan": w3.plan}}), flush=True)
         return
 
-    wl = Workload(torch, args.workload)
+    main_plan = None
+    if args.variant:
+        vlab = {v[0]: v for v in VARIANTS}[args.variant]
+        args.workload, main_plan = vlab[1], tuple(vlab[2:])
+    wl = Workload(torch, args.workload, plan=main_plan)
     if args.graph:
         wl.capture(stream)
     sampler = ClockSampler(local)
@@ -573,7 +641,7 @@ def main():
     extra = {}
     if rank == 0 and not args.no_extra:
         for label, name, *plan in VARIANTS:
-            if name == args.workload and label == name:
+            if label == (args.variant or args.workload):
                 continue
             w2 = Workload(torch, name, plan=tuple(plan))
             if args.graph:
@@ -584,6 +652,7 @@ def main():
             s2 = w2.s
             tf, tb = s2["flops"] / (pk["bf16"] * 1e12), s2["bytes"] / (pk["hbm"] * 1e9)
             extra[label] = {"ms_per_step": ms, "tflops": s2["flops"] / (ms * 1e-3) / 1e12,
+                            "tag": plan_tag(w2.plan),
                            "gbs": s2["bytes"] / (ms * 1e-3) / 1e9, "roofline_us": max(tf, tb) * 1e6,
                            "bound": "hbm" if tb >= tf else "tensor",
                            "roofline_frac": max(tf, tb) / (ms * 1e-3), "kernel_ms": kms,
@@ -608,7 +677,7 @@ def main():
                 "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16" if wl.sp["in_dtype"] == "bf16" else "fp16",
                 "data": "synthetic (seeded splitmix64)",
-                "config": {"workload": args.workload, "G": wl.sp["G"], "N": wl.sp["N"], "in": wl.sp["in"],
+                "config": {"workload": args.workload, "variant": args.variant, "G": wl.sp["G"], "N": wl.sp["N"], "in": wl.sp["in"],
                            "C": wl.sp["C"], "K": wl.sp["K"], "filt": wl.sp["filt"], "stride": wl.sp["stride"],
                            "pad": wl.sp["pad_l"], "in_dtype": wl.sp["in_dtype"], "out_dtype": wl.sp["out_dtype"],
                            "split_k": wl.split_k, "mode": wl.mode, "plan": wl.plan,
@@ -622,6 +691,10 @@ def main():
                 "wall_s_timed": t_wall, "workloads": extra}
         if ws == 1 and not args.no_extra:
             line["cpu_baseline"] = cpu_baseline(args.workload)
+        if extra:
+            main = {"ms_per_step": step_ms, "kernel_roofline_frac": roof["frac"], "roofline_frac": roof["step_frac"],
+                    "tag": plan_tag(wl.plan)}
+            line["configs"] = compact_configs(args.variant or args.workload, main, extra)
         print(json.dumps(line), flush=True)
     if pg:
         pg.barrier()

@@ -20,10 +20,12 @@
 //    not once per tap;
 //  * B = W tiles (rows = k, 128 bytes = 64 c, MN-major), one per tap, loaded
 //    from a (C, taps, K, G) view of W so that k beyond the group reads zero;
-//  * fp32 accumulators in TMEM; all eight warps store dX (one pixel per lane).
+//  * fp32 accumulators in TMEM, two buffers; warps 2..5 read them (one TMEM
+//    lane quadrant, i.e. 32 pixels, per warp) and store dX.
 //
-// Warp roles as in the weight-gradient kernel: warp 0 lane 0 issues TMA into
-// an mbarrier ring, warp 1 issues the MMAs, every wait is bounded.
+// Warp roles (192 threads): warp 0 lane 0 issues TMA into an mbarrier ring,
+// warp 1 issues the MMAs, warps 2..5 run the epilogue while the next tile's
+// loads and MMAs proceed; every wait is bounded.
 #pragma once
 
 #include <cuda_bf16.h>

@@ -31,9 +31,10 @@
 // read as xs 64-column atoms one dil_w row apart -- 128x192x16 MMAs for 3x3
 // filters, at the tensor rate.
 //
-// Warp roles (192 threads): warp 0 lane 0 issues TMA; warp 1 owns TMEM and its
-// lane 0 issues tcgen05.mma; warps 2..5 read TMEM (lane quadrant = warp % 4)
-// and store dW / atomically add / write the split-K workspace.
+// Warp roles (256 threads): warp 0 lane 0 issues TMA; warp 1 owns TMEM and, as
+// a converged warp, issues tcgen05.mma from one elected lane; after the main
+// loop all eight warps read TMEM (lane quadrant = warp % 4, column half =
+// warp / 4) and store dW / atomically add / write the split-K workspace.
 #pragma once
 
 #include <cuda_bf16.h>

@@ -337,9 +337,9 @@ class Workload:
         self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device="cuda")
         self.plan = binding.wg_plan_string(sp, self.split_k, self.mode, self.gm, **kw)
         # This library's kernels per call: the main kernel, plus the split reduction
-        # kernel where the plan has one ("reduce=kernel"; the atomic mode's memset
-        # is a runtime call).
-        self.launches_per_step = 1 + (1 if "reduce=kernel" in self.plan else 0)
+        # kernel ("reduce=kernel") or the kernel that zeroes dW before atomic
+        # accumulation ("zero=kernel") where the plan has one.
+        self.launches_per_step = 1 + (1 if "reduce=kernel" in self.plan else 0) + (1 if "zero=kernel" in self.plan else 0)
         self.call = binding.PreparedCall(sp, self.x, self.dy, self.dw, self.split_k, self.mode, self.gm, self.ws,
                                          self.ws_bytes, **kw)
         self.graph = None

@@ -280,28 +280,66 @@ __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
     }
     __syncthreads();
     // ---------------------------------------------------- reduce over the CTA
+    // Thread tid holds channel vector v = tid % NV of slot tid / NV (a row and
+    // column segment of the tile).  When NV divides 32, each warp first adds its
+    // 32 / NV slots with a butterfly of shuffles (lanes l and l ^ m, m = 16, 8,
+    // ... down to NV; the steps are unrolled so that the 9 * GM chains
+    // interleave), lanes 0..NV-1 store the warp's sums, and the warps' sums are
+    // added in warp order.  Otherwise every slot is stored and the slots are
+    // added in order.  Both orders are fixed: the result is reproducible.
     float* red = reinterpret_cast<float*>(smem);
-    if (tid < p.nused) {
-        const int slot = tid / NV, v = tid % NV;
+    const bool shfl = NV < 32 && (32 % NV) == 0;
+    int nparts;
+    if (shfl) {
+        nparts = n_cwarps;
+        if (warp < n_cwarps) {
 #pragma unroll
-        for (int t = 0; t < MAXT; ++t)
-            if (t < p.T)
+            for (int m = 16; m >= 1; m >>= 1) {
+                if (m < NV) break;
 #pragma unroll
-                for (int j = 0; j < GM; ++j) red[(slot * p.T + t) * p.CB + v * GM + j] = acc[t][j];
+                for (int t = 0; t < MAXT; ++t)
+#pragma unroll
+                    for (int j = 0; j < GM; ++j) acc[t][j] += __shfl_xor_sync(0xffffffffu, acc[t][j], m);
+            }
+            if (lane < NV) {
+#pragma unroll
+                for (int t = 0; t < MAXT; ++t)
+                    if (t < p.T)
+#pragma unroll
+                        for (int j = 0; j < GM; ++j) red[(warp * p.CB + lane * GM + j) * p.T + t] = acc[t][j];
+            }
+        }
+    } else {
+        nparts = p.nused / NV;
+        if (tid < p.nused) {
+            const int slot = tid / NV, v = tid % NV;
+#pragma unroll
+            for (int t = 0; t < MAXT; ++t)
+                if (t < p.T)
+#pragma unroll
+                    for (int j = 0; j < GM; ++j) red[(slot * p.CB + v * GM + j) * p.T + t] = acc[t][j];
+        }
     }
     __syncthreads();
-    const int nslots = p.R * p.nseg;
-    for (int idx = tid; idx < p.T * p.CB; idx += blockDim.x) {
-        const int t = idx / p.CB, c = idx - t * p.CB;
+    // One output (c, t) per thread, idx = c * T + t (the parts are stored in
+    // that order, so that the reads are consecutive words): the parts added in
+    // order.  dW index o = g * T + t; its workspace offset uses 32-bit
+    // arithmetic (the depthwise workspace is one row of G * T < 2^31 elements).
+    const int TC = p.T * p.CB, W = p.ws.W;
+    // Atomic accumulation: wait for the kernel that zeroes dW (see zero_f32_kernel).
+    if (p.mode == 2) pdl_wait();
+    for (int idx = tid; idx < TC; idx += blockDim.x) {
+        const int c = idx / p.T, t = idx - c * p.T;
         float s = 0.f;
-        for (int sl = 0; sl < nslots; ++sl) s += red[(sl * p.T + t) * p.CB + c];
+        for (int sl = 0; sl < nparts; ++sl) s += red[sl * TC + idx];
         const int g = cb * p.CB + c;
         if (g >= p.G) continue;
-        const long long o = (long long)g * p.T + t;
+        const int o = g * p.T + t;
         if (p.mode == 2) {
             if (ntl > 0) red_add_f32(static_cast<float*>(p.out) + o, s);
         } else if (p.mode == 3) {
-            static_cast<float*>(p.out)[ws_offset(p.ws, o, split)] = s;
+            const int jw = o / W;
+            static_cast<float*>(p.out)[((long long)jw * p.ws.S + split) * W + (o - jw * W)] = s;
         } else if (p.out_dtype == 2) {
             static_cast<float*>(p.out)[o] = s;
         } else if (p.out_dtype == 0) {

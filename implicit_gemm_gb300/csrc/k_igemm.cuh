@@ -459,6 +459,10 @@ __global__ void __launch_bounds__(kIgThreads, 1)
     __syncwarp();
     // ---------------------------------------------------- epilogue (all warps)
     named_bar_sync(2, kIgThreads);  // the producer is done and may read tbase
+    // Atomic accumulation: dW was zeroed by a kernel launched just before this
+    // one (programmatic dependent launch); wait for it only here, so that its
+    // launch and run overlap the main loop.
+    if (p.mode == 2) pdl_wait();
     tc_fence_after();
     tbase = *tslot;
     {
@@ -564,6 +568,21 @@ __global__ void __launch_bounds__(kIgThreads, 1)
         tc_fence_after();
         tmem_dealloc(tbase, (uint32_t)p.tmem_cols);
     }
+}
+
+// dW = 0 before atomic split-K accumulation (the page's Preprocess zeroes the
+// output when k_batch > 1).  Launched just before the main kernel, which is a
+// programmatic dependent of it: the main kernel's CTAs start at once and wait
+// for this grid (griddepcontrol.wait) only before their first atomic add.
+__global__ void __launch_bounds__(256) zero_f32_kernel(float* __restrict__ p, long long n)
+{
+    pdl_launch_dependents();
+    const long long n4 = n >> 2;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    float4* p4 = reinterpret_cast<float4*>(p);  // 16-byte aligned (checked on the host)
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride)
+        p4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long i = (n4 << 2) + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = 0.f;
 }
 
 // Stage 2 of the deterministic split-K mode (the two-stage wgrad that PR

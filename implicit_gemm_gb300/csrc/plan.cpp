@@ -706,21 +706,22 @@ std::string plan_string(const Plan& pl)
                  "katoms=%d "
                  "box=(w%d,h%d,d%d,n%d) KT=%d ktiles=%lld per_split=%lld atoms=%d mtiles=%d mt_per_cta=%d "
                  "mranges=%d tmem_cols=%d stages=%d stage_bytes=%d smem=%d grid=(%u,%u,%u) block=%u ws=%zu "
-                 "reduce=%s",
+                 "reduce=%s zero=%s",
                  ig.halo ? "halo" : "pertap", ig.xs ? "mn" : "m", ig.Nmma, mode, pl.S, ig.cluster, ig.Gm, ig.n_gblocks, ig.n_cchunks, ig.Nt, ig.n_ntiles, ig.n_katoms, ig.box[0], ig.box[1],
                  ig.box[2], ig.box[3], ig.KT, ig.total_kt, pl.per_split, ig.n_atoms, ig.n_mtiles, ig.mt_per_cta,
                  ig.n_mranges, ig.tmem_cols, ig.stages, ig.stage_bytes, ig.smem_bytes, pl.grid[0], pl.grid[1],
-                 pl.grid[2], pl.block, pl.ws_bytes, pl.mode == MODE_DETERMINISTIC ? "kernel" : "none");
+                 pl.grid[2], pl.block, pl.ws_bytes, pl.mode == MODE_DETERMINISTIC ? "kernel" : "none",
+                 pl.mode == MODE_ATOMIC ? "kernel" : "none");
     } else {
         const DwPlan& dw = pl.dw;
         snprintf(buf, sizeof buf,
                  "kernel=depthwise mode=%s S=%d Gm=%d CB=%d cblocks=%d R=%d nseg=%d seg_len=%d threads=%d "
                  "xtile=(w%d,h%d) tiles=%lld per_split=%lld stages=%d stage_bytes=%d smem=%d sliding=%d "
-                 "grid=(%u,%u,%u) block=%u ws=%zu reduce=%s",
+                 "grid=(%u,%u,%u) block=%u ws=%zu reduce=%s zero=%s",
                  mode, pl.S, dw.Gm, dw.CB, dw.n_cblocks, dw.R, dw.nseg, dw.seg_len, dw.threads, dw.xw, dw.xh,
                  dw.total_tiles, pl.per_split, dw.stages, dw.stage_bytes, dw.smem_bytes, dw.sliding, pl.grid[0],
                  pl.grid[1], pl.grid[2], pl.block, pl.ws_bytes,
-                 pl.mode == MODE_DETERMINISTIC ? "kernel" : "none");
+                 pl.mode == MODE_DETERMINISTIC ? "kernel" : "none", pl.mode == MODE_ATOMIC ? "kernel" : "none");
     }
     (void)pb;
     return buf;

@@ -271,6 +271,11 @@ __device__ __forceinline__ void pdl_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Wait until the grid this one was launched behind (with the
+// programmatic-serialization attribute) has completed and its memory
+// operations are visible; returns at once when there is none.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {

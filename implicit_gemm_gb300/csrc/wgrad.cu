@@ -384,11 +384,18 @@ int launch_reduce(const wg::Plan& pl, void* ws, void* dw, cudaStream_t stream)
 
 // A call runs as launch_pre (zero dW for atomic accumulation), the main kernel
 // (launch_main), then launch_post (the mark event, then the split reduction).
+// The zeroing is a kernel of this library rather than cudaMemsetAsync: the main
+// kernel is launched as its programmatic dependent and waits for it only
+// before its atomic adds (a memset before the main kernel measured ~4 us per
+// call on GB300, a dependent zeroing kernel is hidden behind the main loop).
 int launch_pre(const wg::Plan& pl, void* dw, cudaStream_t stream)
 {
     if (pl.mode == wg::MODE_ATOMIC) {
-        const cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)pl.pb.dw_elems * 4, stream);
-        if (e != cudaSuccess) return cuda_fail("cudaMemsetAsync(dW)", e);
+        const long long n = pl.pb.dw_elems;
+        const long long blocks = std::max(1LL, std::min<long long>((n / 4 + 255) / 256, 4LL * num_sms()));
+        wg::zero_f32_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<float*>(dw), n);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail("zero_f32_kernel launch", e);
     }
     return WG_OK;
 }
@@ -400,16 +407,28 @@ int launch_igemm_main(const wg::Plan& pl, const Prepared& pr, cudaStream_t strea
     if (st) return st;
     const dim3 grid(pl.grid[0], pl.grid[1], pl.grid[2]);
     cudaError_t e;
-    if (ig.cluster > 1) {
-        // Consecutive splits form a cluster (grid z is a multiple of the cluster size).
+    const bool after_zero = pl.mode == wg::MODE_ATOMIC;
+    if (ig.cluster > 1 || after_zero) {
+        // Consecutive splits form a cluster (grid z is a multiple of the cluster
+        // size); in atomic mode the kernel is a programmatic dependent of the
+        // zeroing kernel.
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 1;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = (unsigned)ig.cluster;
+        cudaLaunchAttribute attr[2];
+        unsigned na = 0;
+        if (ig.cluster > 1) {
+            attr[na].id = cudaLaunchAttributeClusterDimension;
+            attr[na].val.clusterDim.x = 1;
+            attr[na].val.clusterDim.y = 1;
+            attr[na].val.clusterDim.z = (unsigned)ig.cluster;
+            ++na;
+        }
+        if (after_zero) {
+            attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[na].val.programmaticStreamSerializationAllowed = 1;
+            ++na;
+        }
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = na;
         cfg.gridDim = grid;
         cfg.blockDim = dim3(pl.block);
         cfg.dynamicSmemBytes = (size_t)ig.smem_bytes;
@@ -440,8 +459,24 @@ int launch_dw_t(const wg::Plan& pl, dim3 grid, const CUtensorMap& tmx, const CUt
     auto k = wg::depthwise_wgrad_kernel<BF16, GM, SLIDE>;
     const int st = ensure_smem(k, pl.dw.smem_bytes);
     if (st) return st;
-    k<<<grid, pl.block, pl.dw.smem_bytes, stream>>>(tmx, tmy, prm);
-    const cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if (pl.mode == wg::MODE_ATOMIC) {
+        // A programmatic dependent of the kernel that zeroes dW.
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(pl.block);
+        cfg.dynamicSmemBytes = (size_t)pl.dw.smem_bytes;
+        cfg.stream = stream;
+        e = cudaLaunchKernelEx(&cfg, k, tmx, tmy, prm);
+    } else {
+        k<<<grid, pl.block, pl.dw.smem_bytes, stream>>>(tmx, tmy, prm);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return cuda_fail("depthwise_wgrad_kernel launch", e);
     return WG_OK;
 }
@@ -707,7 +742,9 @@ void* g_noalloc_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.  In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// per device (with that device current) and cached for the life of the
+// process: a cudaDeviceReset ends the context the address belongs to, and the
+// cached value must not be used after it.
 int noalloc_scratch(void** out)
 {
     int dev = 0;
@@ -741,29 +778,33 @@ int wg_conv_bwd_weight_noalloc(const wg_problem* p, const void* x, const void* d
     st = wg_workspace_size(p, &o, &need);
     if (st) return st;
     if (need > kNoAllocScratchBytes) {
-        wg::Problem pb;
-        std::string err;
-        if (wg::normalize(p, &pb, &err)) return set_err(WG_ERR_INVALID_ARGUMENT, err);
-        // Workspace bytes per partial (rows of whole 4-element-aligned slices).
-        wg::Plan pl1;
-        wg_options o1 = o;
-        o1.split_k = 1;
-        o1.mode = WG_MODE_DETERMINISTIC;
-        o1.cluster = 1;
-        if (plan_for(p, &o1, &pl1)) return WG_ERR_INVALID_ARGUMENT;
-        const size_t per_split = (size_t)pl1.ws_rows * pl1.ws_nj * pl1.ws_W * 4;
-        const size_t fit = kNoAllocScratchBytes / per_split;
-        if (o.split_k != 0 || fit < 2) {
+        if (o.split_k != 0) {
             char buf[256];
             snprintf(buf, sizeof buf,
                      "the no-allocation entry point has %zu bytes of scratch; this problem and split degree need %zu",
                      kNoAllocScratchBytes, need);
             return set_err(WG_ERR_WORKSPACE, buf);
         }
-        // Automatic split degree: the largest that fits the scratch array.
-        o.split_k = (int)std::min<size_t>(fit, 65535);
-        st = wg_workspace_size(p, &o, &need);
-        if (st) return st;
+        // Automatic split degree: the largest that fits the scratch array.  One
+        // partial sum per cluster of Q splits reaches the workspace, so Q * fit
+        // splits fit; when not even two partials fit, one split (direct mode,
+        // no workspace).
+        wg::Plan pl1;
+        wg_options o1 = o;
+        o1.split_k = 1;
+        o1.mode = WG_MODE_DETERMINISTIC;
+        o1.cluster = 1;
+        if ((st = plan_for(p, &o1, &pl1))) return st;
+        const size_t per_partial = (size_t)pl1.ws_rows * pl1.ws_nj * pl1.ws_W * 4;
+        const size_t fit = kNoAllocScratchBytes / per_partial;
+        const int Q = o.cluster > 1 ? o.cluster : 1;
+        if (fit < 2) {
+            o.split_k = Q;
+            if (Q > 1) o.mode = WG_MODE_DIRECT;  // one cluster: its sum is dW
+        } else {
+            o.split_k = (int)std::min<size_t>(fit * Q, (size_t)(65535 / Q) * Q);
+        }
+        if ((st = wg_workspace_size(p, &o, &need))) return st;
         if (need > kNoAllocScratchBytes) return set_err(WG_ERR_WORKSPACE, "split-K workspace does not fit the scratch array");
     }
     return wg_conv_bwd_weight(p, x, dy, dw, &o, need ? scratch : nullptr, need ? kNoAllocScratchBytes : 0, stream);

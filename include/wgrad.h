@@ -53,8 +53,10 @@ typedef enum { WG_BF16 = 0, WG_FP16 = 1, WG_FP32 = 2 } wg_dtype;
 /* How split-K partial sums are combined.
  *  DIRECT:        no split (split_k must be 1 or 0); dW = cast(sum).
  *  ATOMIC:        dW is zeroed on the stream first (the Preprocess memset of the
- *                 CK page), then every split adds its fp32 partial with a
- *                 global atomic.  fp32 dW only.  Not bitwise reproducible.
+ *                 CK page; here a kernel whose successor, the split-K kernel,
+ *                 waits for it only before its first add), then every split
+ *                 adds its fp32 partial with a global atomic.  fp32 dW only.
+ *                 Not bitwise reproducible.
  *  DETERMINISTIC: two-stage: every split writes an fp32 partial to the
  *                 workspace, then a second kernel sums the splits in a fixed
  *                 order (for S >= 8: four contiguous ranges of splits, each in
@@ -152,9 +154,14 @@ typedef struct {
  * Returns WG_OK or WG_ERR_INVALID_ARGUMENT.  Host only. */
 WG_API int wg_problem_normalize(wg_problem* p);
 
-/* Bytes of device workspace that wg_conv_bwd_weight needs for (p, opt)
- * (0 unless the chosen mode is DETERMINISTIC with more than one split, where it
- * is S * G*K*Z*Y*X*C * 4, the unmerged size).  opt may be NULL (all defaults).
+/* Bytes of device workspace that wg_conv_bwd_weight needs for (p, opt): the
+ * caller-visible workspace sizing of the two-stage (deterministic split-K)
+ * path, sized from the unmerged dimensions as the PR #12359 page ("add group
+ * merging (Gm) for depthwise grouped conv", PR #12951's
+ * wgrad_two_stage_workspace_nbytes) states it.  0 unless the chosen mode is
+ * DETERMINISTIC with more than one partial sum reaching memory, where it is
+ * (partials) * G*K*Z*Y*X*C * 4 bytes, each (g, k) row of Z*Y*X*C rounded up to
+ * whole reduction slices.  opt may be NULL (all defaults).
  * Returns WG_OK, WG_ERR_INVALID_ARGUMENT or WG_ERR_NOT_SUPPORTED.  Host only. */
 WG_API int wg_workspace_size(const wg_problem* p, const wg_options* opt, size_t* bytes);
 
@@ -196,12 +203,16 @@ WG_API const char* wg_last_error(void);
  *
  * Arguments and results are those of wg_conv_bwd_weight without the workspace.
  * With split_k = 0 the split degree is capped so that the partial sums fit the
- * array; an explicit split_k (or a dW too large for two splits) that needs more
- * than 16 MiB returns WG_ERR_WORKSPACE with the sizes in wg_last_error().
+ * array (with clusters of Q splits, Q times as many splits fit); when not even
+ * two partial sums of dW fit, the call runs one split (one cluster), which
+ * needs no workspace.  An explicit split_k whose partial sums need more than
+ * 16 MiB returns WG_ERR_WORKSPACE with the sizes in wg_last_error().
  *
  * The first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call before any stream
- * capture.  All calls share the one array and it keeps the last call's
+ * device current) and caches it for the rest of the process; make that first
+ * call before any stream capture, and make no call on a device after a
+ * cudaDeviceReset of it (the cached address belongs to the context the reset
+ * destroyed).  All calls share the one array and it keeps the last call's
  * contents; the kernels write every element they later read, so nothing needs
  * clearing, but calls whose work overlaps on the GPU (other streams, other
  * threads) race on it and must be serialised by the caller. */

@@ -3,7 +3,8 @@ once, and from several host threads.
 
 * Graphs: a deterministic weight-gradient call (split-K kernel plus the
   reduction kernel it launches with programmatic dependent launch), an atomic
-  one (memset node), a backward-data call and a host-buffer call are captured
+  one (the kernel that zeroes dW, then the split-K kernel launched as its
+  programmatic dependent), a backward-data call and a host-buffer call are captured
   once and replayed with new input values copied into the same buffers; each
   replay must give the bits of an eager call on those values.
 * Streams: four different problems launched on four streams without

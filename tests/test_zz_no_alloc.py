@@ -45,7 +45,16 @@ CASES = [
     ("depthwise_3d_split3", spec(3, 8, 2, 1, 1, [5, 6, 5], [3, 3, 3], [1, 1, 1], [1, 1, 1], [1, 1, 1], [1, 1, 1]),
      3, "deterministic", 0),
     ("depthwise_2d_auto", spec(2, 64, 3, 1, 1, [12, 10], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]), 0, "auto", 8),
+    # The automatic plan's partial sums need more than the 16 MiB array
+    # (S = 8 partials of 2.25 MiB): the call caps the split degree to 7.
+    ("capped_auto_split", spec(2, 1, 8, 256, 256, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]), 0, "auto", 0),
+    # One partial sum of dW is 9 MiB, so not even two fit: the call runs one
+    # split (direct mode, no workspace).
+    ("direct_when_two_partials_do_not_fit", spec(2, 1, 8, 512, 512, [14, 14], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
+     0, "auto", 0),
 ]
+
+SCRATCH_BYTES = 16 << 20
 
 
 @pytest.mark.parametrize("name,sp,split_k,mode,gm", CASES, ids=[c[0] for c in CASES])
@@ -55,7 +64,10 @@ def test_noalloc_matches_regular_entry_twice(name, sp, split_k, mode, gm):
     else:
         x, dy = make_inputs(sp, ("uniform", -1.0, 1.0), 91, 92)
     dt = sp["in_dtype"]
-    _, A = oracle.wgrad(sp, oracle.decode(x, dt), oracle.decode(dy, dt))
+    if name in ("capped_auto_split", "direct_when_two_partials_do_not_fit"):
+        # the case must reach the branch it is named for
+        assert binding.wg_workspace_size(sp, split_k, mode, gm) > SCRATCH_BYTES
+    ref_dw, A = oracle.wgrad(sp, oracle.decode(x, dt), oracle.decode(dy, dt))
     xd, dyd = _dev(x, dt), _dev(dy, dt)
     ref = _out(sp)
     binding.conv_bwd_weight(sp, xd, dyd, split_k, mode, gm, out=ref)
@@ -68,6 +80,7 @@ def test_noalloc_matches_regular_entry_twice(name, sp, split_k, mode, gm):
         binding.wg_check_status()
         got_np = got.float().cpu().numpy().astype(np.float64)
         assert_close(got_np, ref_np, A, sp["out_dtype"], f"{name} call {call}")
+        assert_close(got_np, ref_dw, A, sp["out_dtype"], f"{name} call {call} against the oracle")
         if first is None:
             first = got_np
         else:

@@ -79,12 +79,13 @@ VARIANTS = [
     ("2d_dense_n32_h56_c64_k64/S4_deterministic", "2d_dense_n32_h56_c64_k64", 4, "deterministic", 0, "auto"),
     ("2d_dense_n32_h56_c64_k64/taps_m", "2d_dense_n32_h56_c64_k64", 0, "auto", 0, "igemm_taps_m"),
     ("2d_grouped_g32_c8_k8_n32_h28", "2d_grouped_g32_c8_k8_n32_h28", 0, "auto", 0, "auto"),
-    ("2d_grouped_g32_c8_k8_n32_h28/atomic", "2d_grouped_g32_c8_k8_n32_h28", 0, "atomic", 0, "auto"),
-    ("2d_depthwise_g512_n64_h28/gm8", "2d_depthwise_g512_n64_h28", 0, "auto", 8, "auto"),
-    ("2d_depthwise_g512_n64_h28/gm1", "2d_depthwise_g512_n64_h28", 0, "auto", 1, "auto"),
-    ("2d_depthwise_g512_n64_h28/gm2", "2d_depthwise_g512_n64_h28", 0, "auto", 2, "auto"),
+    ("2d_grouped_g32_c8_k8_n32_h28/deterministic", "2d_grouped_g32_c8_k8_n32_h28", 0, "deterministic", 0, "auto"),
+    # Merge degrees with the two-stage epilogue pinned, as the pages compare them.
+    ("2d_depthwise_g512_n64_h28/gm8", "2d_depthwise_g512_n64_h28", 0, "deterministic", 8, "auto"),
+    ("2d_depthwise_g512_n64_h28/gm1", "2d_depthwise_g512_n64_h28", 0, "deterministic", 1, "auto"),
+    ("2d_depthwise_g512_n64_h28/gm2", "2d_depthwise_g512_n64_h28", 0, "deterministic", 2, "auto"),
     ("2d_depthwise_g512_n64_h28", "2d_depthwise_g512_n64_h28", 0, "auto", 0, "auto"),
-    ("2d_depthwise_g512_n64_h28/gm4", "2d_depthwise_g512_n64_h28", 0, "auto", 4, "auto"),
+    ("2d_depthwise_g512_n64_h28/gm4", "2d_depthwise_g512_n64_h28", 0, "deterministic", 4, "auto"),
     ("2d_depthwise_g512_n64_h28/gm4_atomic", "2d_depthwise_g512_n64_h28", 0, "atomic", 4, "auto"),
     ("2d_depthwise_g512_n64_h28/tensor_core", "2d_depthwise_g512_n64_h28", 0, "auto", 0, "igemm"),
     ("3d_n4_d16_c128_k96_s2", "3d_n4_d16_c128_k96_s2", 8, "atomic", 0, "auto"),
@@ -124,7 +125,7 @@ CONFIG_LABELS = [
     ("c2_dense_S1_direct", "2d_dense_n32_h56_c64_k64/S1_direct"),
     ("c2_dense_S4_det", "2d_dense_n32_h56_c64_k64/S4_deterministic"),
     ("c3_grouped_auto", "2d_grouped_g32_c8_k8_n32_h28"),
-    ("c3_grouped_atomic", "2d_grouped_g32_c8_k8_n32_h28/atomic"),
+    ("c3_grouped_det", "2d_grouped_g32_c8_k8_n32_h28/deterministic"),
     ("c4_dw_auto", "2d_depthwise_g512_n64_h28"),
     ("c4_dw_gm1", "2d_depthwise_g512_n64_h28/gm1"),
     ("c4_dw_gm2", "2d_depthwise_g512_n64_h28/gm2"),

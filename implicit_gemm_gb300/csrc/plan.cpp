@@ -102,12 +102,15 @@ struct IgCand {
 };
 
 // Cost terms of the split-K epilogue, in SM cycles (GB300 at ~2 GHz): L2
-// takes ~2900 bytes per cycle device-wide; a second (reduction) kernel adds a
-// few microseconds of launch and ramp; the cluster reduction writes the CTA's
-// partial sums to shared memory and reads them back through distributed
-// shared memory at ~12 B/cycle (measured), plus two cluster barriers.
+// takes ~2900 bytes per cycle device-wide; every kernel beyond the main one
+// (the reduction of the two-stage path, the zeroing kernel of the atomic path)
+// adds one launch, ~2.07 us per kernel in a stream of back-to-back calls
+// (measured with empty kernels: 2.07 us per call for one kernel, 4.1 us for
+// two); the cluster reduction writes the CTA's partial sums to shared memory
+// and reads them back through distributed shared memory at ~12 B/cycle
+// (measured), plus two cluster barriers.
 constexpr long long kL2BytesPerClk = 2900;
-constexpr long long kReduceLaunchClk = 3000;
+constexpr long long kExtraLaunchClk = 4280;
 // Cold reads from HBM, device-wide (~6 TB/s at ~2 GHz): no split degree reads
 // the inputs faster than this.
 constexpr long long kDramBytesPerClk = 3000;
@@ -117,14 +120,25 @@ long long epilogue_clk(long long dw_bytes, int n_out, int Q, long long red_bytes
     long long c = 0;
     if (Q > 1) c += red_bytes / 128 + red_bytes / 12 + 1500;
     if (atomic) {
-        c += (long long)n_out * dw_bytes / (kL2BytesPerClk / 3);
+        if (n_out > 1) c += (long long)n_out * dw_bytes / (kL2BytesPerClk / 3) + kExtraLaunchClk;
     } else if (n_out > 1) {
-        c += 2 * (long long)n_out * dw_bytes / kL2BytesPerClk + kReduceLaunchClk;
+        c += 2 * (long long)n_out * dw_bytes / kL2BytesPerClk + kExtraLaunchClk;
     }
     return c;
 }
 
 int cap_index(int q) { return q == 1 ? 0 : q == 2 ? 1 : q == 4 ? 2 : 3; }
+
+// Whether split partial sums are added with atomics: mode ATOMIC, or mode
+// AUTO with an fp32 dW (the fp32 atomic add writes dW directly; 16-bit dW
+// goes through the two-stage path).  On GB300 the atomic path -- a zeroing
+// kernel hidden behind the main loop, then one fp32 add per partial element
+// -- measured faster than the two-stage one (partials written, a second
+// kernel summing them) on every fp32 workload of the benchmark.
+bool takes_atomic(const wg_options& o, const Problem& pb)
+{
+    return o.mode == WG_MODE_ATOMIC || (o.mode == WG_MODE_AUTO && pb.out_dtype == WG_FP32);
+}
 
 // Cycles the device needs to read the inputs once from HBM: all of dY, and the
 // part of X that some tap reaches (along each dim a fraction of about
@@ -302,6 +316,7 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
                 const long long base = mranges * c.n_ntiles * ig.n_gblocks;
                 const long long s_fill = split_for(o, base, ktiles, caps);
                 const bool auto_s = o.split_k == 0 && o.mode != WG_MODE_DIRECT && o.cluster <= 1;
+                const bool atomic_sum = takes_atomic(o, pb);
                 const long long dram_clk = dram_read_clk(pb);
                 const long long red_bytes = (long long)mt * c.Nmma * 512;
                 for (int fi = 0; fi < (auto_s ? 4 : 1); ++fi) {
@@ -313,8 +328,7 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
                     const long long waves = cdiv(base * S, caps.cluster_ctas[0]);
                     const long long main_clk = waves * cdiv(ktiles, S) * tile_clk;
                     const long long cost = std::max(main_clk, dram_clk) + main_clk / 8 +
-                                           epilogue_clk(pb.dw_elems * 4, (int)S, 1, red_bytes,
-                                                        o.mode == WG_MODE_ATOMIC);
+                                           epilogue_clk(pb.dw_elems * 4, (int)S, 1, red_bytes, atomic_sum);
                     if (best.cost < 0 || cost < best.cost) {
                         c.mt = mt;
                         c.stages = stages;
@@ -412,7 +426,7 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
         return fail(err, WG_ERR_NOT_SUPPORTED,
                     "cluster reduction: the CTA's partial sums (%lld bytes) do not fit its shared memory", red_bytes);
     const long long dw_bytes = pb.dw_elems * 4;
-    const bool atomic = o.mode == WG_MODE_ATOMIC;
+    const bool atomic = takes_atomic(o, pb);
     int S, Q;
     if (o.split_k > 0) {
         S = o.split_k;
@@ -666,6 +680,8 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
         pl->mode = MODE_ATOMIC;
     else if (n_out == 1)
         pl->mode = MODE_DIRECT;
+    else if (takes_atomic(o, pb))
+        pl->mode = MODE_ATOMIC;
     else
         pl->mode = MODE_DETERMINISTIC;
     // Workspace rows: one per (g, k) of T*C elements for the tensor-core kernel

@@ -63,7 +63,10 @@ typedef enum { WG_BF16 = 0, WG_FP16 = 1, WG_FP32 = 2 } wg_dtype;
  *                 index order, then the range sums in range order; for S < 8:
  *                 index order) and casts (round to nearest even) to dW.
  *                 Bitwise reproducible for a given problem and split degree.
- *  AUTO:          DIRECT when the chosen split degree is 1, else DETERMINISTIC. */
+ *  AUTO:          DIRECT when the chosen split degree is 1; otherwise ATOMIC
+ *                 for an fp32 dW (measured the faster of the two on GB300)
+ *                 and DETERMINISTIC for a 16-bit dW.  Ask for DETERMINISTIC
+ *                 explicitly when bitwise reproducibility matters. */
 typedef enum {
     WG_MODE_AUTO = 0,
     WG_MODE_DIRECT = 1,

@@ -77,14 +77,16 @@ def _bits(t):
 @pytest.mark.parametrize("name", ["2d_dense_n32_h56_c64_k64", "2d_depthwise_g512_n64_h28", "2d_1x1_n32_h56_c64_k256",
                                   "2d_grouped_g32_c8_k8_n32_h28"])
 def test_host_entry_bitwise_equals_device_entry(name):
+    # Two-stage mode, so that both entry points give one bit pattern.
     sp = WORKLOADS[name][0]
-    ref, got = _run_both(sp, 401)
+    ref, got = _run_both(sp, 401, mode="deterministic")
     np.testing.assert_array_equal(_bits(got), _bits(ref))
 
 
 def test_host_entry_direct_and_split_modes():
     sp = spec(2, 1, 7, 64, 64, [112, 96], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16", "fp32")
-    for kw in ({"split_k": 0}, {"split_k": 1, "mode": "direct"}, {"split_k": 13, "mode": "deterministic"}):
+    for kw in ({"split_k": 0, "mode": "deterministic"}, {"split_k": 1, "mode": "direct"},
+               {"split_k": 13, "mode": "deterministic"}):
         ref, got = _run_both(sp, 411, **kw)
         np.testing.assert_array_equal(_bits(got), _bits(ref), err_msg=str(kw))
 

@@ -75,22 +75,28 @@ WORKLOAD_MODES = [
     ("2d_dense_n32_h56_c64_k64", 8, "direct", 0, 8),
     ("2d_grouped_g32_c8_k8_n32_h28", 0, "auto", 0, 0),
     ("2d_grouped_g32_c8_k8_n32_h28", 0, "atomic", 0, 0),
+    ("2d_grouped_g32_c8_k8_n32_h28", 0, "deterministic", 0, 0),
     ("2d_grouped_g32_c8_k8_n32_h28", 32, "deterministic", 0, 4),
     ("2d_grouped_g32_c8_k8_n32_h28", 16, "atomic", 0, 8),
     ("2d_depthwise_g512_n64_h28", 0, "auto", 0, 0),
-    ("2d_depthwise_g512_n64_h28", 0, "auto", 1, 0),
+    ("2d_depthwise_g512_n64_h28", 0, "deterministic", 0, 0),
+    ("2d_depthwise_g512_n64_h28", 0, "deterministic", 1, 0),
+    ("2d_depthwise_g512_n64_h28", 0, "deterministic", 2, 0),
+    ("2d_depthwise_g512_n64_h28", 0, "deterministic", 4, 0),
+    ("2d_depthwise_g512_n64_h28", 0, "deterministic", 8, 0),
     ("2d_depthwise_g512_n64_h28", 0, "auto", 2, 0),
-    ("2d_depthwise_g512_n64_h28", 0, "auto", 4, 0),
-    ("2d_depthwise_g512_n64_h28", 0, "auto", 8, 0),
     ("2d_depthwise_g512_n64_h28", 0, "atomic", 8, 0),
     ("2d_depthwise_g512_n64_h28", 1, "direct", 8, 0),
     ("3d_n4_d16_c128_k96_s2", 8, "atomic", 0, 0),
     ("3d_n4_d16_c128_k96_s2", 8, "deterministic", 0, 1),
     ("3d_n4_d16_c128_k96_s2", 16, "deterministic", 0, 2),
     ("3d_n4_d16_c128_k96_s2", 0, "auto", 0, 0),
+    ("3d_n4_d16_c128_k96_s2", 0, "deterministic", 0, 0),
     ("2d_1x1_n32_h56_c64_k256", 0, "auto", 0, 0),
     ("2d_1x1_n32_h56_c64_k256", 0, "atomic", 0, 0),
+    ("2d_1x1_n32_h56_c64_k256", 0, "deterministic", 0, 0),
     ("2d_1x1s2_n32_h56_c256_k128", 0, "auto", 0, 0),
+    ("2d_1x1s2_n32_h56_c256_k128", 0, "deterministic", 0, 0),
     ("2d_1x1s2_n32_h56_c256_k128", 1, "direct", 0, 0),
 ]
 

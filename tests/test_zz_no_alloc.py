@@ -44,14 +44,16 @@ CASES = [
     ("dense_56x56_auto", None, 0, "auto", 0),
     ("depthwise_3d_split3", spec(3, 8, 2, 1, 1, [5, 6, 5], [3, 3, 3], [1, 1, 1], [1, 1, 1], [1, 1, 1], [1, 1, 1]),
      3, "deterministic", 0),
-    ("depthwise_2d_auto", spec(2, 64, 3, 1, 1, [12, 10], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]), 0, "auto", 8),
-    # The automatic plan's partial sums need more than the 16 MiB array
+    ("depthwise_2d_auto_split", spec(2, 64, 3, 1, 1, [12, 10], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]), 0,
+     "deterministic", 8),
+    # The automatic split degree's partial sums need more than the 16 MiB array
     # (S = 8 partials of 2.25 MiB): the call caps the split degree to 7.
-    ("capped_auto_split", spec(2, 1, 8, 256, 256, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]), 0, "auto", 0),
+    ("capped_auto_split", spec(2, 1, 8, 256, 256, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]), 0,
+     "deterministic", 0),
     # One partial sum of dW is 9 MiB, so not even two fit: the call runs one
     # split (direct mode, no workspace).
     ("direct_when_two_partials_do_not_fit", spec(2, 1, 8, 512, 512, [14, 14], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
-     0, "auto", 0),
+     0, "deterministic", 0),
 ]
 
 SCRATCH_BYTES = 16 << 20

@@ -480,10 +480,8 @@ int plan_depthwise(Plan* pl, const wg_options& o, int num_sms, std::string* err)
     const Problem& pb = pl->pb;
     DwPlan& dw = pl->dw;
     std::memset(&dw, 0, sizeof dw);
-    // Channel vector: 2 channels by default.  On a sweep of 16 depthwise shapes
-    // (7x7 to 112x112, 32 to 1152 channels, strides 1 and 2) two-channel
-    // vectors, two CTAs per SM, were the fastest or within a few percent of the
-    // fastest width on every shape (1.2x over one channel on the largest).
+    // Channel vector of Gm channels (the caller's merge degree; make_plan picks
+    // the automatic one).
     dw.Gm = o.group_merge > 0 ? o.group_merge : 2;
     const int Wo = pb.out[2], Ho = pb.out[1];
     dw.xw = (Wo - 1) * pb.stride[2] + (pb.filt[2] - 1) * pb.dil[2] + 1;
@@ -653,18 +651,27 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
                     "the depthwise kernel needs C = K = 1, 1-D or 2-D, <= 9 taps and G %% 8 == 0");
     if (use_dw) {
         pl->kind = KIND_DEPTHWISE;
-        st = plan_depthwise(pl, o, num_sms, err);
-        // Automatic vector width: two channels, or four when the sliding 3x3
-        // window is used and every CTA walks many row tiles.  On a sweep of
-        // 16 depthwise shapes four-channel vectors won only there (G = 512,
-        // N = 64, 28x28: 27.9 against 29.6 us, 14 tiles per CTA); with 7 tiles
-        // per CTA or fewer two channels were as fast or faster.
-        if (st == WG_OK && o.group_merge == 0 && pl->dw.sliding && pl->per_split >= 10) {
-            wg_options o4 = o;
-            o4.group_merge = 4;
-            Plan p4;
-            std::memcpy(&p4, pl, sizeof p4);
-            if (plan_depthwise(&p4, o4, num_sms, nullptr) == WG_OK && p4.dw.sliding) std::memcpy(pl, &p4, sizeof p4);
+        // Automatic merge degree, after the PR #12359 page's policy (PR #12951:
+        // the largest admissible Gm at the kernel's tile): the widest channel
+        // vector this kernel admits at its design point of two CTAs per SM
+        // (eight-channel vectors hold 72 accumulators and run one CTA per SM)
+        // where the wider vector saves loads, else two channels.  With the
+        // register sliding window (3x3, stride and dilation 1 along W) each
+        // loaded X vector feeds 3*Gm multiply-adds and each dY vector 9*Gm, so
+        // four channels halve the load instructions per multiply-add against
+        // two; without it every tap reloads its X vector and a wider vector
+        // only cuts the threads per row tile (shorter, more ragged column
+        // segments).  Narrower vectors are tried when a tile does not fit.
+        if (o.group_merge == 0) {
+            const bool window = pb.filt[1] == 3 && pb.filt[2] == 3 && pb.stride[2] == 1 && pb.dil[2] == 1;
+            st = WG_ERR_NOT_SUPPORTED;
+            for (int g = window ? 4 : 2; g >= 1 && st != WG_OK; g /= 2) {
+                wg_options og = o;
+                og.group_merge = g;
+                st = plan_depthwise(pl, og, num_sms, g == 1 ? err : nullptr);
+            }
+        } else {
+            st = plan_depthwise(pl, o, num_sms, err);
         }
     } else {
         if (o.group_merge > 1)

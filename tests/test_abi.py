@@ -281,12 +281,19 @@ def test_planner_choices_on_default_caps():
     assert (dense["taps"], dense["S"], dense["mt_per_cta"], dense["box"]) == ("mn", "75", "1", "(w32,h8,d1,n1)")
     dense = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_dense_n32_h56_c64_k64"][0], kernel="igemm_taps_m"))
     assert (dense["S"], dense["mt_per_cta"], dense["box"]) == ("75", "3", "(w8,h7,d1,n4)")
-    # Depthwise vector width: four channels for the G = 512, N = 64 workload (14
-    # row tiles per CTA), two for a small problem.
+    # Depthwise vector width: four channels where the 3x3 sliding window applies
+    # (whatever the problem size: no threshold on the tile count), two for
+    # stride 2 along W, and the largest that fits when the caller asks for none.
     dwp = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_depthwise_g512_n64_h28"][0]))
     assert (dwp["kernel"], dwp["Gm"]) == ("depthwise", "4")
     small = _plan_fields(binding.wg_plan_string(spec(2, 64, 2, 1, 1, [9, 13], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])))
-    assert small["Gm"] == "2"
+    assert small["Gm"] == "4"
+    strided = _plan_fields(binding.wg_plan_string(spec(2, 64, 2, 1, 1, [9, 13], [3, 3], [2, 2], [1, 1], [1, 1],
+                                                       [1, 1])))
+    assert strided["Gm"] == "2"
+    for g in (1, 2, 4, 8):  # an explicit merge degree is kept
+        p = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_depthwise_g512_n64_h28"][0], 0, "auto", g))
+        assert p["Gm"] == str(g)
     # 8 groups of C = K = 8 folded into a 64-wide window: the column form too.
     grouped = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_grouped_g32_c8_k8_n32_h28"][0]))
     assert (grouped["taps"], grouped["Gm"], grouped["Nmma"], grouped["S"]) == ("mn", "8", "192", "38")

@@ -76,6 +76,16 @@ struct IgParams {
     int mode;       // 1 direct, 2 atomic, 3 workspace
     int out_dtype;  // wg_dtype
     int clq;        // CTAs per cluster along the split (1: no cluster reduction)
+    // Staged output (split modes): the CTA covers whole groups (every tap,
+    // channel and k of groups g0 .. g0 + Gm - 1, windows starting at their first
+    // channel), so its results form one contiguous block of dW, Gm*K*T*C
+    // elements, that the epilogue gathers in shared memory and adds or stores
+    // with 16-byte accesses.
+    int staged;
+    // Staged output: atom_of[(tap / (xs ? xs : 1)) * ncc + cc] is the index of
+    // the atom holding channel chunk cc of filter tap `tap` (x = 0 when the x
+    // taps sit on the columns).
+    unsigned char atom_of[256];
     void* out;
     WsLayout ws;    // split-K workspace layout (mode 3): rows (g, k) of L = T * C, S / clq partials
     unsigned char patch_ph[32][4];
@@ -502,7 +512,29 @@ __global__ void __launch_bounds__(kIgThreads, 1)
                         if (j < n) red[(m * Nt + cb + j) * 128 + row] = v[j];
                 }
         }
-        for (int m = 0; m < mtn && p.clq == 1; ++m) {
+        if (p.staged) {
+            // Dump the accumulators into the idle pipeline buffers column by
+            // column (dump[(m * Nmma + col) * 128 + row]: a warp's 32 rows of a
+            // column are 32 consecutive words); the valid (diagonal) elements
+            // are picked out in dW order after the barrier below.
+            float* dump = reinterpret_cast<float*>(smem);
+            for (int m = 0; m < mtn; ++m)
+                for (int cb = c_lo; cb < c_hi; cb += kEpiCols) {
+                    const int n = min(kEpiCols, c_hi - cb);
+                    float v[kEpiCols];
+                    if (have_acc) {
+                        tmem_ld_batch(trow + (uint32_t)(m * Nmma + cb), n, v);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < kEpiCols; ++j) v[j] = 0.f;
+                    }
+                    float* d = dump + (m * Nmma + cb) * 128 + row;
+#pragma unroll
+                    for (int j = 0; j < kEpiCols; ++j)
+                        if (j < n) d[j * 128] = v[j];
+                }
+        }
+        for (int m = 0; m < mtn && p.clq == 1 && !p.staged; ++m) {
             const int atom = atom0 + 2 * m + (row >> 6);
             bool vrow = atom < n_atoms;
             int tap = 0, cc = 0;
@@ -554,6 +586,46 @@ __global__ void __launch_bounds__(kIgThreads, 1)
                     epilogue_mtile<1, __half>(ta, nc, have_acc, vrow, nl, K, static_cast<__half*>(out), rowbase,
                                               kstride);
                 }
+            }
+        }
+    }
+    if (p.staged) {
+        // Write the CTA's dW block, Gm*K*T*C elements in dW order, four
+        // consecutive channels at a time: element (g0 + gl, k, tap, c) is row
+        // (atom % 2) * 64 + cw % 64 of M-tile atom / 2, cw = gl * C + c, and
+        // column (x-block) * 64 + gl * K + k (gl * K + k without x-blocks) of the
+        // dump.  Vector fp32 atomic adds (atomic) or stores into the split's
+        // workspace rows (deterministic; a row of T*C elements, a multiple of 4,
+        // never splits a vector across slices).
+        named_bar_sync(3, kIgThreads);
+        const float* dump = reinterpret_cast<const float*>(smem);
+        const int C = p.C, K = p.K, T = p.T, TC = T * C, C4 = C >> 2, xs = p.xs, X = xs ? xs : 1;
+        const int nv4 = p.Gm * K * TC / 4;
+        const long long e0 = (long long)g0 * K * TC;
+        for (int i = threadIdx.x; i < nv4; i += kIgThreads) {
+            int rest = i / C4;
+            const int c = (i - rest * C4) * 4;
+            const int tap = rest % T;
+            rest /= T;
+            const int k = rest % K, gl = rest / K;
+            const int x = tap % X;
+            const int cw = gl * C + c, cc = cw >> 6;
+            const int a = p.atom_of[(tap / X) * p.ncc + cc];
+            const int rowi = (a & 1) * 64 + (cw & 63);
+            const int col = (xs ? (xs - 1 - x) * 64 : 0) + gl * K + k;
+            const float4 v = *reinterpret_cast<const float4*>(dump + ((a >> 1) * p.Nmma + col) * 128 + rowi);
+            const long long e = e0 + 4LL * i;
+            if (p.mode == 2) {
+                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(static_cast<float*>(p.out) + e),
+                             "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                             : "memory");
+            } else {
+                const long long r = (long long)(g0 + gl) * K + k;
+                const int xe = tap * C + c;
+                const int j = xe / p.ws.W;
+                float* o = static_cast<float*>(p.out) +
+                           ((r * p.ws.nj + j) * p.ws.S + split) * (long long)p.ws.W + (xe - j * p.ws.W);
+                *reinterpret_cast<float4*>(o) = v;
             }
         }
     }

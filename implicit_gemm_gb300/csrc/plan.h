@@ -83,6 +83,7 @@ struct IgemmPlan {
     long long est_cycles;  // planner's cost estimate (for the plan string)
     long long tile_clk;    // planner's estimate of one K-tile on one CTA, in SM cycles
     int cluster;           // CTAs per thread-block cluster along the split (1: none)
+    int staged;            // 1: each CTA's results are one contiguous dW block, written from shared memory
 };
 
 // CUDA-core depthwise kernel (cpg = kpg = 1).

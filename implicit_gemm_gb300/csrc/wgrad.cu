@@ -295,6 +295,17 @@ int prepare_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, v
     prm.idesc = wg::make_idesc_f16(pb.in_dtype == WG_BF16, true, true, 128, ig.Nmma);
     prm.mode = pl.mode, prm.out_dtype = pb.out_dtype;
     prm.clq = ig.cluster;
+    prm.staged = ig.staged;
+    if (ig.staged) {
+        // Inverse atom table: (tap / X, chunk) -> atom index (x = 0 taps when
+        // the x taps sit on the columns; every atom when they do not).
+        const int xe = ig.xs ? ig.xs : 1;
+        for (int i = 0; i < ig.n_atoms; ++i) {
+            const int tap = ig.halo ? ig.atom_tap[i] : i / ig.n_cchunks;
+            const int cc = ig.halo ? ig.atom_cc[i] : i % ig.n_cchunks;
+            prm.atom_of[(tap / xe) * ig.n_cchunks + cc] = (unsigned char)i;
+        }
+    }
     prm.out = pl.mode == wg::MODE_DETERMINISTIC ? ws : dw;
     prm.ws = ws_layout(pl);
     // K-step descriptor parts: pixel row r of the tile (w fastest) sits at patch

@@ -298,3 +298,32 @@ def test_depthwise_workload_on_tensor_cores(split_k, mode):
     sp, x, dy, (dw, A) = workload("2d_depthwise_g512_n64_h28")
     got = run_gpu(sp, x, dy, split_k, mode, kernel="igemm")
     assert_close(got, dw, A, sp["out_dtype"], f"depthwise igemm S={split_k} {mode}")
+
+
+# Folded groups whose CTAs cover whole groups write their split's dW block from
+# shared memory in dW order (plan "out=staged"): 16 groups of 4 channels per
+# 64-channel window, both tile forms, atomic and two-stage modes, 16-bit dW
+# through the two-stage path.
+STAGED_SP = spec(2, 64, 8, 4, 4, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])
+
+
+def test_staged_output_folded_groups():
+    sp = STAGED_SP
+    xi, dyi = make_inputs(sp, ("int", -2, 2), 71, 72)
+    dwi, _ = ref(sp, xi, dyi)
+    x, dy = make_inputs(sp, ("uniform", -1.0, 1.0), 73, 74)
+    dw, A = ref(sp, x, dy)
+    seen = 0
+    for kernel in ("auto", "igemm_taps_m", "igemm_taps_mn"):
+        for split_k, mode in ((0, "auto"), (0, "deterministic"), (0, "atomic")):
+            plan = binding.wg_plan_string(sp, split_k, mode, 0, kernel=kernel)
+            seen += "out=staged" in plan
+            got = run_gpu(sp, xi, dyi, split_k, mode, kernel=kernel)
+            np.testing.assert_array_equal(got, dwi, err_msg=f"{kernel} {mode}: {plan}")
+            got = run_gpu(sp, x, dy, split_k, mode, kernel=kernel)
+            assert_close(got, dw, A, sp["out_dtype"], f"{kernel} {mode}")
+        for odt in ("bf16", "fp16"):
+            s16 = dict(sp, out_dtype=odt)
+            got = run_gpu(s16, x, dy, 0, "deterministic", kernel=kernel)
+            assert_close(got, dw, A, odt, f"{kernel} deterministic {odt}")
+    assert seen >= 5, "the staged output was not exercised"

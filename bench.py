@@ -294,14 +294,24 @@ def cpu_baseline(name):
 
 
 L2_BYTES = 129 * 1000 * 1000
-# DRAM bytes (read + write) of one launch of the workload's main kernel from an
-# ncu capture of the kernel as it now stands (summaries under profiles/); a
-# workload without such a capture reports null.
+# DRAM bytes (read + write) of one launch of the main kernel of a plan (a
+# VARIANTS label, or a workload name for its default plan) from an ncu capture
+# of the kernel as it now stands (summaries under profiles/); a plan without
+# such a capture reports null.  ncu flushes the caches before the captured
+# launch, so atomic plans also count the dW lines their atomic adds fetch.
 TRAFFIC = {
-    # igemm_wgrad_kernel, plan taps=mn S = 75, one M-tile per CTA: 25,778,688 B read + 0 B written.
-    "2d_dense_n32_h56_c64_k64": 25_778_688,
-    # depthwise_wgrad_kernel<bf16, 4, sliding>: 103,047,168 B read + 3,496,960 B written.
-    "2d_depthwise_g512_n64_h28": 106_544_128,
+    # igemm_wgrad_kernel, taps=mn S = 75 two-stage: 25,781,504 B read + 0 B written.
+    "2d_dense_n32_h56_c64_k64": 25_781_504,
+    # igemm_wgrad_kernel, Gm = 8 fold, staged atomic output: 25,854,208 B read + 0 B written.
+    "2d_grouped_g32_c8_k8_n32_h28": 25_854_208,
+    # depthwise_wgrad_kernel<bf16, 4, sliding>, atomic: 103,107,840 B read + 3,512,320 B written.
+    "2d_depthwise_g512_n64_h28": 106_620_160,
+    # igemm_wgrad_kernel, per-tap S = 4 atomic: 6,010,368 B read (X + dY + the dW lines) + 0 B written.
+    "3d_n4_d16_c128_k96_s2/auto": 6_010_368,
+    # igemm_wgrad_kernel, S = 87 atomic: 64,385,280 B read + 357,376 B written.
+    "2d_1x1_n32_h56_c64_k256": 64_742_656,
+    # igemm_wgrad_kernel, per-tap S = 49 atomic: 19,493,888 B read + 0 B written.
+    "2d_1x1s2_n32_h56_c256_k128": 19_493_888,
 }
 MAX_COPIES = 512
 
@@ -539,6 +549,35 @@ def run_sweep(torch, stream, flush, steps, warmup):
           flush=True)
 
 
+def run_floor(torch, flush, reps=20):
+    """Cold-read floors, measured as the peaks in MEASURED_PEAKS.json are (torch ops,
+    CUDA events) but with L2 flushed before each rep: for each workload's
+    algorithmic bytes B, a copy of B/2 bytes (B of traffic) and a read-only
+    reduction over B bytes; best and median of `reps` event-timed reps."""
+    def timed(fn):
+        ts = []
+        for _ in range(reps + 3):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(); fn(); b.record(); torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        ts = ts[3:]
+        return min(ts), statistics.median(ts)
+    pk = peaks()
+    for name in ("2d_dense_n32_h56_c64_k64", "2d_depthwise_g512_n64_h28", "3d_n4_d16_c128_k96_s2"):
+        nbytes = int(sizes(WORKLOADS[name][0])["bytes"]) // 16 * 16
+        a = torch.ones(nbytes // 4, dtype=torch.bfloat16, device="cuda")
+        b = torch.empty_like(a)
+        r = torch.ones(nbytes // 8, dtype=torch.int64, device="cuda")
+        cp, cpm = timed(lambda: b.copy_(a))
+        rd, rdm = timed(lambda: torch.sum(r))
+        print(json.dumps({"floor": name, "bytes": nbytes, "copy_best_us": cp, "copy_median_us": cpm,
+                          "read_best_us": rd, "read_median_us": rdm,
+                          "copy_frac_of_peak": nbytes / (cp * 1e-6) / 1e9 / pk["hbm"],
+                          "read_frac_of_peak": nbytes / (rd * 1e-6) / 1e9 / pk["hbm"]}), flush=True)
+        del a, b, r
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -552,6 +591,8 @@ def main():
     ap.add_argument("--graph", action="store_true", help="replay a CUDA graph of the call instead of calling it")
     ap.add_argument("--dgrad", action="store_true",
                     help="time backward-data on the workload's geometry instead of the weight gradient (no extras)")
+    ap.add_argument("--floor", action="store_true",
+                    help="time torch's copy and a read-only reduction of each workload's algorithmic bytes (cold L2)")
     ap.add_argument("--sweep", action="store_true",
                     help="time the automatic plan against fixed merge widths on a depthwise shape sweep")
     args = ap.parse_args()
@@ -576,6 +617,10 @@ def main():
     stream = torch.cuda.Stream()
     flush = L2Flush(torch)
     pk = peaks()
+    if args.floor:
+        if rank == 0:
+            run_floor(torch, flush)
+        return
     if args.sweep:
         if rank == 0:
             run_sweep(torch, stream, flush, min(args.steps, 200), args.warmup)
@@ -635,7 +680,7 @@ def main():
                 "unit": "TFLOP/s"}
         roof["step_frac"] = s["flops"] / (step_ms * 1e-3) / 1e12 / pk["bf16"]
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = TRAFFIC.get(args.workload)
+    roof["traffic"] = TRAFFIC.get(args.variant or args.workload)
     roof["peak_source"] = pk["src"]
     roof["kernel"] = "igemm_wgrad_kernel" if "igemm" in wl.plan else "depthwise_wgrad_kernel"
     roof["kernel_ms"] = kern_ms
@@ -660,7 +705,7 @@ def main():
                            "gbs": s2["bytes"] / (ms * 1e-3) / 1e9, "roofline_us": max(tf, tb) * 1e6,
                            "bound": "hbm" if tb >= tf else "tensor",
                            "roofline_frac": max(tf, tb) / (ms * 1e-3), "kernel_ms": kms,
-                           "kernel_roofline_frac": max(tf, tb) / (kms * 1e-3), "traffic": TRAFFIC.get(name),
+                           "kernel_roofline_frac": max(tf, tb) / (kms * 1e-3), "traffic": TRAFFIC.get(label),
                            "l2": w2.l2_note(), "plan": w2.plan}
             del w2
         # Backward-data (dgrad) on the dense and 1x1 geometries.

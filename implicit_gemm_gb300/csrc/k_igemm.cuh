@@ -774,6 +774,53 @@ __global__ void __launch_bounds__(kRedThreads)
     slices_reduce_store(sm, sm + (size_t)spc * w.S * w.W, w, sl0, nsl, dw, out_dtype);
 }
 
+// Register path: one CTA per workspace slice (W <= 128 elements), warp g adds
+// split range g (the ranges of red_groups) of the slice's float4 columns, lane =
+// column, with every load of its range issued before the first add (the loads
+// come from L2, where the split-K kernel has just written them, so one round
+// trip covers them all); then each element's range sums are added in range
+// order.  The same order as the bulk path, bit for bit.
+constexpr int kRegMaxRange = 32;  // splits one lane holds at once (larger ranges loop)
+__global__ void __launch_bounds__(128)
+    reduce_splits_regs_kernel(const float* __restrict__ ws, void* __restrict__ dw, const WsLayout w, int out_dtype)
+{
+    __shared__ float4 part[kRedGroups][32];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int S = w.S, W = w.W, W4 = W >> 2, G = red_groups(S);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long sl = blockIdx.x;
+    if (warp < G && lane < W4) {
+        const int s0 = G == 1 ? 0 : (S * warp) >> 2, s1 = G == 1 ? S : (S * (warp + 1)) >> 2;
+        const float4* q = reinterpret_cast<const float4*>(ws + (sl * S + s0) * (long long)W) + lane;
+        float4 a = __ldcg(q);
+        int s = s0 + 1;
+        q += W4;
+        while (s < s1) {
+            const int n = min(kRegMaxRange, s1 - s);
+            float4 v[kRegMaxRange];
+#pragma unroll
+            for (int j = 0; j < kRegMaxRange; ++j)
+                if (j < n) v[j] = __ldcg(q + j * W4);
+#pragma unroll
+            for (int j = 0; j < kRegMaxRange; ++j)
+                if (j < n) a.x += v[j].x, a.y += v[j].y, a.z += v[j].z, a.w += v[j].w;
+            s += n;
+            q += n * W4;
+        }
+        part[warp][lane] = a;
+    }
+    __syncthreads();
+    const int i = threadIdx.x;
+    if (i >= W) return;
+    const int r = (int)(sl / w.nj);
+    const int x0 = (int)(sl - (long long)r * w.nj) * W;
+    if (x0 + i >= w.L) return;
+    const float* p0 = reinterpret_cast<const float*>(&part[0][0]);
+    float a = p0[i];
+    for (int g = 1; g < G; ++g) a += p0[g * 128 + i];
+    store_cast(dw, (long long)r * w.L + x0 + i, a, out_dtype);
+}
+
 // Fallback for split counts whose slice block does not fit shared memory: one
 // thread per element, same layout and summation order.
 __global__ void __launch_bounds__(kRedThreads)

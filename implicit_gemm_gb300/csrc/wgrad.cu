@@ -351,6 +351,30 @@ int prepare_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, v
     return WG_OK;
 }
 
+// Resident CTAs per SM of the register-path reduction kernel (occupancy
+// calculator, once per device).
+int reduce_regs_ctas_per_sm()
+{
+    static std::mutex mu;
+    static std::map<int, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, wg::reduce_splits_regs_kernel, 128, 0) != cudaSuccess ||
+        n <= 0) {
+        cudaGetLastError();
+        n = 1;
+    }
+    cache.emplace(dev, n);
+    return n;
+}
+
 // Stage 2 of deterministic split-K, launched as a programmatic dependent of the
 // split-K kernel just before it on the stream.
 int launch_reduce(const wg::Plan& pl, void* ws, void* dw, cudaStream_t stream)
@@ -379,7 +403,17 @@ int launch_reduce(const wg::Plan& pl, void* ws, void* dw, cudaStream_t stream)
     cfg.blockDim = dim3(wg::kRedThreads);
     cudaError_t e;
     const float* wsf = static_cast<const float*>(ws);
-    if (smem <= wg::kMaxSmemPerCta && n_slices < (1LL << 31) && w.W <= 128) {
+    // Register path when every slice gets its own resident CTA (one wave): all
+    // loads of a split range are then in flight at once.  Otherwise the bulk
+    // path, which packs several slices per CTA.  Measured: 56x56 two-stage
+    // S = 75 (384 slices) 19.5 -> 18.5 us per call, grouped two-stage (256
+    // slices) 19.8 -> 18.9 us; 3-D S = 8 (2,592 slices, about six waves of the
+    // register kernel) 19.5 us with the bulk path against 22.6 us.
+    if (n_slices < (1LL << 31) && w.W <= 128 && n_slices <= (long long)num_sms() * reduce_regs_ctas_per_sm()) {
+        cfg.gridDim = dim3((unsigned)n_slices);
+        cfg.blockDim = dim3(128);
+        e = cudaLaunchKernelEx(&cfg, wg::reduce_splits_regs_kernel, wsf, dw, w, pb.out_dtype);
+    } else if (smem <= wg::kMaxSmemPerCta && n_slices < (1LL << 31) && w.W <= 128) {
         const int st = ensure_smem(wg::reduce_splits_bulk_kernel, (int)smem);
         if (st) return st;
         cfg.gridDim = dim3((unsigned)((n_slices + spc - 1) / spc));

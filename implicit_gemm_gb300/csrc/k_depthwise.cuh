@@ -154,8 +154,9 @@ __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
     const int ntl = max(0, min(p.per_split, p.total_tiles - t0));
     const int n_cwarps = nthreads >> 5;
 
-    // A split-reduction kernel launched after this one may take each SM as soon
-    // as this grid's CTA there exits (it waits for the whole grid's results).
+    // The kernel launched after this one (the split reduction, or the next
+    // call's first kernel) may be scheduled at once; it waits for this whole
+    // grid's results before it reads them.
     pdl_launch_dependents();
     // Row tile i of this split into ring stage i % stages: X rows with halo, dY rows.
     auto issue_tile = [&](int i) {
@@ -182,6 +183,10 @@ __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
             mbar_init(&empty[i], (uint32_t)n_cwarps);
         }
         fence_mbar_init();
+        // A programmatic dependent of the kernel before it on the stream: unless
+        // that is this call's zeroing kernel (which waited for everything before
+        // it), X and dY are read only after it has finished.
+        if (p.mode != 2) pdl_wait();
         for (int i = 0; i < pre; ++i) issue_tile(i);
     }
     __syncthreads();
@@ -326,8 +331,10 @@ __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
     // order.  dW index o = g * T + t; its workspace offset uses 32-bit
     // arithmetic (the depthwise workspace is one row of G * T < 2^31 elements).
     const int TC = p.T * p.CB, W = p.ws.W;
-    // Atomic accumulation: wait for the kernel that zeroes dW (see zero_f32_kernel).
-    if (p.mode == 2) pdl_wait();
+    // Atomic accumulation: wait for the kernel that zeroes dW (see
+    // zero_f32_kernel); in the other modes this returns at once.  Every thread
+    // passes it before its first global write.
+    pdl_wait();
     for (int idx = tid; idx < TC; idx += blockDim.x) {
         const int c = idx / p.T, t = idx - c * p.T;
         float s = 0.f;

@@ -325,8 +325,9 @@ __global__ void __launch_bounds__(kIgThreads, 1)
     const int c_al = (g0 * p.C) & ~7;
     const int k_base = ((g0 * p.K) & ~7) + nt * p.Nt;
 
-    // A split-reduction kernel launched after this one may take each SM as soon
-    // as this grid's CTA there exits (it waits for the whole grid's results).
+    // The kernel launched after this one (the split reduction, or the next
+    // call's first kernel) may be scheduled at once; it waits for this whole
+    // grid's results before it reads them.
     pdl_launch_dependents();
     // Stage i of the TMA ring: the K-tile's X patches (or per-tap boxes) and dY.
     const uint32_t tx = (uint32_t)(p.n_patches * p.patch_tx + p.dy_tx);
@@ -370,6 +371,13 @@ __global__ void __launch_bounds__(kIgThreads, 1)
     // tensor maps' first fetch by the TMA unit (~1 us) then overlaps the
     // prologue instead of following it.  (Issuing every ring stage here held
     // the other warps at the barrier for longer than the data took to land.)
+    // This kernel is a programmatic dependent of the kernel before it on the
+    // stream.  Unless that kernel is this call's zeroing kernel (which itself
+    // waited for everything before it), X and dY are read only after
+    // griddepcontrol.wait, and so is TMEM taken (a kernel before it could still
+    // be about to allocate); the tensor-map prefetch and the barrier set-up run
+    // before, overlapping the previous kernel's tail.
+    const bool wait_first = p.mode != 2;
     int pre = 0;
     if (threadIdx.x == 0) {
         if (nk > 0) {
@@ -382,10 +390,12 @@ __global__ void __launch_bounds__(kIgThreads, 1)
         }
         mbar_init(accb, 1);
         fence_mbar_init();
+        if (wait_first) pdl_wait();
         pre = min(1, nk);
         for (int i = 0; i < pre; ++i) issue_stage(i);
     }
     if (warp == 1) {
+        if (wait_first) pdl_wait();
         tmem_alloc(tslot, (uint32_t)p.tmem_cols);
         tmem_relinquish();
         tc_fence_before();
@@ -471,8 +481,10 @@ __global__ void __launch_bounds__(kIgThreads, 1)
     named_bar_sync(2, kIgThreads);  // the producer is done and may read tbase
     // Atomic accumulation: dW was zeroed by a kernel launched just before this
     // one (programmatic dependent launch); wait for it only here, so that its
-    // launch and run overlap the main loop.
-    if (p.mode == 2) pdl_wait();
+    // launch and run overlap the main loop.  In the other modes the previous
+    // kernel finished before the first stage was loaded and this returns at
+    // once; every thread passes it before its first global write.
+    pdl_wait();
     tc_fence_after();
     tbase = *tslot;
     {
@@ -648,6 +660,10 @@ __global__ void __launch_bounds__(kIgThreads, 1)
 // for this grid (griddepcontrol.wait) only before their first atomic add.
 __global__ void __launch_bounds__(256) zero_f32_kernel(float* __restrict__ p, long long n)
 {
+    // It is itself a programmatic dependent of the kernel before it on the
+    // stream: it waits for that kernel before letting the main kernel launch,
+    // so the main kernel may read X and dY without waiting.
+    pdl_wait();
     pdl_launch_dependents();
     const long long n4 = n >> 2;
     const long long stride = (long long)gridDim.x * blockDim.x;
@@ -748,6 +764,7 @@ __global__ void __launch_bounds__(kRedThreads)
     extern __shared__ uint8_t red_raw[];
     float* sm = align_shared<float>(red_raw, 128);
     __shared__ uint64_t bar;
+    pdl_launch_dependents();  // the next call's first kernel waits for this grid before it reads
     const long long sl0 = (long long)blockIdx.x * spc;
     const int nsl = (int)min((long long)spc, n_slices - sl0);
     const uint32_t total = (uint32_t)nsl * (uint32_t)w.S * (uint32_t)w.W * 4u;
@@ -785,6 +802,7 @@ __global__ void __launch_bounds__(128)
     reduce_splits_regs_kernel(const float* __restrict__ ws, void* __restrict__ dw, const WsLayout w, int out_dtype)
 {
     __shared__ float4 part[kRedGroups][32];
+    pdl_launch_dependents();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int S = w.S, W = w.W, W4 = W >> 2, G = red_groups(S);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -827,6 +845,7 @@ __global__ void __launch_bounds__(kRedThreads)
     reduce_splits_kernel(const float* __restrict__ ws, void* __restrict__ dw, long long E, const WsLayout w,
                          int out_dtype)
 {
+    pdl_launch_dependents();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long i = (long long)blockIdx.x * kRedThreads + threadIdx.x;
     if (i >= E) return;

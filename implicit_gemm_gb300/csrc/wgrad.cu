@@ -375,6 +375,17 @@ int reduce_regs_ctas_per_sm()
     return n;
 }
 
+// Programmatic stream serialization for a launch (see launch_pre).
+void pdl_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, unsigned* na, cudaStream_t stream)
+{
+    attr[*na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[*na].val.programmaticStreamSerializationAllowed = 1;
+    ++*na;
+    cfg->attrs = attr;
+    cfg->numAttrs = *na;
+    cfg->stream = stream;
+}
+
 // Stage 2 of deterministic split-K, launched as a programmatic dependent of the
 // split-K kernel just before it on the stream.
 int launch_reduce(const wg::Plan& pl, void* ws, void* dw, cudaStream_t stream)
@@ -395,11 +406,8 @@ int launch_reduce(const wg::Plan& pl, void* ws, void* dw, cudaStream_t stream)
     const long long smem = smem_for(spc);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cfg.stream = stream;
+    unsigned na = 0;
+    pdl_config(&cfg, attr, &na, stream);
     cfg.blockDim = dim3(wg::kRedThreads);
     cudaError_t e;
     const float* wsf = static_cast<const float*>(ws);
@@ -433,13 +441,26 @@ int launch_reduce(const wg::Plan& pl, void* ws, void* dw, cudaStream_t stream)
 // kernel is launched as its programmatic dependent and waits for it only
 // before its atomic adds (a memset before the main kernel measured ~4 us per
 // call on GB300, a dependent zeroing kernel is hidden behind the main loop).
+//
+// Every kernel of a call is launched with programmatic stream serialization,
+// the first one too: it may be scheduled while the kernel before it on the
+// stream (the previous call's last kernel, or the caller's) is still running,
+// and waits for it (griddepcontrol.wait) before it touches memory that kernel
+// may write; its launch and set-up (barriers, tensor-map prefetch) overlap
+// that kernel's tail.  A kernel before it that was not launched this way, or
+// a copy or event between them, gives ordinary stream order.
 int launch_pre(const wg::Plan& pl, void* dw, cudaStream_t stream)
 {
     if (pl.mode == wg::MODE_ATOMIC) {
         const long long n = pl.pb.dw_elems;
         const long long blocks = std::max(1LL, std::min<long long>((n / 4 + 255) / 256, 4LL * num_sms()));
-        wg::zero_f32_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<float*>(dw), n);
-        const cudaError_t e = cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        unsigned na = 0;
+        pdl_config(&cfg, attr, &na, stream);
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(256);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, wg::zero_f32_kernel, static_cast<float*>(dw), n);
         if (e != cudaSuccess) return cuda_fail("zero_f32_kernel launch", e);
     }
     return WG_OK;
@@ -450,39 +471,24 @@ int launch_igemm_main(const wg::Plan& pl, const Prepared& pr, cudaStream_t strea
     const wg::IgemmPlan& ig = pl.ig;
     const int st = ensure_smem(wg::igemm_wgrad_kernel, ig.smem_bytes);
     if (st) return st;
-    const dim3 grid(pl.grid[0], pl.grid[1], pl.grid[2]);
-    cudaError_t e;
-    const bool after_zero = pl.mode == wg::MODE_ATOMIC;
-    if (ig.cluster > 1 || after_zero) {
-        // Consecutive splits form a cluster (grid z is a multiple of the cluster
-        // size); in atomic mode the kernel is a programmatic dependent of the
-        // zeroing kernel.
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[2];
-        unsigned na = 0;
-        if (ig.cluster > 1) {
-            attr[na].id = cudaLaunchAttributeClusterDimension;
-            attr[na].val.clusterDim.x = 1;
-            attr[na].val.clusterDim.y = 1;
-            attr[na].val.clusterDim.z = (unsigned)ig.cluster;
-            ++na;
-        }
-        if (after_zero) {
-            attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr[na].val.programmaticStreamSerializationAllowed = 1;
-            ++na;
-        }
-        cfg.attrs = attr;
-        cfg.numAttrs = na;
-        cfg.gridDim = grid;
-        cfg.blockDim = dim3(pl.block);
-        cfg.dynamicSmemBytes = (size_t)ig.smem_bytes;
-        cfg.stream = stream;
-        e = cudaLaunchKernelEx(&cfg, wg::igemm_wgrad_kernel, pr.tmx, pr.tmy, pr.ig);
-    } else {
-        wg::igemm_wgrad_kernel<<<grid, pl.block, ig.smem_bytes, stream>>>(pr.tmx, pr.tmy, pr.ig);
-        e = cudaGetLastError();
+    // Consecutive splits form a cluster (grid z is a multiple of the cluster
+    // size); the kernel is a programmatic dependent of the kernel before it
+    // (the zeroing kernel in atomic mode).
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
+    if (ig.cluster > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = (unsigned)ig.cluster;
+        ++na;
     }
+    pdl_config(&cfg, attr, &na, stream);
+    cfg.gridDim = dim3(pl.grid[0], pl.grid[1], pl.grid[2]);
+    cfg.blockDim = dim3(pl.block);
+    cfg.dynamicSmemBytes = (size_t)ig.smem_bytes;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, wg::igemm_wgrad_kernel, pr.tmx, pr.tmy, pr.ig);
     if (e != cudaSuccess) return cuda_fail("igemm_wgrad_kernel launch", e);
     return WG_OK;
 }
@@ -504,24 +510,16 @@ int launch_dw_t(const wg::Plan& pl, dim3 grid, const CUtensorMap& tmx, const CUt
     auto k = wg::depthwise_wgrad_kernel<BF16, GM, SLIDE>;
     const int st = ensure_smem(k, pl.dw.smem_bytes);
     if (st) return st;
-    cudaError_t e;
-    if (pl.mode == wg::MODE_ATOMIC) {
-        // A programmatic dependent of the kernel that zeroes dW.
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        cfg.gridDim = grid;
-        cfg.blockDim = dim3(pl.block);
-        cfg.dynamicSmemBytes = (size_t)pl.dw.smem_bytes;
-        cfg.stream = stream;
-        e = cudaLaunchKernelEx(&cfg, k, tmx, tmy, prm);
-    } else {
-        k<<<grid, pl.block, pl.dw.smem_bytes, stream>>>(tmx, tmy, prm);
-        e = cudaGetLastError();
-    }
+    // A programmatic dependent of the kernel before it (the kernel that zeroes
+    // dW in atomic mode).
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    unsigned na = 0;
+    pdl_config(&cfg, attr, &na, stream);
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(pl.block);
+    cfg.dynamicSmemBytes = (size_t)pl.dw.smem_bytes;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k, tmx, tmy, prm);
     if (e != cudaSuccess) return cuda_fail("depthwise_wgrad_kernel launch", e);
     return WG_OK;
 }

@@ -118,6 +118,11 @@ __global__ void __launch_bounds__(256)
     dgrad_fold_w_kernel(const uint16_t* __restrict__ w, uint16_t* __restrict__ we, int G, int K, int C, int T, int Gm,
                         long long n)
 {
+    // A programmatic dependent of the kernel before it (which may still read
+    // the previous contents of `we`); the backward-data kernel launched after
+    // it waits for this grid before it reads `we`.
+    pdl_wait();
+    pdl_launch_dependents();
     const int Km = Gm * K, Cm = Gm * C;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
         long long r = i;
@@ -205,10 +210,15 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     const int stages = p.stages, stage_bytes = p.stage_bytes, patch_bytes = p.patch_bytes;
     const int n_catoms = p.n_catoms, X = p.X, TG = p.TG, Nt = p.Nt;
 
+    // The next kernel on the stream may be scheduled at once (it waits for this
+    // grid before it reads what this grid writes).
+    pdl_launch_dependents();
     // Thread 0 (the TMA producer) prefetches the tensor maps, initialises the
     // barriers and issues the resident W tiles before the block barrier, and
     // warp 1 allocates TMEM meanwhile: the TMA unit's first fetch of the
-    // tensor maps then overlaps the prologue.
+    // tensor maps then overlaps the prologue.  This kernel is a programmatic
+    // dependent of the kernel before it: dY and W are read, and TMEM taken,
+    // only after griddepcontrol.wait.
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmy);
         tma_prefetch_desc(&tmw);
@@ -222,6 +232,7 @@ __global__ void __launch_bounds__(kDgThreads, 1)
         }
         mbar_init(wbar, 1);
         fence_mbar_init();
+        pdl_wait();
         if (wr) {
             // Every (K chunk, tap, channel atom) tile of the one (channel tile, group).
             mbar_arrive_expect_tx(wbar, (uint32_t)p.w_bytes);
@@ -233,6 +244,7 @@ __global__ void __launch_bounds__(kDgThreads, 1)
         }
     }
     if (warp == 1) {
+        pdl_wait();
         tmem_alloc(tslot, (uint32_t)p.tmem_cols);
         tmem_relinquish();
         tc_fence_before();
@@ -349,6 +361,7 @@ __global__ void __launch_bounds__(kDgThreads, 1)
         // pixels i / 4, 8 + i / 4, 16 + i / 4 and 24 + i / 4, so that a store
         // instruction covers eight 64-byte runs.  Tiles of zeros skip TMEM and
         // staging and store zeros in the same pattern.
+        pdl_wait();  // returns at once: the previous kernel finished before the first load
         const int q = warp & 3;
         const uint32_t trow = tbase + ((uint32_t)(q * 32) << 16);
         const uint32_t sw = smem_u32(staging) + (uint32_t)(q * 32 * kDgStageRow);

@@ -1008,14 +1008,29 @@ int wg_conv_bwd_data(const wg_problem* p, const void* dy, const void* w, void* d
         const wg::Problem& pb = d.pb;
         const long long n = (long long)d.Gb * d.Km * pb.T * d.Cm;
         const unsigned blocks = (unsigned)std::min<long long>((n + 255) / 256, 4096);
-        wg::dgrad_fold_w_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(w), static_cast<uint16_t*>(wexp),
-                                                       pb.G, pb.K, pb.C, (int)pb.T, d.Gm, n);
-        e = cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        unsigned na = 0;
+        pdl_config(&cfg, attr, &na, s);
+        cfg.gridDim = dim3(blocks);
+        cfg.blockDim = dim3(256);
+        e = cudaLaunchKernelEx(&cfg, wg::dgrad_fold_w_kernel, static_cast<const uint16_t*>(w),
+                               static_cast<uint16_t*>(wexp), pb.G, pb.K, pb.C, (int)pb.T, d.Gm, n);
         if (e != cudaSuccess) return cuda_fail("dgrad_fold_w_kernel launch", e);
     }
-    wg::dgrad_kernel<<<dim3(d.grid[0], d.grid[1], d.grid[2]), d.block, d.smem_bytes, s>>>(pr.tmy, pr.tmw, pr.prm);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail("dgrad_kernel launch", e);
+    {
+        // Like the weight-gradient kernels, a programmatic dependent of the
+        // kernel before it (see launch_pre).
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        unsigned na = 0;
+        pdl_config(&cfg, attr, &na, s);
+        cfg.gridDim = dim3(d.grid[0], d.grid[1], d.grid[2]);
+        cfg.blockDim = dim3(d.block);
+        cfg.dynamicSmemBytes = (size_t)d.smem_bytes;
+        e = cudaLaunchKernelEx(&cfg, wg::dgrad_kernel, pr.tmy, pr.tmw, pr.prm);
+        if (e != cudaSuccess) return cuda_fail("dgrad_kernel launch", e);
+    }
     if (g_mark && (e = cudaEventRecord(g_mark, s)) != cudaSuccess) return cuda_fail("cudaEventRecord(mark)", e);
     return WG_OK;
 }

@@ -4,7 +4,8 @@ once, and from several host threads.
 * Graphs: a deterministic weight-gradient call (split-K kernel plus the
   reduction kernel it launches with programmatic dependent launch), an atomic
   one (the kernel that zeroes dW, then the split-K kernel launched as its
-  programmatic dependent), a backward-data call and a host-buffer call are captured
+  programmatic dependent), an atomic depthwise one, a backward-data call and a
+  host-buffer call are captured
   once and replayed with new input values copied into the same buffers; each
   replay must give the bits of an eager call on those values.
 * Streams: four different problems launched on four streams without
@@ -75,9 +76,14 @@ class Call:
 DENSE = spec(2, 1, 8, 64, 64, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16", "bf16")
 
 
-@pytest.mark.parametrize("split_k,mode", [(0, "auto"), (24, "atomic")])
-def test_graph_replay_matches_eager(split_k, mode):
-    c = Call(dict(DENSE, out_dtype="fp32") if mode == "atomic" else DENSE, split_k, mode)
+DEPTHWISE = spec(2, 256, 32, 1, 1, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16", "fp32")
+
+
+@pytest.mark.parametrize("sp,split_k,mode", [(DENSE, 0, "auto"), (dict(DENSE, out_dtype="fp32"), 24, "atomic"),
+                                             (DEPTHWISE, 0, "atomic")], ids=["dense_auto", "dense_atomic",
+                                                                             "depthwise_atomic"])
+def test_graph_replay_matches_eager(sp, split_k, mode):
+    c = Call(sp, split_k, mode)
     s = torch.cuda.Stream()
     eager = {}
     for seed in (910, 920, 930):

@@ -720,6 +720,10 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
                                 dump <= (long long)ig.stages * ig.stage_bytes
                             ? 1
                             : 0;
+        // The kernel instance compiled for the most common stride-1 family (see
+        // igemm_wgrad_kernel): x taps on the columns, one M-tile per CTA, a
+        // split mode.
+        pl->ig.spec = ig.xs > 0 && ig.mt_per_cta == 1 && pl->mode != MODE_DIRECT ? 1 : 0;
     }
     pl->ws_rows = pl->kind == KIND_IGEMM ? (long long)pb.G * pb.K : 1;
     pl->ws_L = pb.dw_elems / pl->ws_rows;
@@ -753,12 +757,12 @@ std::string plan_string(const Plan& pl)
                  "katoms=%d "
                  "box=(w%d,h%d,d%d,n%d) KT=%d ktiles=%lld per_split=%lld atoms=%d mtiles=%d mt_per_cta=%d "
                  "mranges=%d tmem_cols=%d stages=%d stage_bytes=%d smem=%d grid=(%u,%u,%u) block=%u ws=%zu "
-                 "reduce=%s zero=%s out=%s",
+                 "reduce=%s zero=%s out=%s code=%s",
                  ig.halo ? "halo" : "pertap", ig.xs ? "mn" : "m", ig.Nmma, mode, pl.S, ig.cluster, ig.Gm, ig.n_gblocks, ig.n_cchunks, ig.Nt, ig.n_ntiles, ig.n_katoms, ig.box[0], ig.box[1],
                  ig.box[2], ig.box[3], ig.KT, ig.total_kt, pl.per_split, ig.n_atoms, ig.n_mtiles, ig.mt_per_cta,
                  ig.n_mranges, ig.tmem_cols, ig.stages, ig.stage_bytes, ig.smem_bytes, pl.grid[0], pl.grid[1],
                  pl.grid[2], pl.block, pl.ws_bytes, pl.mode == MODE_DETERMINISTIC ? "kernel" : "none",
-                 pl.mode == MODE_ATOMIC ? "kernel" : "none", ig.staged ? "staged" : "direct");
+                 pl.mode == MODE_ATOMIC ? "kernel" : "none", ig.staged ? "staged" : "direct", ig.spec ? "x1" : "any");
     } else {
         const DwPlan& dw = pl.dw;
         snprintf(buf, sizeof buf,

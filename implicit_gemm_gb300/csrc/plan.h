@@ -84,6 +84,7 @@ struct IgemmPlan {
     long long tile_clk;    // planner's estimate of one K-tile on one CTA, in SM cycles
     int cluster;           // CTAs per thread-block cluster along the split (1: none)
     int staged;            // 1: each CTA's results are one contiguous dW block, written from shared memory
+    int spec;              // kernel instance: 1 = x taps on the columns, one M-tile per CTA, split mode; 0 = any plan
 };
 
 // CUDA-core depthwise kernel (cpg = kpg = 1).

@@ -8,10 +8,12 @@
 
 namespace wg {
 
-// Device status word: bit 0 = a bounded wait ran out.  Read and cleared by
-// wg_check_status on the host.
+// Device status word: bit 0 = a bounded wait ran out; bit 1 = a kernel
+// instance was launched for a plan it is not compiled for (an internal
+// error).  Read and cleared by wg_check_status on the host.
 __device__ unsigned int g_status;
 constexpr unsigned int kStatusTimeout = 1u;
+constexpr unsigned int kStatusBadPlan = 2u;
 
 // Upper bound of any single wait, in nanoseconds of %globaltimer.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;

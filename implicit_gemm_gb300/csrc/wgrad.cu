@@ -125,7 +125,7 @@ wg::DeviceCaps device_caps()
     if (it != cache.end()) return it->second;
     wg::DeviceCaps c = wg::default_caps(sms);
     const int smem = wg::kMaxSmemPerCta;
-    if (ensure_smem(wg::igemm_wgrad_kernel, smem) == WG_OK) {
+    if (ensure_smem(wg::igemm_wgrad_kernel<0>, smem) == WG_OK) {
         for (int i = 0, q = 1; i < 4; ++i, q *= 2) {
             cudaLaunchConfig_t cfg = {};
             cudaLaunchAttribute attr[1];
@@ -139,7 +139,7 @@ wg::DeviceCaps device_caps()
             cfg.blockDim = dim3(wg::kIgThreads);
             cfg.dynamicSmemBytes = (size_t)smem;
             int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, wg::igemm_wgrad_kernel, &cfg) == cudaSuccess && n > 0)
+            if (cudaOccupancyMaxActiveClusters(&n, wg::igemm_wgrad_kernel<0>, &cfg) == cudaSuccess && n > 0)
                 c.cluster_ctas[i] = n * q;
             else
                 cudaGetLastError();
@@ -469,7 +469,8 @@ int launch_pre(const wg::Plan& pl, void* dw, cudaStream_t stream)
 int launch_igemm_main(const wg::Plan& pl, const Prepared& pr, cudaStream_t stream)
 {
     const wg::IgemmPlan& ig = pl.ig;
-    const int st = ensure_smem(wg::igemm_wgrad_kernel, ig.smem_bytes);
+    auto kernel = ig.spec == 1 ? wg::igemm_wgrad_kernel<1> : wg::igemm_wgrad_kernel<0>;
+    const int st = ensure_smem(kernel, ig.smem_bytes);
     if (st) return st;
     // Consecutive splits form a cluster (grid z is a multiple of the cluster
     // size); the kernel is a programmatic dependent of the kernel before it
@@ -488,7 +489,7 @@ int launch_igemm_main(const wg::Plan& pl, const Prepared& pr, cudaStream_t strea
     cfg.gridDim = dim3(pl.grid[0], pl.grid[1], pl.grid[2]);
     cfg.blockDim = dim3(pl.block);
     cfg.dynamicSmemBytes = (size_t)ig.smem_bytes;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, wg::igemm_wgrad_kernel, pr.tmx, pr.tmy, pr.ig);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, pr.tmx, pr.tmy, pr.ig);
     if (e != cudaSuccess) return cuda_fail("igemm_wgrad_kernel launch", e);
     return WG_OK;
 }
@@ -757,7 +758,9 @@ int wg_check_status(void* stream)
         const unsigned int zero = 0;
         e = cudaMemcpyToSymbol(wg::g_status, &zero, sizeof zero);
         if (e != cudaSuccess) return cuda_fail("cudaMemcpyToSymbol(status)", e);
-        return set_err(WG_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out");
+        return set_err(WG_ERR_DEVICE_TIMEOUT, (v & wg::kStatusBadPlan)
+                                                  ? "internal error: a kernel instance got a plan it is not built for"
+                                                  : "a kernel's bounded wait ran out");
     }
     return WG_OK;
 }

@@ -81,7 +81,8 @@ typedef enum {
     WG_ERR_MISALIGNED = 3,       /* a base pointer is not 16-byte aligned */
     WG_ERR_WORKSPACE = 4,        /* workspace missing or smaller than wg_workspace_size */
     WG_ERR_CUDA = 5,             /* a CUDA runtime/driver call failed */
-    WG_ERR_DEVICE_TIMEOUT = 6    /* a kernel's bounded wait ran out (reported by wg_check_status) */
+    WG_ERR_DEVICE_TIMEOUT = 6    /* a kernel's bounded wait ran out, or (an internal error) a kernel
+                                    found its launch inconsistent; reported by wg_check_status */
 } wg_status;
 
 /* Problem record (the host arguments of the CK page: G_, N_, C_, K_, spatial

@@ -93,6 +93,18 @@ def test_size_limits():
     assert binding.wg_workspace_size(small, split_k=65535, mode="deterministic") > 0
 
 
+def test_kernel_instance_choice():
+    # The trimmed instance serves x-taps-on-columns plans with one M-tile per
+    # CTA in a split mode; every other plan takes the general one.
+    dense = WORKLOADS["2d_dense_n32_h56_c64_k64"][0]
+    assert binding.wg_plan_string(dense).endswith("code=x1")
+    direct = binding.wg_plan_string(dense, 1, "direct", kernel="igemm_taps_mn")
+    assert "taps=mn" in direct and "mode=direct" in direct and direct.endswith("code=any")
+    assert binding.wg_plan_string(dense, kernel="igemm_taps_m").endswith("code=any")
+    for name in ("2d_grouped_g32_c8_k8_n32_h28", "3d_n4_d16_c128_k96_s2", "2d_1x1_n32_h56_c64_k256"):
+        assert binding.wg_plan_string(WORKLOADS[name][0]).endswith("code=any"), name
+
+
 def test_workspace_sizes():
     sp = WORKLOADS["2d_dense_n32_h56_c64_k64"][0]
     E = 1 * 64 * 9 * 64  # rows of 576 = 6 slices of 96: no padding

@@ -211,31 +211,43 @@ __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
         }
     } else {
         // ------------------------------------------------ compute threads
-        const bool active = tid < p.nused;
         const int v = tid % NV, rest = tid / NV;
         const int seg = rest % p.nseg, r = rest / p.nseg;
         const int wo_a = seg * p.seg_len, wo_b = min(p.Wo, wo_a + p.seg_len);
+        const bool active = tid < p.nused && wo_a < wo_b;
+        // Per-tile work is kept small: the thread's offsets inside a stage are
+        // the same for every tile, and the tile's row strip advances by one
+        // (the tiles of a split are consecutive) instead of being divided out.
+        const int cv = v * GM;
+        const int x_off = (r * sh) * xw * CB + cv, y_off = (r * Wo) * CB + cv;
+        // General filters: each tap's offset from the pixel's first X vector.
+        int tap_off[MAXT];
+#pragma unroll
+        for (int t = 0; t < MAXT; ++t) {
+            const int tt = t < p.T ? t : 0;
+            const int ty = tt / p.X, tx = tt - (tt / p.X) * p.X;
+            tap_off[t] = (ty * p.dh * p.xw + tx * p.dw) * p.CB;
+        }
+        int strip = t0 % p.n_hstrips;
         for (int i = 0; i < ntl; ++i) {
             const int st = i % p.stages;
             const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
             if (!mbar_wait(&full[st], ph)) break;
-            const int tile = t0 + i;
-            const int n = tile / p.n_hstrips;
-            const int ho0 = (tile - n * p.n_hstrips) * p.R;
-            if (active && ho0 + r < p.Ho && wo_a < wo_b) {
+            const int ho0 = strip * p.R;
+            strip = strip + 1 == p.n_hstrips ? 0 : strip + 1;
+            if (active && ho0 + r < p.Ho) {
                 const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + st * p.stage_bytes);
                 const uint16_t* ys = reinterpret_cast<const uint16_t*>(smem + st * p.stage_bytes + p.x_bytes_al);
-                const int cv = v * GM;
                 if constexpr (SLIDE3) {
                     // 3x3 filter, stride 1 and dilation 1 along W: a 3x3 window of
                     // X vectors slides along the row, one new column per pixel.
                     // Unrolled by 3 so the three window columns change roles
                     // instead of being copied.
                     const int CBv = CB;
-                    const uint16_t* xr0 = xs + (r * sh) * xw * CBv + cv;
+                    const uint16_t* xr0 = xs + x_off;
                     const uint16_t* xr1 = xr0 + dh * xw * CBv;
                     const uint16_t* xr2 = xr1 + dh * xw * CBv;
-                    const uint16_t* yr = ys + (r * Wo) * CBv + cv;
+                    const uint16_t* yr = ys + y_off;
                     Packed<GM> wa[3], wb[3], wc[3];
                     load_col3<GM>(xr0, xr1, xr2, wo_a * CBv, wa);
                     load_col3<GM>(xr0, xr1, xr2, (wo_a + 1) * CBv, wb);
@@ -257,17 +269,10 @@ __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
                         }
                     }
                 } else {
-                    int tap_off[MAXT];
-#pragma unroll
-                    for (int t = 0; t < MAXT; ++t) {
-                        const int tt = t < p.T ? t : 0;
-                        const int ty = tt / p.X, tx = tt - (tt / p.X) * p.X;
-                        tap_off[t] = (ty * p.dh * p.xw + tx * p.dw) * p.CB;
-                    }
                     for (int wo = wo_a; wo < wo_b; ++wo) {
                         Packed<GM> dy;
-                        load_vec<GM>(ys + (r * p.Wo + wo) * p.CB + cv, dy);
-                        const uint16_t* xb = xs + ((r * p.sh) * p.xw + wo * p.sw) * p.CB + cv;
+                        load_vec<GM>(ys + y_off + wo * CB, dy);
+                        const uint16_t* xb = xs + x_off + wo * p.sw * CB;
 #pragma unroll
                         for (int t = 0; t < MAXT; ++t) {
                             if (t < p.T) {

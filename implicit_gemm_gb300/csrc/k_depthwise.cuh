@@ -229,9 +229,9 @@ __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
             tap_off[t] = (ty * p.dh * p.xw + tx * p.dw) * p.CB;
         }
         int strip = t0 % p.n_hstrips;
+        int st = 0;
+        uint32_t ph = 0;
         for (int i = 0; i < ntl; ++i) {
-            const int st = i % p.stages;
-            const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
             if (!mbar_wait(&full[st], ph)) break;
             const int ho0 = strip * p.R;
             strip = strip + 1 == p.n_hstrips ? 0 : strip + 1;
@@ -286,6 +286,7 @@ __global__ void __launch_bounds__(288, GM >= 8 ? 1 : 2)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
+            if (++st == p.stages) st = 0, ph ^= 1u;
         }
     }
     __syncthreads();

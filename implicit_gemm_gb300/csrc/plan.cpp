@@ -651,21 +651,22 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
                     "the depthwise kernel needs C = K = 1, 1-D or 2-D, <= 9 taps and G %% 8 == 0");
     if (use_dw) {
         pl->kind = KIND_DEPTHWISE;
-        // Automatic merge degree, after the PR #12359 page's policy (PR #12951:
-        // the largest admissible Gm at the kernel's tile): the widest channel
-        // vector this kernel admits at its design point of two CTAs per SM
-        // (eight-channel vectors hold 72 accumulators and run one CTA per SM)
-        // where the wider vector saves loads, else two channels.  With the
-        // register sliding window (3x3, stride and dilation 1 along W) each
-        // loaded X vector feeds 3*Gm multiply-adds and each dY vector 9*Gm, so
-        // four channels halve the load instructions per multiply-add against
-        // two; without it every tap reloads its X vector and a wider vector
-        // only cuts the threads per row tile (shorter, more ragged column
-        // segments).  Narrower vectors are tried when a tile does not fit.
+        // Automatic merge degree.  The PR #12359 page's policy (PR #12951)
+        // takes the largest admissible Gm at the kernel's tile; here the
+        // vector is two channels, one packed 32-bit word: every load moves a
+        // pair and every mixed-precision multiply-add pair reads one word.
+        // Wider vectors cut the load instructions per multiply-add further,
+        // but with the per-tile work of the loop reduced to its loads and
+        // multiply-adds the main loop runs at the DRAM rate either way, while
+        // a wider vector lengthens the end of every CTA (9*Gm accumulators per
+        // thread through the shuffle reduction) and shortens the column
+        // segments (more segment starts and ragged tails).  Measured with the
+        // policy sweep over 16 shapes (bench.py --sweep): two channels best or
+        // within a few percent on the 3x3 shapes.  One channel when a
+        // two-channel tile does not fit.
         if (o.group_merge == 0) {
-            const bool window = pb.filt[1] == 3 && pb.filt[2] == 3 && pb.stride[2] == 1 && pb.dil[2] == 1;
             st = WG_ERR_NOT_SUPPORTED;
-            for (int g = window ? 4 : 2; g >= 1 && st != WG_OK; g /= 2) {
+            for (int g = 2; g >= 1 && st != WG_OK; g /= 2) {
                 wg_options og = o;
                 og.group_merge = g;
                 st = plan_depthwise(pl, og, num_sms, g == 1 ? err : nullptr);

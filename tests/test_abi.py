@@ -293,13 +293,13 @@ def test_planner_choices_on_default_caps():
     assert (dense["taps"], dense["S"], dense["mt_per_cta"], dense["box"]) == ("mn", "75", "1", "(w32,h8,d1,n1)")
     dense = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_dense_n32_h56_c64_k64"][0], kernel="igemm_taps_m"))
     assert (dense["S"], dense["mt_per_cta"], dense["box"]) == ("75", "3", "(w8,h7,d1,n4)")
-    # Depthwise vector width: four channels where the 3x3 sliding window applies
-    # (whatever the problem size: no threshold on the tile count), two for
-    # stride 2 along W, and the largest that fits when the caller asks for none.
+    # Depthwise vector width: two channels (one packed word) whatever the
+    # filter, stride or problem size -- no threshold on anything -- unless the
+    # caller asks for a width.
     dwp = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_depthwise_g512_n64_h28"][0]))
-    assert (dwp["kernel"], dwp["Gm"]) == ("depthwise", "4")
+    assert (dwp["kernel"], dwp["Gm"]) == ("depthwise", "2")
     small = _plan_fields(binding.wg_plan_string(spec(2, 64, 2, 1, 1, [9, 13], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1])))
-    assert small["Gm"] == "4"
+    assert small["Gm"] == "2"
     strided = _plan_fields(binding.wg_plan_string(spec(2, 64, 2, 1, 1, [9, 13], [3, 3], [2, 2], [1, 1], [1, 1],
                                                        [1, 1])))
     assert strided["Gm"] == "2"

@@ -300,18 +300,18 @@ L2_BYTES = 129 * 1000 * 1000
 # such a capture reports null.  ncu flushes the caches before the captured
 # launch, so atomic plans also count the dW lines their atomic adds fetch.
 TRAFFIC = {
-    # igemm_wgrad_kernel, taps=mn S = 75 two-stage: 25,783,040 B read + 256 B written.
-    "2d_dense_n32_h56_c64_k64": 25_783_296,
-    # igemm_wgrad_kernel, Gm = 8 fold, staged atomic output: 25,854,976 B read + 5,888 B written.
-    "2d_grouped_g32_c8_k8_n32_h28": 25_860_864,
-    # depthwise_wgrad_kernel<bf16, 4, sliding>, atomic: 103,167,488 B read + 3,410,432 B written.
-    "2d_depthwise_g512_n64_h28": 106_577_920,
-    # igemm_wgrad_kernel, per-tap S = 4 atomic: 6,010,880 B read (X + dY + the dW lines) + 0 B written.
+    # igemm_wgrad_kernel<1> (x taps on the columns, one M-tile), S = 75 two-stage: 25,775,872 B read + 0 B written.
+    "2d_dense_n32_h56_c64_k64": 25_775_872,
+    # igemm_wgrad_kernel<0>, Gm = 8 fold, staged atomic output: 25,855,232 B read + 0 B written.
+    "2d_grouped_g32_c8_k8_n32_h28": 25_855_232,
+    # depthwise_wgrad_kernel<bf16, 2, sliding>, atomic: 103,135,744 B read + 3,367,680 B written.
+    "2d_depthwise_g512_n64_h28": 106_503_424,
+    # igemm_wgrad_kernel<0>, per-tap S = 4 atomic: 6,010,880 B read (X + dY + the dW lines) + 0 B written.
     "3d_n4_d16_c128_k96_s2/auto": 6_010_880,
-    # igemm_wgrad_kernel, S = 87 atomic: 64,386,816 B read + 95,232 B written.
-    "2d_1x1_n32_h56_c64_k256": 64_482_048,
-    # igemm_wgrad_kernel, per-tap S = 49 atomic: 19,495,168 B read + 0 B written.
-    "2d_1x1s2_n32_h56_c256_k128": 19_495_168,
+    # igemm_wgrad_kernel<0>, S = 87 atomic: 64,386,816 B read + 195,840 B written.
+    "2d_1x1_n32_h56_c64_k256": 64_582_656,
+    # igemm_wgrad_kernel<0>, per-tap S = 49 atomic: 19,494,656 B read + 0 B written.
+    "2d_1x1s2_n32_h56_c256_k128": 19_494_656,
 }
 MAX_COPIES = 512
 

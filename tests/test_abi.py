@@ -403,17 +403,3 @@ def test_planner_invariants_on_random_problems():
                         raise AssertionError(f"forced column form planned as rows: {ps}")
     assert min(checked.values()) > 20, checked
 
-
-def test_multiply_shift_division_is_exact():
-    # The staged epilogue divides item indices (< 2^20) by small divisors
-    # (< 4096) as (n * fd) >> 32 with fd = floor(2^32 / d) + 1.  floor(n / d)
-    # changes only at multiples of d and the error term grows with n, so
-    # checking n = k*d - 1 and k*d for every k covers every n below 2^20.
-    import numpy as np
-    for d in range(1, 4096):
-        fd = (1 << 32) // d + 1
-        k = np.arange(1, (1 << 20) // d + 1, dtype=np.uint64)
-        for n in (k * np.uint64(d) - np.uint64(1), k * np.uint64(d)):
-            n = n[n < (1 << 20)]
-            q = (n * np.uint64(fd)) >> np.uint64(32)
-            assert np.array_equal(q, n // np.uint64(d)), d

@@ -211,3 +211,64 @@ def test_concurrent_host_threads_match_alone():
         t.join()
     assert not errors, errors
     binding.wg_check_status()
+
+
+# Every kernel of a call is launched as a programmatic dependent of the kernel
+# before it and waits for it before reading X and dY.  Here the kernel before
+# it is the library's own backward-data kernel, which lets its dependents
+# launch at once and writes the X that the weight-gradient call reads: a call
+# that read X before that kernel finished would see stale or partial values.
+# Each mode's first kernel is covered: the split-K kernel (two-stage), the
+# zeroing kernel (atomic), the depthwise kernel (depthwise, two-stage and
+# atomic).
+CHAIN = [
+    ("two_stage", spec(2, 1, 8, 64, 64, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16", "bf16"),
+     "deterministic"),
+    ("atomic", spec(2, 1, 8, 64, 64, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16", "fp32"), "atomic"),
+    ("depthwise_atomic", spec(2, 64, 8, 1, 1, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16", "fp32"),
+     "atomic"),
+    ("depthwise_two_stage", spec(2, 64, 8, 1, 1, [28, 28], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], "bf16", "fp32"),
+     "deterministic"),
+]
+
+
+@pytest.mark.parametrize("name,sp,mode", CHAIN, ids=[c[0] for c in CHAIN])
+def test_call_waits_for_the_kernel_that_writes_its_input(name, sp, mode):
+    torch.manual_seed(7)
+    # Backward-data on the same geometry writes X (bf16) from dY1 and W.
+    spd = dict(sp, out_dtype="bf16")
+    n_x = sp["N"] * int(np.prod(sp["in"])) * sp["G"] * sp["C"]
+    n_dy = sp["N"] * int(np.prod(sp["in"])) * sp["G"] * sp["K"]  # stride 1, same padding: out = in
+    dy1 = [torch.randn(n_dy, device="cuda").to(torch.bfloat16) for _ in range(3)]
+    w = torch.randn(_ndw(sp), device="cuda").to(torch.bfloat16)
+    dy2 = torch.randn(n_dy, device="cuda").to(torch.bfloat16)
+    x = torch.empty(n_x, dtype=torch.bfloat16, device="cuda")
+    odt = torch.float32 if sp["out_dtype"] == "fp32" else torch.bfloat16
+    nb_d = binding.wg_bwd_data_workspace_size(spd)
+    ws_d = torch.empty(max(nb_d, 16), dtype=torch.uint8, device="cuda")
+    nb = binding.wg_workspace_size(sp, 0, mode, 0)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    chained = []
+    with torch.cuda.stream(s):
+        for d in dy1:  # no synchronisation inside the chain
+            binding.wg_conv_bwd_data(spd, d, w, x, ws_d, nb_d, stream=s)
+            dw = torch.full((_ndw(sp),), float("nan"), dtype=odt, device="cuda")
+            binding.wg_conv_bwd_weight(sp, x, dy2, dw, 0, mode, 0, ws, nb, stream=s)
+            chained.append(dw)
+    s.synchronize()
+    binding.wg_check_status()
+    for i, d in enumerate(dy1):
+        # The same calls one at a time, with the device idle in between.
+        binding.wg_conv_bwd_data(spd, d, w, x, ws_d, nb_d)
+        torch.cuda.synchronize()
+        ref = torch.empty((_ndw(sp),), dtype=odt, device="cuda")
+        binding.wg_conv_bwd_weight(sp, x, dy2, ref, 0, mode, 0, ws, nb)
+        torch.cuda.synchronize()
+        got, want = chained[i].float().cpu().numpy(), ref.float().cpu().numpy()
+        if mode == "deterministic":
+            np.testing.assert_array_equal(got, want, err_msg=f"{name} call {i}")
+        else:
+            np.testing.assert_allclose(got, want, rtol=0, atol=1e-4 * float(np.max(np.abs(want))),
+                                       err_msg=f"{name} call {i}")
+    binding.wg_check_status()

@@ -12,6 +12,8 @@ once, and from several host threads.
   synchronising in between must each give the bits of a run alone.
 * Threads: four host threads calling concurrently (the library caches plans
   and tensor maps under a lock) must give the same bits.
+* Launch chain: a backward-data kernel writes the X of a weight-gradient call
+  queued right behind it; the call's first kernel must wait for it.
 """
 import threading
 

@@ -299,9 +299,20 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
                 // workload, where 2, 3 and 5 M-tiles per CTA measured 27.6,
                 // 24.7 and 26.5 us), plus a fixed overhead; fewer than 3 stages
                 // exposes latency.
+                // With the x taps on the columns the MMAs' operand reads and
+                // the stage's TMA writes share the SM's shared-memory
+                // bandwidth, so a tile with less halo (fewer stage bytes per
+                // pixel) costs less although the tensor pipe would tie (grouped
+                // G = 32: a 32 x 4 pixel tile 14.7 us against 14.9-15.1 us for
+                // 8 x 2 x 8 images; 8 x 14 measured 14.4 us).  Charging the
+                // stage bytes to the plans with every tap on the rows as well
+                // moved three 5x5 depthwise folds to tiles that ran 3-12%
+                // slower, so there the MMA term stays alone.
                 const long long mranges = cdiv(c.n_mtiles, mt);
+                const long long ksteps = c.KT / 16;
                 const long long mma_one = std::max<long long>(c.Nmma / 2, 32 + c.Nmma / 4);
-                const long long mma_clk = (long long)mt * (c.KT / 16) * mma_one;
+                const long long smem_clk = (long long)mt * ksteps * (32 + c.Nmma / 4) + stage / 128;
+                const long long mma_clk = std::max((long long)mt * ksteps * mma_one, mn ? smem_clk : 0LL);
                 const long long load_clk = stage / 40;
                 long long tile_clk = std::max(mma_clk, load_clk) + 64;
                 if (stages < 3) tile_clk = tile_clk * 13 / 10;

@@ -302,8 +302,8 @@ L2_BYTES = 129 * 1000 * 1000
 TRAFFIC = {
     # igemm_wgrad_kernel<1> (x taps on the columns, one M-tile), S = 75 two-stage: 25,775,872 B read + 0 B written.
     "2d_dense_n32_h56_c64_k64": 25_775_872,
-    # igemm_wgrad_kernel<0>, Gm = 8 fold, staged atomic output: 25,855,232 B read + 0 B written.
-    "2d_grouped_g32_c8_k8_n32_h28": 25_855_232,
+    # igemm_wgrad_kernel<0>, Gm = 8 fold, 32 x 4 pixel tiles, staged atomic output: 25,854,464 B read + 0 B written.
+    "2d_grouped_g32_c8_k8_n32_h28": 25_854_464,
     # depthwise_wgrad_kernel<bf16, 2, sliding>, atomic: 103,135,744 B read + 3,367,680 B written.
     "2d_depthwise_g512_n64_h28": 106_503_424,
     # igemm_wgrad_kernel<0>, per-tap S = 4 atomic: 6,010,880 B read (X + dY + the dW lines) + 0 B written.

@@ -144,7 +144,8 @@ def plan_tag(plan):
     f = dict(kv.split("=", 1) for kv in plan.split() if "=" in kv)
     if f.get("kernel") == "depthwise":
         return f"dw Gm{f['Gm']} {f['mode'][:3]} S{f['S']}"
-    return f"tc {f.get('taps', '')} {f['mode'][:3]} S{f['S']} Gm{f.get('Gm', 1)}"
+    pair = " pair" if f.get("code") == "pair" else ""
+    return f"tc {f.get('taps', '')}{pair} {f['mode'][:3]} S{f['S']} Gm{f.get('Gm', 1)}"
 
 
 def compact_configs(main_label, main, extra):

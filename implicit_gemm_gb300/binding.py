@@ -112,7 +112,7 @@ def make_problem(spec: dict) -> WgProblem:
     return p
 
 
-KERNELS = {"auto": 0, "igemm": 1, "depthwise": 2, "igemm_taps_m": 3, "igemm_taps_mn": 4}
+KERNELS = {"auto": 0, "igemm": 1, "depthwise": 2, "igemm_taps_m": 3, "igemm_taps_mn": 4, "igemm_pair": 5}
 
 
 def make_options(split_k: int = 0, mode: str = "auto", group_merge: int = 0, cluster: int = 0,

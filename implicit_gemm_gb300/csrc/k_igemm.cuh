@@ -82,6 +82,12 @@ struct IgParams {
     // elements, that the epilogue gathers in shared memory and adds or stores
     // with 16-byte accesses.
     int staged;
+    // CTA pair (igemm_wgrad_pair_kernel): the split's two M-tiles run on the
+    // two CTAs of a cluster that share M = 256 MMAs.  Both load the same X
+    // patch, rank 0 at byte pair_xoff of the stage and rank 1 pair_xshift
+    // bytes lower, so that rank 1's first atom (the tile's third) sits at the
+    // offset of rank 0's first atom.
+    int pair, pair_xoff, pair_xshift;
     // Staged output: atom_of[(tap / (xs ? xs : 1)) * ncc + cc] is the index of
     // the atom holding channel chunk cc of filter tap `tap` (x = 0 when the x
     // taps sit on the columns).
@@ -320,7 +326,13 @@ __global__ void __launch_bounds__(kIgThreads, 1)
 
     if constexpr (SPEC == 1) {
         // The host launches this instance only for its plan family.
-        if (!p.xs || p.mtpc != 1 || p.mode == 1) {
+        if (!p.xs || p.mtpc != 1 || p.mode == 1 || p.pair) {
+            if (threadIdx.x == 0) atomicOr(&g_status, kStatusBadPlan);
+            return;
+        }
+    } else {
+        // Pair plans run on igemm_wgrad_pair_kernel.
+        if (p.pair) {
             if (threadIdx.x == 0) atomicOr(&g_status, kStatusBadPlan);
             return;
         }

@@ -98,6 +98,8 @@ bool dim_phases(int F, int s, int d, DimPhases* o)
 struct IgCand {
     int halo, box[4], nt[4], KT, mt, stages, stage_bytes, patch[3], patch_bytes, n_patches, dy_off;
     int xs, Nt, n_ntiles, n_katoms, n_atoms, n_mtiles, Nmma, dy_w, dy_bytes;
+    int pair;
+    long long tx_bytes;  // TMA bytes per K-tile and CTA
     long long cost, tile_clk, S;
 };
 
@@ -114,6 +116,9 @@ constexpr long long kExtraLaunchClk = 4280;
 // Cold reads from HBM, device-wide (~6 TB/s at ~2 GHz): no split degree reads
 // the inputs faster than this.
 constexpr long long kDramBytesPerClk = 3000;
+// The CTA pair's extra cost per call (cluster launch, cluster barriers and the
+// paired TMEM allocation and release), measured ~1 us.
+constexpr long long kPairCallClk = 2100;
 
 long long epilogue_clk(long long dw_bytes, int n_out, int Q, long long red_bytes, bool atomic)
 {
@@ -226,10 +231,41 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
         mn_no = "no cluster reduction";
     else if (!ph_ok || ig.n_cchunks > kMaxPatches || (long long)Z * Y * ig.n_cchunks > kMaxHaloAtoms)
         mn_no = "one halo patch per channel chunk";
-    if (o.kernel == WG_KERNEL_IGEMM_TAPS_MN && mn_no)
+    if ((o.kernel == WG_KERNEL_IGEMM_TAPS_MN || o.kernel == WG_KERNEL_IGEMM_PAIR) && mn_no)
         return fail(err, WG_ERR_NOT_SUPPORTED, "the x-taps-on-columns tile needs %s", mn_no);
-    const bool try_m = o.kernel != WG_KERNEL_IGEMM_TAPS_MN;
+    // The CTA-pair form of it (igemm_wgrad_pair_kernel): a split's two M-tiles
+    // (atoms y = 0, 1 and y = 2, 3 of one 64-channel chunk) on the two CTAs of
+    // a cluster, rank r staging output channels 32r .. 32r+31 of dY.
+    const char* pair_no = nullptr;
+    if (mn_no)
+        pair_no = mn_no;
+    else if (Gm != 1 || kwin != 64)
+        pair_no = "K = 64 without group folding";
+    else if (ig.n_cchunks != 1)
+        pair_no = "C <= 64";
+    else if (Z != 1 || (Y != 3 && Y != 4))
+        pair_no = "a 2-D filter with 3 or 4 taps along h";
+    else if (caps.cluster_ctas[1] < 2)
+        pair_no = "clusters of two CTAs at the kernel's shared-memory size";
+    if (o.kernel == WG_KERNEL_IGEMM_PAIR && pair_no)
+        return fail(err, WG_ERR_NOT_SUPPORTED, "the CTA-pair tile needs %s", pair_no);
+    // Where the x taps can go on the columns and the k window is 64 wide, the
+    // form with every tap on the rows (then N = 64) is taken only when asked
+    // for: on the 56x56 C = K = 64 workload it measured slower at every split
+    // degree (S = 1: 616 against 373 us; S = 4: 160 against 99 us; S = 75:
+    // 25.3 against 21.1 us), although the cost model below rates it close at
+    // low split degrees (its 128x64 MMAs and nine tap views per K-tile cost
+    // more than the model charges).  Wider k windows give it N = 128-256
+    // MMAs at the tensor rate, and the model chooses.
     const bool try_mn = !mn_no && o.kernel != WG_KERNEL_IGEMM_TAPS_M;
+    const bool try_m = o.kernel == WG_KERNEL_IGEMM_TAPS_M ||
+                       (!(try_mn && ig.Nt <= 64) && o.kernel != WG_KERNEL_IGEMM_TAPS_MN &&
+                        o.kernel != WG_KERNEL_IGEMM_PAIR);
+    const bool try_single_mn = o.kernel != WG_KERNEL_IGEMM_PAIR;
+    const bool try_pair = !pair_no && o.kernel != WG_KERNEL_IGEMM_TAPS_MN && o.kernel != WG_KERNEL_IGEMM_TAPS_M;
+    // Pairs resident at once (clusters must sit within one GPC).
+    DeviceCaps caps_pair = caps;
+    caps_pair.cluster_ctas[0] = caps.cluster_ctas[1] / 2 * 2;
 
     const int avail = kMaxSmemPerCta - 3072;
     IgCand best{};
@@ -286,12 +322,26 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
             if (dy_bytes > avail) continue;
             c.dy_bytes = (int)dy_bytes;
             const long long ktiles = (long long)c.nt[0] * c.nt[1] * c.nt[2] * c.nt[3];
-            for (int mt = mt_max; mt >= 1; --mt) {
+            // mt M-tiles per CTA from mt_max down to 1, then (pr = 1) the CTA
+            // pair: one M-tile per CTA, half of dY.
+            for (int it = 0; it <= mt_max; ++it) {
+                const int pr = it == mt_max ? 1 : 0;
+                const int mt = pr ? 1 : mt_max - it;
+                if (pr ? !(mn && try_pair) : (mn && !try_single_mn)) continue;
                 const int n_x = halo ? c.n_patches : 2 * mt;
-                const long long stage = ((long long)n_x * c.patch_bytes + c.dy_bytes + 1023) / 1024 * 1024;
-                if (stage > avail) continue;
+                // The pair's stage: [dY half][xshift][X patch]; xshift (atom 2's
+                // row offset, 2 dil_h patch rows) must keep the X copies 1024-aligned.
+                const long long dy_cta = pr ? c.dy_bytes / 2 : c.dy_bytes;
+                const long long xshift = pr ? 2LL * pb.dil[1] * c.patch[0] * 128 : 0;
+                if (xshift % 1024) continue;
+                const long long stage = ((long long)n_x * c.patch_bytes + dy_cta + 1023) / 1024 * 1024 + xshift;
+                // The single-CTA stage of the same tile (the pair is costed from it).
+                const long long stage1 = ((long long)n_x * c.patch_bytes + c.dy_bytes + 1023) / 1024 * 1024;
+                if (stage > avail || stage1 > avail) continue;
                 const int stages = std::min(8, (int)(avail / stage));
                 if (stages < 2) continue;
+                // Stage bytes the TMA writes (the pair's gap is not written).
+                const long long written = pr ? (long long)n_x * c.patch_bytes + dy_cta : stage;
                 // Per K-tile and CTA: the MMAs -- each the longer of the tensor
                 // pipe (N/2 cycles) and its shared-memory reads (A 4 KB + B 32*N
                 // bytes at ~128 B/cycle) -- against the stage's fill at ~40
@@ -311,11 +361,21 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
                 const long long mranges = cdiv(c.n_mtiles, mt);
                 const long long ksteps = c.KT / 16;
                 const long long mma_one = std::max<long long>(c.Nmma / 2, 32 + c.Nmma / 4);
-                const long long smem_clk = (long long)mt * ksteps * (32 + c.Nmma / 4) + stage / 128;
+                const long long smem_clk = (long long)mt * ksteps * (32 + c.Nmma / 4) + stage1 / 128;
                 const long long mma_clk = std::max((long long)mt * ksteps * mma_one, mn ? smem_clk : 0LL);
-                const long long load_clk = stage / 40;
+                const long long load_clk = stage1 / 40;
                 long long tile_clk = std::max(mma_clk, load_clk) + 64;
-                if (stages < 3) tile_clk = tile_clk * 13 / 10;
+                if ((pr ? stages : std::min(8, (int)(avail / stage1))) < 3) tile_clk = tile_clk * 13 / 10;
+                // The CTA pair halves each SM's operand reads of B and its dY
+                // loads, but on the 56x56 workload its K-tile measured only
+                // 3.5% shorter than the single CTA's (0.804 against 0.833 us
+                // with one split; equal with 75 splits, when the memory system
+                // rather than the SM bounds the loop), and its cluster launch,
+                // barriers and paired TMEM release cost ~1 us per call
+                // (kPairCallClk below): it pays for long splits only (S = 1
+                // and 4: 360 and 97 us against 373 and 99; S = 38 and 75:
+                // 20.1 and 16.2 us against 19.1 and 15.5).
+                if (pr) tile_clk = tile_clk * 965 / 1000;
                 // Whole-call estimate for the split degrees this tiling may get
                 // (the caller's; else enough splits to fill the device once, or
                 // 3/4, 2/3 or 1/2 of that): the K-tiles of one split in waves of
@@ -325,7 +385,8 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
                 // the per-SM loads, bounds the main loop (1x1 C 64 -> K 256:
                 // 23.3-23.8 us with S = 75-100 against 24.8 us with S = 150).
                 const long long base = mranges * c.n_ntiles * ig.n_gblocks;
-                const long long s_fill = split_for(o, base, ktiles, caps);
+                const DeviceCaps& cp = pr ? caps_pair : caps;
+                const long long s_fill = split_for(o, base, ktiles, cp);
                 const bool auto_s = o.split_k == 0 && o.mode != WG_MODE_DIRECT && o.cluster <= 1;
                 const bool atomic_sum = takes_atomic(o, pb);
                 const long long dram_clk = dram_read_clk(pb);
@@ -336,15 +397,22 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
                     if (fi > 0) S = cdiv(ktiles, cdiv(ktiles, S));  // splits of whole, even K-tile counts
                     // The per-CTA estimate also breaks ties between tilings whose
                     // main loops all sit under the HBM bound (with weight 1/8).
-                    const long long waves = cdiv(base * S, caps.cluster_ctas[0]);
+                    const long long waves = cdiv(base * S, cp.cluster_ctas[0]);
                     const long long main_clk = waves * cdiv(ktiles, S) * tile_clk;
-                    const long long cost = std::max(main_clk, dram_clk) + main_clk / 8 +
+                    const long long cost = std::max(main_clk, dram_clk) + main_clk / 8 + (pr ? kPairCallClk : 0) +
                                            epilogue_clk(pb.dw_elems * 4, (int)S, 1, red_bytes, atomic_sum);
-                    if (best.cost < 0 || cost < best.cost) {
+                    // With the x taps on the columns, ties go to the fewer TMA
+                    // bytes per K-tile (fewer bytes through L2; among the tilings
+                    // of the other form this moved 5x5 depthwise folds to slower
+                    // tiles, as the shared-memory charge above did).
+                    if (best.cost < 0 || cost < best.cost ||
+                        (mn && best.xs && cost == best.cost && written < best.tx_bytes)) {
                         c.mt = mt;
                         c.stages = stages;
                         c.stage_bytes = (int)stage;
                         c.dy_off = n_x * c.patch_bytes;
+                        c.pair = pr;
+                        c.tx_bytes = written;
                         c.cost = cost;
                         c.tile_clk = tile_clk;
                         c.S = S;
@@ -364,7 +432,9 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
     ig.n_mtiles = best.n_mtiles;
     ig.Nmma = best.Nmma;
     ig.dy_w = best.dy_w;
-    ig.dy_bytes = best.dy_bytes;
+    ig.pair = best.pair;
+    // A CTA of the pair stages 32 of the 64 output channels of the dY patch.
+    ig.dy_bytes = ig.pair ? best.dy_bytes / 2 : best.dy_bytes;
     std::memcpy(ig.box, best.box, sizeof best.box);
     std::memcpy(ig.ntile, best.nt, sizeof best.nt);
     std::memcpy(ig.patch, best.patch, sizeof best.patch);
@@ -376,6 +446,13 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
     ig.n_patches = ig.halo ? best.n_patches : 2 * ig.mt_per_cta;
     ig.dy_off = ig.n_patches * ig.patch_bytes;
     ig.stage_bytes = round_up(ig.dy_off + ig.dy_bytes, 1024);
+    if (ig.pair) {
+        // [dY half][xshift][X patch] (rank 1's X copy xshift bytes lower).
+        ig.pair_xshift = 2 * pb.dil[1] * ig.patch[0] * 128;
+        ig.dy_off = 0;
+        ig.pair_xoff = round_up(ig.dy_bytes, 1024) + ig.pair_xshift;
+        ig.stage_bytes = ig.pair_xoff + ig.patch_bytes;
+    }
     ig.stages = std::min(8, avail / ig.stage_bytes);
     // Stage buffers, then 1 KB of slack that a padding atom's reads may reach,
     // then 1 KB of barriers and tables; plus 1 KB to align the base.
@@ -424,6 +501,15 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
             ig.atom_off[i] = at[i].off;
             ig.atom_tap[i] = (unsigned short)at[i].tap;
             ig.atom_cc[i] = (unsigned char)at[i].cc;
+        }
+        if (ig.pair) {
+            // Rank 1's X copy sits pair_xshift bytes lower, so that its atoms
+            // (y = 2, 3) are read at the offsets of rank 0's (y = 0, 1): the
+            // pair shares one A descriptor.  Atoms y are dil_h rows apart.
+            const unsigned d1 = ig.atom_off[1] - ig.atom_off[0], d2 = ig.atom_off[2] - ig.atom_off[0];
+            if (na < 3 || ig.atom_off[0] != 0 || d2 != (unsigned)ig.pair_xshift || d2 != 2 * d1 ||
+                (na == 4 && ig.atom_off[3] - ig.atom_off[0] != 3 * d1))
+                return fail(err, WG_ERR_NOT_SUPPORTED, "CTA-pair atoms are not evenly spaced");
         }
     }
 
@@ -642,7 +728,7 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
         return fail(err, WG_ERR_INVALID_ARGUMENT, "group_merge must be 0, 1, 2, 4 or 8");
     if (o.cluster != 0 && o.cluster != 1 && o.cluster != 2 && o.cluster != 4 && o.cluster != 8)
         return fail(err, WG_ERR_INVALID_ARGUMENT, "cluster must be 0, 1, 2, 4 or 8");
-    if (o.kernel < WG_KERNEL_AUTO || o.kernel > WG_KERNEL_IGEMM_TAPS_MN)
+    if (o.kernel < WG_KERNEL_AUTO || o.kernel > WG_KERNEL_IGEMM_PAIR)
         return fail(err, WG_ERR_INVALID_ARGUMENT, "bad kernel selector");
     if (o.mode == WG_MODE_DIRECT && o.split_k > 1 && o.split_k != o.cluster)
         return fail(err, WG_ERR_INVALID_ARGUMENT,
@@ -735,7 +821,7 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
         // The kernel instance compiled for the most common stride-1 family (see
         // igemm_wgrad_kernel): x taps on the columns, one M-tile per CTA, a
         // split mode.
-        pl->ig.spec = ig.xs > 0 && ig.mt_per_cta == 1 && pl->mode != MODE_DIRECT ? 1 : 0;
+        pl->ig.spec = ig.pair ? 2 : ig.xs > 0 && ig.mt_per_cta == 1 && pl->mode != MODE_DIRECT ? 1 : 0;
     }
     pl->ws_rows = pl->kind == KIND_IGEMM ? (long long)pb.G * pb.K : 1;
     pl->ws_L = pb.dw_elems / pl->ws_rows;
@@ -774,7 +860,8 @@ std::string plan_string(const Plan& pl)
                  ig.box[2], ig.box[3], ig.KT, ig.total_kt, pl.per_split, ig.n_atoms, ig.n_mtiles, ig.mt_per_cta,
                  ig.n_mranges, ig.tmem_cols, ig.stages, ig.stage_bytes, ig.smem_bytes, pl.grid[0], pl.grid[1],
                  pl.grid[2], pl.block, pl.ws_bytes, pl.mode == MODE_DETERMINISTIC ? "kernel" : "none",
-                 pl.mode == MODE_ATOMIC ? "kernel" : "none", ig.staged ? "staged" : "direct", ig.spec ? "x1" : "any");
+                 pl.mode == MODE_ATOMIC ? "kernel" : "none", ig.staged ? "staged" : "direct",
+                 ig.spec == 2 ? "pair" : ig.spec ? "x1" : "any");
     } else {
         const DwPlan& dw = pl.dw;
         snprintf(buf, sizeof buf,

@@ -84,7 +84,14 @@ struct IgemmPlan {
     long long tile_clk;    // planner's estimate of one K-tile on one CTA, in SM cycles
     int cluster;           // CTAs per thread-block cluster along the split (1: none)
     int staged;            // 1: each CTA's results are one contiguous dW block, written from shared memory
-    int spec;              // kernel instance: 1 = x taps on the columns, one M-tile per CTA, split mode; 0 = any plan
+    int spec;              // kernel instance: 2 = the CTA pair; 1 = x taps on the columns, one M-tile per CTA, split mode; 0 = any plan
+    // CTA pair (xs > 0, two M-tiles): the M-tiles of a split run on the two
+    // CTAs of a cluster that share M = 256 MMAs (tcgen05 .cta_group::2); each
+    // stages 32 of the 64 output channels of the dY patch (dy_bytes is that
+    // half, at offset 0 of the stage) and the same X patch, rank 0's at
+    // pair_xoff and rank 1's pair_xshift bytes lower (the row offset of atom
+    // 2), so that one A descriptor serves both.
+    int pair, pair_xoff, pair_xshift;
 };
 
 // CUDA-core depthwise kernel (cpg = kpg = 1).

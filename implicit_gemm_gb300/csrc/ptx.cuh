@@ -318,6 +318,10 @@ __device__ __forceinline__ void cluster_sync_all()
 {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
+// The two halves of cluster_sync_all, for work between them: every thread
+// arrives once and then waits once, on every path.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
 // Issue a load of 16 consecutive 32-bit TMEM columns of this warp's 32 lanes
 // into r[0..15]; the registers are valid only after tmem_wait_fence.
@@ -339,6 +343,58 @@ __device__ __forceinline__ void reg_fence16(uint32_t* r)
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
                    "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
                    "+r"(r[15]));
+}
+
+// ---------------------------------------------------------------- CTA pairs
+// Two CTAs of a cluster of two (ranks 0 and 1, on two SMs) share one MMA of
+// M = 256: each holds half of A's rows and half of B's columns in its shared
+// memory and 128 rows of D in its tensor memory; rank 0 issues the MMAs.
+// Every tcgen05 operation of a kernel that uses them names .cta_group::2.
+
+// Tensor memory at the same column address in both CTAs of the pair.  One warp
+// of each CTA issues it (converged); each gets the address in its own `dst`.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D[tmem of both CTAs] (+)= A * B over the pair; the descriptors' addresses
+// are offsets valid in both CTAs' shared memory.  Issued by one thread of rank 0.
+__device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+// Arrive once on the mbarrier at the same offset `bar` in both CTAs of the
+// pair when the pair MMAs issued so far by this thread complete.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"((unsigned short)3)
+        : "memory");
+}
+// 5-D tiled tensor copy into this CTA's shared memory whose byte count is
+// signalled on an mbarrier that may sit in either CTA of the pair
+// (`bar_cluster`: a shared::cluster address, e.g. from mapa_shared).
+__device__ __forceinline__ void tma_load_5d_pair(void* dst, const CUtensorMap* tm, uint32_t bar_cluster, int c0, int c1,
+                                                 int c2, int c3, int c4)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar_cluster)
+        : "memory");
 }
 
 __device__ __forceinline__ void red_add_f32(float* addr, float v)

@@ -15,6 +15,7 @@
 #include "k_depthwise.cuh"
 #include "k_dgrad.cuh"
 #include "k_igemm.cuh"
+#include "k_igemm_pair.cuh"
 #include "plan.h"
 
 static_assert(wg::kDgStaging == wg::kDgStagingBytes, "planner and kernel disagree on the dgrad staging size");
@@ -263,10 +264,12 @@ int prepare_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, v
     {
         const cuuint64_t dims[5] = {GK, (cuuint64_t)pb.out[2], (cuuint64_t)pb.out[1], (cuuint64_t)pb.out[0],
                                     (cuuint64_t)pb.N};
-        const cuuint32_t box[5] = {64, (cuuint32_t)ig.dy_w, (cuuint32_t)ig.box[1], (cuuint32_t)ig.box[2],
-                                   (cuuint32_t)ig.box[3]};
+        // A CTA of a pair stages 32 output channels (64-byte rows, 64-byte swizzle).
+        const cuuint32_t box[5] = {ig.pair ? 32u : 64u, (cuuint32_t)ig.dy_w, (cuuint32_t)ig.box[1],
+                                   (cuuint32_t)ig.box[2], (cuuint32_t)ig.box[3]};
         const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-        const int st = encode(&tmy, pb.in_dtype, const_cast<void*>(dy), dims, box, estr, CU_TENSOR_MAP_SWIZZLE_128B, "dY");
+        const int st = encode(&tmy, pb.in_dtype, const_cast<void*>(dy), dims, box, estr,
+                              ig.pair ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, "dY");
         if (st) return st;
     }
     wg::IgParams& prm = out->ig;
@@ -292,7 +295,8 @@ int prepare_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, v
     prm.patch_tx = ig.halo ? ig.patch[0] * ig.patch[1] * ig.patch[2] * ig.box[3] * 128 : ig.slot_bytes;
     prm.n_patches = ig.n_patches, prm.dy_off = ig.dy_off, prm.slot_bytes = ig.slot_bytes;
     prm.stage_bytes = ig.stage_bytes, prm.stages = ig.stages, prm.tmem_cols = ig.tmem_cols;
-    prm.idesc = wg::make_idesc_f16(pb.in_dtype == WG_BF16, true, true, 128, ig.Nmma);
+    prm.idesc = wg::make_idesc_f16(pb.in_dtype == WG_BF16, true, true, ig.pair ? 256 : 128, ig.Nmma);
+    prm.pair = ig.pair, prm.pair_xoff = ig.pair_xoff, prm.pair_xshift = ig.pair_xshift;
     prm.mode = pl.mode, prm.out_dtype = pb.out_dtype;
     prm.clq = ig.cluster;
     prm.staged = ig.staged;
@@ -336,8 +340,10 @@ int prepare_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, v
                 const int in = q / ig.box[2];
                 r[h] = (unsigned)(((in * ig.box[2] + id) * ig.box[1] + ih) * ig.dy_w + iw);
             }
+            // Rows of 128 bytes (eight 16-byte units), or 64 for a CTA pair's half.
+            const unsigned u = ig.pair ? 4u : 8u;
             prm.kd_table_b[ks] =
-                ((unsigned long long)((r[1] - r[0]) * 8u) << 32) + (unsigned long long)(r[0] * 8u);
+                ((unsigned long long)((r[1] - r[0]) * u) << 32) + (unsigned long long)(r[0] * u);
         }
     }
     if (ig.halo) {
@@ -469,16 +475,25 @@ int launch_pre(const wg::Plan& pl, void* dw, cudaStream_t stream)
 int launch_igemm_main(const wg::Plan& pl, const Prepared& pr, cudaStream_t stream)
 {
     const wg::IgemmPlan& ig = pl.ig;
-    auto kernel = ig.spec == 1 ? wg::igemm_wgrad_kernel<1> : wg::igemm_wgrad_kernel<0>;
+    auto kernel = ig.spec == 2   ? wg::igemm_wgrad_pair_kernel
+                  : ig.spec == 1 ? wg::igemm_wgrad_kernel<1>
+                                 : wg::igemm_wgrad_kernel<0>;
     const int st = ensure_smem(kernel, ig.smem_bytes);
     if (st) return st;
     // Consecutive splits form a cluster (grid z is a multiple of the cluster
-    // size); the kernel is a programmatic dependent of the kernel before it
-    // (the zeroing kernel in atomic mode).
+    // size), or the two M-ranges of a split do (CTA pair: grid x = 2); the
+    // kernel is a programmatic dependent of the kernel before it (the zeroing
+    // kernel in atomic mode).
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     unsigned na = 0;
-    if (ig.cluster > 1) {
+    if (ig.pair) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    } else if (ig.cluster > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
         attr[na].val.clusterDim.x = 1;
         attr[na].val.clusterDim.y = 1;

@@ -119,13 +119,21 @@ typedef struct {
  *              K = 64 into 64*X columns per MMA.  Needs stride 1, a k window
  *              that is a multiple of 64 (K, or K times the groups folded into
  *              one tile when C and K are small), 2 <= X <= 4 and no cluster;
- *              WG_ERR_NOT_SUPPORTED otherwise. */
+ *              WG_ERR_NOT_SUPPORTED otherwise.  One CTA per M-tile.
+ *  IGEMM_PAIR: the IGEMM_TAPS_MN tile with a split's two M-tiles on the two
+ *              CTAs of a thread-block cluster sharing M = 256 MMAs
+ *              (tcgen05 .cta_group::2), each CTA staging half of the output
+ *              channels of dY.  Needs what IGEMM_TAPS_MN needs, plus K = 64
+ *              with no group folding, C <= 64, a 2-D filter with 3 or 4 taps
+ *              along h; WG_ERR_NOT_SUPPORTED otherwise.  IGEMM and AUTO choose
+ *              between the forms by the planner's cost model. */
 typedef enum {
     WG_KERNEL_AUTO = 0,
     WG_KERNEL_IGEMM = 1,
     WG_KERNEL_DEPTHWISE = 2,
     WG_KERNEL_IGEMM_TAPS_M = 3,
-    WG_KERNEL_IGEMM_TAPS_MN = 4
+    WG_KERNEL_IGEMM_TAPS_MN = 4,
+    WG_KERNEL_IGEMM_PAIR = 5
 } wg_kernel;
 
 /* Per-call options (the CK page's k_batch, plus the two ways of combining splits).

@@ -94,10 +94,18 @@ def test_size_limits():
 
 
 def test_kernel_instance_choice():
-    # The trimmed instance serves x-taps-on-columns plans with one M-tile per
-    # CTA in a split mode; every other plan takes the general one.
+    # The CTA-pair kernel serves the pair plans (automatic for long splits:
+    # one or four splits of the 56x56 workload); the trimmed instance serves
+    # single-CTA x-taps-on-columns plans with one M-tile per CTA in a split
+    # mode (the 56x56 workload's automatic S = 75); every other plan takes the
+    # general one.
     dense = WORKLOADS["2d_dense_n32_h56_c64_k64"][0]
     assert binding.wg_plan_string(dense).endswith("code=x1")
+    assert binding.wg_plan_string(dense, 1, "direct").endswith("code=pair")
+    assert binding.wg_plan_string(dense, 4, "deterministic").endswith("code=pair")
+    assert binding.wg_plan_string(dense, kernel="igemm_pair").endswith("code=pair")
+    assert binding.wg_plan_string(dense, 1, "direct", kernel="igemm_pair").endswith("code=pair")
+    assert binding.wg_plan_string(dense, kernel="igemm_taps_mn").endswith("code=x1")
     direct = binding.wg_plan_string(dense, 1, "direct", kernel="igemm_taps_mn")
     assert "taps=mn" in direct and "mode=direct" in direct and direct.endswith("code=any")
     assert binding.wg_plan_string(dense, kernel="igemm_taps_m").endswith("code=any")
@@ -216,7 +224,7 @@ def test_kernel_selector():
     assert e.value.status == 2
     with pytest.raises(binding.WgradError) as e:
         lib_opts = binding.make_options()
-        lib_opts.kernel = 5
+        lib_opts.kernel = 6
         p = binding.make_problem(dense)
         import ctypes
         buf = ctypes.create_string_buffer(256)
@@ -252,6 +260,38 @@ def test_tap_form_selector():
     # Depthwise problems run on the tensor cores under either tap form selector.
     dw = WORKLOADS["2d_depthwise_g512_n64_h28"][0]
     assert "kernel=igemm_tcgen05" in binding.wg_plan_string(dw, kernel="igemm_taps_m")
+
+
+def test_pair_selector():
+    # The CTA-pair form: the x-taps-on-columns tile with K = 64 (no fold), one
+    # 64-channel chunk (C <= 64) and a 2-D filter of 3 or 4 rows: the split's
+    # two M-tiles on the two CTAs of a cluster (grid x = 2).
+    ok = [spec(2, 1, 2, 64, 64, [13, 11], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),
+          spec(2, 1, 2, 40, 64, [9, 14], [4, 3], [1, 1], [1, 2], [2, 1], [1, 1]),
+          spec(2, 2, 3, 64, 64, [7, 10], [3, 2], [1, 1], [2, 1], [2, 0], [2, 1]),
+          spec(2, 1, 1, 16, 64, [20, 19], [3, 4], [1, 1], [1, 1], [1, 2], [1, 1])]
+    for sp in ok:
+        for mode in ("auto", "deterministic", "direct"):
+            f = _plan_fields(binding.wg_plan_string(sp, 1 if mode == "direct" else 0, mode, kernel="igemm_pair"))
+            assert f["code"] == "pair" and f["taps"] == "mn" and f["mranges"] == "2" and f["mt_per_cta"] == "1", f
+            assert f["grid"].startswith("(2,") and f["Nmma"] == str(64 * sp["filt"][-1]), f
+    bad = [spec(2, 1, 2, 64, 128, [13, 11], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),  # K = 128
+           spec(2, 1, 2, 96, 64, [13, 11], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),   # C = 96: two chunks
+           spec(2, 1, 2, 64, 64, [13, 11], [2, 3], [1, 1], [1, 1], [1, 1], [1, 1]),   # 2 taps along h
+           spec(2, 1, 2, 64, 64, [13, 11], [5, 3], [1, 1], [1, 1], [2, 1], [2, 1]),   # 5 taps along h
+           spec(3, 1, 2, 64, 64, [5, 6, 7], [3, 3, 3], [1, 1, 1], [1, 1, 1], [1, 1, 1], [1, 1, 1]),  # 3-D
+           spec(1, 1, 3, 64, 64, [50], [3], [1], [1], [1], [1]),                        # 1-D
+           spec(2, 32, 2, 8, 8, [9, 10], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1]),     # folded groups
+           spec(2, 1, 2, 64, 64, [13, 11], [3, 3], [2, 2], [1, 1], [1, 1], [1, 1])]   # stride 2
+    for sp in bad:
+        with pytest.raises(binding.WgradError) as e:
+            binding.wg_plan_string(sp, kernel="igemm_pair")
+        assert e.value.status == 2, sp
+    with pytest.raises(binding.WgradError) as e:
+        binding.wg_plan_string(ok[0], 4, "deterministic", 0, cluster=2, kernel="igemm_pair")
+    assert e.value.status == 2
+    # The single-CTA selector never takes the pair.
+    assert _plan_fields(binding.wg_plan_string(ok[0], kernel="igemm_taps_mn"))["code"] != "pair"
 
 
 def test_dgrad_plans_and_limits():

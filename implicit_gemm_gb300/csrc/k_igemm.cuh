@@ -705,6 +705,37 @@ __global__ void __launch_bounds__(256) zero_f32_kernel(float* __restrict__ p, lo
     for (long long i = (n4 << 2) + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = 0.f;
 }
 
+// dW = cast(ws) after atomic accumulation of a 16-bit dW into the fp32
+// workspace ws (round to nearest even).  A programmatic dependent of the main
+// kernel: it may start at once and waits for that grid before reading.
+template <typename OUT>
+__global__ void __launch_bounds__(256) cast_f32_kernel(const float* __restrict__ ws, OUT* __restrict__ dw, long long n)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const long long n4 = n >> 2;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const float4* w4 = reinterpret_cast<const float4*>(ws);  // 16-byte aligned (checked on the host)
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+        const float4 v = w4[i];
+        OUT o[4];
+        if constexpr (std::is_same<OUT, __nv_bfloat16>::value) {
+            o[0] = __float2bfloat16_rn(v.x), o[1] = __float2bfloat16_rn(v.y);
+            o[2] = __float2bfloat16_rn(v.z), o[3] = __float2bfloat16_rn(v.w);
+        } else {
+            o[0] = __float2half_rn(v.x), o[1] = __float2half_rn(v.y);
+            o[2] = __float2half_rn(v.z), o[3] = __float2half_rn(v.w);
+        }
+        *reinterpret_cast<uint2*>(dw + 4 * i) = *reinterpret_cast<const uint2*>(o);  // dW 16-byte aligned
+    }
+    for (long long i = (n4 << 2) + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        if constexpr (std::is_same<OUT, __nv_bfloat16>::value)
+            dw[i] = __float2bfloat16_rn(ws[i]);
+        else
+            dw[i] = __float2half_rn(ws[i]);
+    }
+}
+
 // Stage 2 of the deterministic split-K mode (the two-stage wgrad that PR
 // #11602 and PR #12359 refer to): dW = cast(sum over splits of ws[s]) in a
 // fixed order that depends on S only: for S >= 8 the splits fall into four

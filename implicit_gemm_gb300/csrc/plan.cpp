@@ -135,11 +135,16 @@ long long epilogue_clk(long long dw_bytes, int n_out, int Q, long long red_bytes
 int cap_index(int q) { return q == 1 ? 0 : q == 2 ? 1 : q == 4 ? 2 : 3; }
 
 // Whether split partial sums are added with atomics: mode ATOMIC, or mode
-// AUTO with an fp32 dW (the fp32 atomic add writes dW directly; 16-bit dW
-// goes through the two-stage path).  On GB300 the atomic path -- a zeroing
-// kernel hidden behind the main loop, then one fp32 add per partial element
-// -- measured faster than the two-stage one (partials written, a second
-// kernel summing them) on every fp32 workload of the benchmark.
+// AUTO with an fp32 dW.  On GB300 the atomic path -- a zeroing kernel hidden
+// behind the main loop, then one fp32 add per partial element -- measured
+// faster than the two-stage one (partials written, a second kernel summing
+// them) on every fp32 workload of the benchmark (the 56x56 workload with S =
+// 75: 14.1 against 15.5 us).  A 16-bit dW takes the adds through an fp32 copy
+// in the workspace and a third kernel that casts it, one more grid completion
+// per call: 17.0 us there against 15.5 us two-stage, so AUTO keeps the
+// two-stage path for it.  (Casting in the main kernel instead, by the last
+// split CTA of each tile, put a 96 KB conversion by one CTA at the end of the
+// call: 43.5 us.)
 bool takes_atomic(const wg_options& o, const Problem& pb)
 {
     return o.mode == WG_MODE_ATOMIC || (o.mode == WG_MODE_AUTO && pb.out_dtype == WG_FP32);
@@ -734,8 +739,6 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
         return fail(err, WG_ERR_INVALID_ARGUMENT,
                     "mode DIRECT takes no split, or exactly one cluster of splits (split_k %d, cluster %d)", o.split_k,
                     o.cluster);
-    if (o.mode == WG_MODE_ATOMIC && pb.out_dtype != WG_FP32)
-        return fail(err, WG_ERR_NOT_SUPPORTED, "atomic split-K accumulates in fp32: dW must be WG_FP32");
     if (((long long)pb.G * pb.C * 2) % 16 || ((long long)pb.G * pb.K * 2) % 16)
         return fail(err, WG_ERR_NOT_SUPPORTED, "G*C and G*K must be multiples of 8 (16-byte pixel rows for TMA)");
     const bool depthwise = pb.C == 1 && pb.K == 1;
@@ -839,6 +842,9 @@ int make_plan(const wg_problem* p, const wg_options* opt, const DeviceCaps& caps
     pl->ws_bytes = pl->mode == MODE_DETERMINISTIC
                        ? (size_t)pl->ws_rows * pl->ws_nj * (size_t)n_out * pl->ws_W * 4
                        : 0;
+    // Atomic accumulation of a 16-bit dW: an fp32 copy of dW in the workspace.
+    pl->acc_ws = pl->mode == MODE_ATOMIC && pb.out_dtype != WG_FP32 ? 1 : 0;
+    if (pl->acc_ws) pl->ws_bytes = (size_t)((pb.dw_elems + 3) / 4) * 16;
     return WG_OK;
 }
 
@@ -859,7 +865,8 @@ std::string plan_string(const Plan& pl)
                  ig.halo ? "halo" : "pertap", ig.xs ? "mn" : "m", ig.Nmma, mode, pl.S, ig.cluster, ig.Gm, ig.n_gblocks, ig.n_cchunks, ig.Nt, ig.n_ntiles, ig.n_katoms, ig.box[0], ig.box[1],
                  ig.box[2], ig.box[3], ig.KT, ig.total_kt, pl.per_split, ig.n_atoms, ig.n_mtiles, ig.mt_per_cta,
                  ig.n_mranges, ig.tmem_cols, ig.stages, ig.stage_bytes, ig.smem_bytes, pl.grid[0], pl.grid[1],
-                 pl.grid[2], pl.block, pl.ws_bytes, pl.mode == MODE_DETERMINISTIC ? "kernel" : "none",
+                 pl.grid[2], pl.block, pl.ws_bytes,
+                 pl.mode == MODE_DETERMINISTIC ? "kernel" : pl.acc_ws ? "cast" : "none",
                  pl.mode == MODE_ATOMIC ? "kernel" : "none", ig.staged ? "staged" : "direct",
                  ig.spec == 2 ? "pair" : ig.spec ? "x1" : "any");
     } else {
@@ -871,7 +878,8 @@ std::string plan_string(const Plan& pl)
                  mode, pl.S, dw.Gm, dw.CB, dw.n_cblocks, dw.R, dw.nseg, dw.seg_len, dw.threads, dw.xw, dw.xh,
                  dw.total_tiles, pl.per_split, dw.stages, dw.stage_bytes, dw.smem_bytes, dw.sliding, pl.grid[0],
                  pl.grid[1], pl.grid[2], pl.block, pl.ws_bytes,
-                 pl.mode == MODE_DETERMINISTIC ? "kernel" : "none", pl.mode == MODE_ATOMIC ? "kernel" : "none");
+                 pl.mode == MODE_DETERMINISTIC ? "kernel" : pl.acc_ws ? "cast" : "none",
+                 pl.mode == MODE_ATOMIC ? "kernel" : "none");
     }
     (void)pb;
     return buf;

@@ -118,6 +118,9 @@ struct Plan {
     int kind;
     int mode;
     int S;              // split degree of GemmK
+    // Atomic mode with a 16-bit dW: the splits add into an fp32 copy of dW in
+    // the workspace (zeroed first), which a cast kernel then converts to dW.
+    int acc_ws;
     long long per_split;  // K-tiles (igemm) or row tiles (depthwise) per split
     int n_out;          // partial sums per dW element that reach memory (S / cluster)
     long long ws_rows, ws_L;

@@ -310,7 +310,7 @@ int prepare_igemm(const wg::Plan& pl, const void* x, const void* dy, void* dw, v
             prm.atom_of[(tap / xe) * ig.n_cchunks + cc] = (unsigned char)i;
         }
     }
-    prm.out = pl.mode == wg::MODE_DETERMINISTIC ? ws : dw;
+    prm.out = pl.mode == wg::MODE_DETERMINISTIC || pl.acc_ws ? ws : dw;
     prm.ws = ws_layout(pl);
     // K-step descriptor parts: pixel row r of the tile (w fastest) sits at patch
     // row ((in*PD + id)*PH + ih)*PW + iw of a halo patch, at row r of a per-tap box.
@@ -441,8 +441,9 @@ int launch_reduce(const wg::Plan& pl, void* ws, void* dw, cudaStream_t stream)
     return WG_OK;
 }
 
-// A call runs as launch_pre (zero dW for atomic accumulation), the main kernel
-// (launch_main), then launch_post (the mark event, then the split reduction).
+// A call runs as launch_pre (zero dW, or its fp32 copy in the workspace, for
+// atomic accumulation), the main kernel (launch_main), then launch_post (the
+// mark event, then the split reduction or the cast of the fp32 copy).
 // The zeroing is a kernel of this library rather than cudaMemsetAsync: the main
 // kernel is launched as its programmatic dependent and waits for it only
 // before its atomic adds (a memset before the main kernel measured ~4 us per
@@ -455,9 +456,11 @@ int launch_reduce(const wg::Plan& pl, void* ws, void* dw, cudaStream_t stream)
 // may write; its launch and set-up (barriers, tensor-map prefetch) overlap
 // that kernel's tail.  A kernel before it that was not launched this way, or
 // a copy or event between them, gives ordinary stream order.
-int launch_pre(const wg::Plan& pl, void* dw, cudaStream_t stream)
+int launch_pre(const wg::Plan& pl, void* ws, void* dw, cudaStream_t stream)
 {
     if (pl.mode == wg::MODE_ATOMIC) {
+        // The adds go to dW, or (16-bit dW) to its fp32 copy in the workspace.
+        float* acc = static_cast<float*>(pl.acc_ws ? ws : dw);
         const long long n = pl.pb.dw_elems;
         const long long blocks = std::max(1LL, std::min<long long>((n / 4 + 255) / 256, 4LL * num_sms()));
         cudaLaunchConfig_t cfg = {};
@@ -466,7 +469,7 @@ int launch_pre(const wg::Plan& pl, void* dw, cudaStream_t stream)
         pdl_config(&cfg, attr, &na, stream);
         cfg.gridDim = dim3((unsigned)blocks);
         cfg.blockDim = dim3(256);
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, wg::zero_f32_kernel, static_cast<float*>(dw), n);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, wg::zero_f32_kernel, acc, n);
         if (e != cudaSuccess) return cuda_fail("zero_f32_kernel launch", e);
     }
     return WG_OK;
@@ -516,6 +519,22 @@ int launch_post(const wg::Plan& pl, void* ws, void* dw, cudaStream_t stream)
         if (e != cudaSuccess) return cuda_fail("cudaEventRecord(mark)", e);
     }
     if (pl.mode == wg::MODE_DETERMINISTIC) return launch_reduce(pl, ws, dw, stream);
+    if (pl.acc_ws) {
+        const long long n = pl.pb.dw_elems;
+        const long long blocks = std::max(1LL, std::min<long long>((n / 4 + 255) / 256, 4LL * num_sms()));
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        unsigned na = 0;
+        pdl_config(&cfg, attr, &na, stream);
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(256);
+        const float* src = static_cast<const float*>(ws);
+        const cudaError_t e =
+            pl.pb.out_dtype == WG_BF16
+                ? cudaLaunchKernelEx(&cfg, wg::cast_f32_kernel<__nv_bfloat16>, src, static_cast<__nv_bfloat16*>(dw), n)
+                : cudaLaunchKernelEx(&cfg, wg::cast_f32_kernel<__half>, src, static_cast<__half*>(dw), n);
+        if (e != cudaSuccess) return cuda_fail("cast_f32_kernel launch", e);
+    }
     return WG_OK;
 }
 
@@ -594,7 +613,7 @@ int prepare_depthwise(const wg::Plan& pl, const void* x, const void* dy, void* d
     prm.x_bytes_al = (d.x_bytes + 127) / 128 * 128;
     prm.x_tx = d.x_bytes, prm.dy_tx = d.dy_bytes;
     prm.mode = pl.mode, prm.out_dtype = pb.out_dtype;
-    prm.out = pl.mode == wg::MODE_DETERMINISTIC ? ws : dw;
+    prm.out = pl.mode == wg::MODE_DETERMINISTIC || pl.acc_ws ? ws : dw;
     prm.ws = ws_layout(pl);
     return WG_OK;
 }
@@ -608,7 +627,7 @@ int launch_depthwise_main(const wg::Plan& pl, const Prepared& pr, cudaStream_t s
 
 int launch_call(const wg::Plan& pl, const Prepared& pr, void* dw, void* ws, cudaStream_t stream)
 {
-    int st = launch_pre(pl, dw, stream);
+    int st = launch_pre(pl, ws, dw, stream);
     if (!st)
         st = pl.kind == wg::KIND_IGEMM ? launch_igemm_main(pl, pr, stream) : launch_depthwise_main(pl, pr, stream);
     if (!st) st = launch_post(pl, ws, dw, stream);
@@ -849,7 +868,9 @@ int wg_conv_bwd_weight_noalloc(const wg_problem* p, const void* x, const void* d
         // Automatic split degree: the largest that fits the scratch array.  One
         // partial sum per cluster of Q splits reaches the workspace, so Q * fit
         // splits fit; when not even two partials fit, one split (direct mode,
-        // no workspace).
+        // no workspace).  (An automatic mode whose atomic path needs an fp32
+        // copy of a 16-bit dW larger than the array takes the two-stage path.)
+        if (o.mode == WG_MODE_AUTO) o.mode = WG_MODE_DETERMINISTIC;
         wg::Plan pl1;
         wg_options o1 = o;
         o1.split_k = 1;

@@ -55,8 +55,10 @@ typedef enum { WG_BF16 = 0, WG_FP16 = 1, WG_FP32 = 2 } wg_dtype;
  *  ATOMIC:        dW is zeroed on the stream first (the Preprocess memset of the
  *                 CK page; here a kernel whose successor, the split-K kernel,
  *                 waits for it only before its first add), then every split
- *                 adds its fp32 partial with a global atomic.  fp32 dW only.
- *                 Not bitwise reproducible.
+ *                 adds its fp32 partial with a global atomic.  A 16-bit dW is
+ *                 accumulated the same way in an fp32 copy in the workspace
+ *                 (4 bytes per dW element), which a last kernel casts (round
+ *                 to nearest even) to dW.  Not bitwise reproducible.
  *  DETERMINISTIC: two-stage: every split writes an fp32 partial to the
  *                 workspace, then a second kernel sums the splits in a fixed
  *                 order (for S >= 8: four contiguous ranges of splits, each in
@@ -64,8 +66,9 @@ typedef enum { WG_BF16 = 0, WG_FP16 = 1, WG_FP32 = 2 } wg_dtype;
  *                 index order) and casts (round to nearest even) to dW.
  *                 Bitwise reproducible for a given problem and split degree.
  *  AUTO:          DIRECT when the chosen split degree is 1; otherwise ATOMIC
- *                 for an fp32 dW (measured the faster of the two on GB300)
- *                 and DETERMINISTIC for a 16-bit dW.  Ask for DETERMINISTIC
+ *                 for an fp32 dW and DETERMINISTIC for a 16-bit dW (each
+ *                 measured the faster for its dtype on GB300: the 16-bit
+ *                 atomic path has one more kernel).  Ask for DETERMINISTIC
  *                 explicitly when bitwise reproducibility matters. */
 typedef enum {
     WG_MODE_AUTO = 0,
@@ -173,7 +176,9 @@ WG_API int wg_problem_normalize(wg_problem* p);
  * wgrad_two_stage_workspace_nbytes) states it.  0 unless the chosen mode is
  * DETERMINISTIC with more than one partial sum reaching memory, where it is
  * (partials) * G*K*Z*Y*X*C * 4 bytes, each (g, k) row of Z*Y*X*C rounded up to
- * whole reduction slices.  opt may be NULL (all defaults).
+ * whole reduction slices, or ATOMIC with a 16-bit dW, where it is the fp32
+ * copy of dW (G*K*Z*Y*X*C rounded up to a multiple of 4, times 4 bytes).
+ * opt may be NULL (all defaults).
  * Returns WG_OK, WG_ERR_INVALID_ARGUMENT or WG_ERR_NOT_SUPPORTED.  Host only. */
 WG_API int wg_workspace_size(const wg_problem* p, const wg_options* opt, size_t* bytes);
 

@@ -68,9 +68,9 @@ def test_not_supported_paths():
         binding.wg_workspace_size(s)
     assert e.value.status == 2
     s = spec(2, 1, 1, 16, 16, [8, 8], [3, 3], [1, 1], [1, 1], [1, 1], [1, 1], out_dtype="bf16")
-    with pytest.raises(binding.WgradError) as e:
-        binding.wg_workspace_size(s, split_k=2, mode="atomic")  # fp32 atomics only
-    assert e.value.status == 2
+    # Atomic adds into a 16-bit dW go through an fp32 copy in the workspace.
+    assert binding.wg_workspace_size(s, split_k=2, mode="atomic") == 16 * 9 * 16 * 4
+    assert binding.wg_workspace_size(s, split_k=2, mode="deterministic") == 2 * 16 * 9 * 16 * 4
     with pytest.raises(binding.WgradError) as e:
         binding.wg_workspace_size(s, group_merge=2)  # merge degree is a depthwise option
     assert e.value.status == 2

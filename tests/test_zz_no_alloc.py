@@ -85,7 +85,8 @@ def test_noalloc_matches_regular_entry_twice(name, sp, split_k, mode, gm):
         assert_close(got_np, ref_dw, A, sp["out_dtype"], f"{name} call {call} against the oracle")
         if first is None:
             first = got_np
-        else:
+        elif "mode=atomic" not in binding.wg_plan_string(sp, split_k, mode, gm):
+            # the same bits again (atomic adds may sum in another order)
             np.testing.assert_array_equal(got_np, first)
 
 

@@ -301,18 +301,20 @@ L2_BYTES = 129 * 1000 * 1000
 # such a capture reports null.  ncu flushes the caches before the captured
 # launch, so atomic plans also count the dW lines their atomic adds fetch.
 TRAFFIC = {
-    # igemm_wgrad_kernel<1> (x taps on the columns, one M-tile), S = 75 two-stage: 25,775,872 B read + 0 B written.
-    "2d_dense_n32_h56_c64_k64": 25_775_872,
-    # igemm_wgrad_kernel<0>, Gm = 8 fold, 32 x 4 pixel tiles, staged atomic output: 25,854,464 B read + 0 B written.
-    "2d_grouped_g32_c8_k8_n32_h28": 25_854_464,
+    # igemm_wgrad_kernel<1> (x taps on the columns, one M-tile), S = 75 two-stage: 25,776,384 B read + 0 B written.
+    "2d_dense_n32_h56_c64_k64": 25_776_384,
+    # igemm_wgrad_pair_kernel (CTA pairs), S = 4 two-stage: 25,751,552 B read + 0 B written.
+    "2d_dense_n32_h56_c64_k64/S4_deterministic": 25_751_552,
+    # igemm_wgrad_kernel<0>, Gm = 8 fold, 32 x 4 pixel tiles, staged atomic output: 25,854,720 B read + 0 B written.
+    "2d_grouped_g32_c8_k8_n32_h28": 25_854_720,
     # depthwise_wgrad_kernel<bf16, 2, sliding>, atomic: 103,135,744 B read + 3,367,680 B written.
     "2d_depthwise_g512_n64_h28": 106_503_424,
-    # igemm_wgrad_kernel<0>, per-tap S = 4 atomic: 6,010,880 B read (X + dY + the dW lines) + 0 B written.
-    "3d_n4_d16_c128_k96_s2/auto": 6_010_880,
-    # igemm_wgrad_kernel<0>, S = 87 atomic: 64,386,816 B read + 195,840 B written.
-    "2d_1x1_n32_h56_c64_k256": 64_582_656,
-    # igemm_wgrad_kernel<0>, per-tap S = 49 atomic: 19,494,656 B read + 0 B written.
-    "2d_1x1s2_n32_h56_c256_k128": 19_494_656,
+    # igemm_wgrad_kernel<0>, per-tap S = 4 atomic: 6,010,624 B read (X + dY + the dW lines) + 0 B written.
+    "3d_n4_d16_c128_k96_s2/auto": 6_010_624,
+    # igemm_wgrad_kernel<0>, S = 87 atomic: 64,386,304 B read + 308,480 B written.
+    "2d_1x1_n32_h56_c64_k256": 64_694_784,
+    # igemm_wgrad_kernel<0>, per-tap S = 49 atomic: 19,497,472 B read + 0 B written.
+    "2d_1x1s2_n32_h56_c256_k128": 19_497_472,
 }
 MAX_COPIES = 512
 

@@ -370,7 +370,9 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
                 const long long mma_clk = std::max((long long)mt * ksteps * mma_one, mn ? smem_clk : 0LL);
                 const long long load_clk = stage1 / 40;
                 long long tile_clk = std::max(mma_clk, load_clk) + 64;
-                if ((pr ? stages : std::min(8, (int)(avail / stage1))) < 3) tile_clk = tile_clk * 13 / 10;
+                // Fewer than 3 stages exposes the refill latency -- when the
+                // split has more K-tiles than the ring holds (below).
+                const bool few_stages = (pr ? stages : std::min(8, (int)(avail / stage1))) < 3;
                 // The CTA pair halves each SM's operand reads of B and its dY
                 // loads, but on the 56x56 workload its K-tile measured only
                 // 3.5% shorter than the single CTA's (0.804 against 0.833 us
@@ -403,7 +405,14 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
                     // The per-CTA estimate also breaks ties between tilings whose
                     // main loops all sit under the HBM bound (with weight 1/8).
                     const long long waves = cdiv(base * S, cp.cluster_ctas[0]);
-                    const long long main_clk = waves * cdiv(ktiles, S) * tile_clk;
+                    // A split whose K-tiles all fit the ring issues every load at
+                    // once: no refill waits (3-D stride 2, S = 8: two 128-pixel
+                    // K-tiles in two stages, 11.9 us atomic and 15.0 us two-stage,
+                    // against four 64-pixel K-tiles of six 8 KB boxes, ~1.5 us
+                    // each, that the penalty used to pick: 14.5 and 17.7 us).
+                    const long long kper = cdiv(ktiles, S);
+                    const long long tclk = few_stages && kper > stages ? tile_clk * 13 / 10 : tile_clk;
+                    const long long main_clk = waves * kper * tclk;
                     const long long cost = std::max(main_clk, dram_clk) + main_clk / 8 + (pr ? kPairCallClk : 0) +
                                            epilogue_clk(pb.dw_elems * 4, (int)S, 1, red_bytes, atomic_sum);
                     // With the x taps on the columns, ties go to the fewer TMA
@@ -424,7 +433,7 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
                         c.pair = pr;
                         c.tx_bytes = written;
                         c.cost = cost;
-                        c.tile_clk = tile_clk;
+                        c.tile_clk = tclk;
                         c.S = S;
                         best = c;
                     }

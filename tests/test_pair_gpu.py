@@ -90,12 +90,44 @@ def test_pair_all_modes(sp):
     x, dy = make_inputs(sp, ("uniform", -1.0, 1.0), 81, 82)
     dw, A = ref(sp, x, dy)
     for split_k, mode in MODES:
-        if mode == "atomic" and sp["out_dtype"] != "fp32":
-            continue
         plan = binding.wg_plan_string(sp, split_k, mode, 0, kernel="igemm_pair")
         assert plan.endswith("code=pair"), plan
         got = run_gpu(sp, x, dy, split_k, mode)
         assert_close(got, dw, A, sp["out_dtype"], f"{_ids(sp)} S={split_k} {mode}: {plan}")
+
+
+def _random_pair_problems(count, seed):
+    # Seeded random problems the pair form admits: 2-D, stride 1, K = 64 (no
+    # group fold), C <= 64, 3 or 4 filter rows, 2-4 columns.
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        G = int(rng.choice([1, 1, 2, 3]))
+        C = int(rng.choice([8, 16, 24, 32, 40, 56, 64]))
+        if (G * C) % 8:
+            continue
+        filt = [int(rng.choice([3, 4])), int(rng.choice([2, 3, 4]))]
+        dil = [int(rng.choice([1, 1, 2])), int(rng.choice([1, 1, 2]))]
+        inn = [int(rng.integers(filt[i] * dil[i], 24)) for i in range(2)]
+        pl = [int(rng.integers(0, filt[i])) for i in range(2)]
+        pr = [int(rng.integers(0, filt[i])) for i in range(2)]
+        sp = spec(2, G, int(rng.integers(1, 4)), C, 64, inn, filt, [1, 1], dil, pl, pr,
+                  str(rng.choice(["bf16", "fp16"])), str(rng.choice(["fp32", "bf16", "fp16"])))
+        try:
+            binding.wg_plan_string(sp, 0, "auto", 0, kernel="igemm_pair")
+        except binding.WgradError:
+            continue
+        out.append(sp)
+    return out
+
+
+def test_pair_random_problems():
+    for sp in _random_pair_problems(12, 4242):
+        x, dy = make_inputs(sp, ("uniform", -1.0, 1.0), 85, 86)
+        dw, A = ref(sp, x, dy)
+        for split_k, mode in ((0, "auto"), (1, "direct"), (7, "deterministic"), (3, "atomic")):
+            got = run_gpu(sp, x, dy, split_k, mode)
+            assert_close(got, dw, A, sp["out_dtype"], f"{_ids(sp)} S={split_k} {mode}")
 
 
 @pytest.mark.parametrize("sp", [CASES[i] for i in (0, 1, 2, 3, 4, 6, 8, 10)], ids=_ids)

@@ -1,8 +1,9 @@
 """GPU parity on seeded random problems: 1-, 2- and 3-D, strides, dilations,
 asymmetric pads, groups (folded or not), depthwise, 16-bit and fp32 dW, through
 every kernel selector that accepts the problem (automatic, every tap on the MMA
-rows, the x taps on the columns, the depthwise kernel) in the automatic,
-direct and deterministic split modes, each compared with the fp64 oracle.
+rows, the x taps on the columns, their CTA-pair form, the depthwise kernel) in
+the automatic, direct, deterministic and atomic split modes (a 16-bit dW
+through its fp32 copy and the cast kernel), each compared with the fp64 oracle.
 """
 import numpy as np
 import pytest
@@ -81,8 +82,8 @@ def test_random_problem_every_kernel(sp):
     dt = sp["in_dtype"]
     dw, A = oracle.wgrad(sp, oracle.decode(x, dt), oracle.decode(dy, dt))
     ran = 0
-    for kernel in ("auto", "igemm_taps_m", "igemm_taps_mn", "depthwise"):
-        for split_k, mode in ((0, "auto"), (1, "direct"), (6, "deterministic")):
+    for kernel in ("auto", "igemm_taps_m", "igemm_taps_mn", "igemm_pair", "depthwise"):
+        for split_k, mode in ((0, "auto"), (1, "direct"), (6, "deterministic"), (5, "atomic")):
             try:
                 plan = binding.wg_plan_string(sp, split_k, mode, 0, kernel=kernel)
             except binding.WgradError as e:

@@ -380,9 +380,8 @@ int plan_igemm(Plan* pl, const wg_options& o, const DeviceCaps& caps, std::strin
                 // rather than the SM bounds the loop), and its cluster launch,
                 // barriers and paired TMEM release cost ~1 us per call
                 // (kPairCallClk, added to the call's cost below): it pays for
-                // long splits only (S = 1
-                // and 4: 360 and 97 us against 373 and 99; S = 38 and 75:
-                // 20.1 and 16.2 us against 19.1 and 15.5).
+                // long splits only (S = 1 and 4: 360 and 97 us against 373 and
+                // 99; S = 38 and 75: 20.1 and 16.2 us against 19.1 and 15.5).
                 if (pr) tile_clk = tile_clk * 965 / 1000;
                 // Whole-call estimate for the split degrees this tiling may get
                 // (the caller's; else enough splits to fill the device once, or

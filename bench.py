@@ -309,6 +309,8 @@ TRAFFIC = {
     "2d_grouped_g32_c8_k8_n32_h28": 25_854_720,
     # depthwise_wgrad_kernel<bf16, 2, sliding>, atomic: 103,135,744 B read + 3,367,680 B written.
     "2d_depthwise_g512_n64_h28": 106_503_424,
+    # igemm_wgrad_kernel<0>, per-tap S = 8 atomic (two 128-pixel K-tiles per split): 6,015,744 B read + 0 B written.
+    "3d_n4_d16_c128_k96_s2": 6_015_744,
     # igemm_wgrad_kernel<0>, per-tap S = 4 atomic: 6,010,624 B read (X + dY + the dW lines) + 0 B written.
     "3d_n4_d16_c128_k96_s2/auto": 6_010_624,
     # igemm_wgrad_kernel<0>, S = 87 atomic: 64,386,304 B read + 308,480 B written.

@@ -718,15 +718,17 @@ __global__ void __launch_bounds__(256) cast_f32_kernel(const float* __restrict__
     const float4* w4 = reinterpret_cast<const float4*>(ws);  // 16-byte aligned (checked on the host)
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
         const float4 v = w4[i];
-        OUT o[4];
+        unsigned short b[4];
         if constexpr (std::is_same<OUT, __nv_bfloat16>::value) {
-            o[0] = __float2bfloat16_rn(v.x), o[1] = __float2bfloat16_rn(v.y);
-            o[2] = __float2bfloat16_rn(v.z), o[3] = __float2bfloat16_rn(v.w);
+            b[0] = __bfloat16_as_ushort(__float2bfloat16_rn(v.x)), b[1] = __bfloat16_as_ushort(__float2bfloat16_rn(v.y));
+            b[2] = __bfloat16_as_ushort(__float2bfloat16_rn(v.z)), b[3] = __bfloat16_as_ushort(__float2bfloat16_rn(v.w));
         } else {
-            o[0] = __float2half_rn(v.x), o[1] = __float2half_rn(v.y);
-            o[2] = __float2half_rn(v.z), o[3] = __float2half_rn(v.w);
+            b[0] = __half_as_ushort(__float2half_rn(v.x)), b[1] = __half_as_ushort(__float2half_rn(v.y));
+            b[2] = __half_as_ushort(__float2half_rn(v.z)), b[3] = __half_as_ushort(__float2half_rn(v.w));
         }
-        *reinterpret_cast<uint2*>(dw + 4 * i) = *reinterpret_cast<const uint2*>(o);  // dW 16-byte aligned
+        // Four 16-bit values as one 8-byte store (dW is 16-byte aligned).
+        const uint2 packed = make_uint2((unsigned)b[0] | ((unsigned)b[1] << 16), (unsigned)b[2] | ((unsigned)b[3] << 16));
+        *reinterpret_cast<uint2*>(dw + 4 * i) = packed;
     }
     for (long long i = (n4 << 2) + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
         if constexpr (std::is_same<OUT, __nv_bfloat16>::value)

@@ -113,6 +113,25 @@ def test_kernel_instance_choice():
         assert binding.wg_plan_string(WORKLOADS[name][0]).endswith("code=any"), name
 
 
+def test_planner_measured_choices():
+    # Choices the planner makes because they measured faster on GB300: the
+    # 3-D stride-2 split-K = 8 mode takes two 128-pixel K-tiles per split in a
+    # two-stage ring (no refill), not four 64-pixel ones; the 8x8 problem runs
+    # five CTAs of one M-tile, not two of three; the 56x56 listed non-split and
+    # split-K = 4 modes run on CTA pairs with the x taps on the columns, and
+    # its automatic split degree on single CTAs.
+    f = _plan_fields(binding.wg_plan_string(WORKLOADS["3d_n4_d16_c128_k96_s2"][0], 8, "atomic"))
+    assert (f["KT"], f["per_split"], f["stages"], f["mt_per_cta"]) == ("128", "2", "2", "2"), f
+    f = _plan_fields(binding.wg_plan_string(WORKLOADS["2d_tiny_n1_h8_c16_k32"][0]))
+    assert (f["mt_per_cta"], f["grid"]) == ("1", "(5,1,1)"), f
+    dense = WORKLOADS["2d_dense_n32_h56_c64_k64"][0]
+    for S, mode in ((1, "direct"), (4, "deterministic")):
+        f = _plan_fields(binding.wg_plan_string(dense, S, mode))
+        assert (f["taps"], f["code"]) == ("mn", "pair"), (S, f)
+    f = _plan_fields(binding.wg_plan_string(dense))
+    assert (f["taps"], f["code"], f["S"]) == ("mn", "x1", "75"), f
+
+
 def test_workspace_sizes():
     sp = WORKLOADS["2d_dense_n32_h56_c64_k64"][0]
     E = 1 * 64 * 9 * 64  # rows of 576 = 6 slices of 96: no padding
